@@ -1,0 +1,416 @@
+/*
+ * oracle.c -- plain, slow, obviously correct CPU oracle (fp64).
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg, never by the product library.  No code,
+ * header or table is shared with the CUDA path.
+ *
+ * What it follows:
+ *  - OUT_PROD ("metal: OUT_PROD runs batched, broadcast and narrow shapes on
+ *    the GPU", review comment, first bullet): dst has shape
+ *    {a.ne0, b.ne0, b.ne2, b.ne3}; b.ne2 % a.ne2 == 0 and b.ne3 % a.ne3 == 0
+ *    are required; dst slice (i2, i3) reads src0 slice (i2/dps2, i3/dps3)
+ *    with dps2 = ne12/ne02, dps3 = ne13/ne03 (the CPU backend's slice map,
+ *    also named in the PR description's "per-slice helper" paragraph).
+ *    Per slice: dst[m,n] = sum_k a[m,k] * b[n,k].
+ *  - q8_0 src0 ("metal: OUT_PROD multiplies in float staging", Test
+ *    paragraph, q8_0 weights): blocks of 32 with an fp16 scale d and int8
+ *    values q, element = d*q.  q4_0: fp16 scale d, 4-bit values v,
+ *    element = d*(v-8); byte j of the 16 packed bytes holds element j in its
+ *    low nibble and element j+16 in its high nibble.
+ *  - MUL_MAT_ID_BACK ("Metal kernel_mul_mat_id_back", first bullet): for
+ *    each routed slot (i, t) with expert e = ids[i,t],
+ *    dx[k,i,t] = sum_r W_e[k,r] * g[r,i,t].
+ *  - The fp16 staging defect ("metal: OUT_PROD multiplies in float staging",
+ *    opening paragraph): inputs staged through half overflow past 65504.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define QK 32
+
+/* ------------------------------------------------------------------ */
+/* scalar decoders, written from the IEEE 754 binary16 definition      */
+/* ------------------------------------------------------------------ */
+
+double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int exp = (h >> 10) & 0x1f;
+    int mant = h & 0x3ff;
+    double v;
+    if (exp == 0) {
+        v = ldexp((double)mant, -24);               /* subnormal / zero */
+    } else if (exp == 31) {
+        v = mant ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + mant), exp - 25); /* (1.mant) * 2^(exp-15) */
+    }
+    return sign ? -v : v;
+}
+
+double oracle_bf16_to_double(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+double oracle_round_to_half(double x)
+{
+    if (isnan(x)) return x;
+    double ax = fabs(x);
+    /* 65504 is the largest finite half; its ulp is 32, so anything at or
+     * above 65504 + 16 rounds (ties-to-even goes up, 65504 is odd) to Inf. */
+    if (ax >= 65520.0) return x < 0 ? -INFINITY : INFINITY;
+    if (ax == 0.0) return x;
+    int e;
+    frexp(ax, &e);                 /* ax = f * 2^e, f in [0.5, 1) */
+    int unbiased = e - 1;          /* ax in [2^unbiased, 2^(unbiased+1)) */
+    if (unbiased < -14) unbiased = -14;   /* subnormal spacing */
+    double quantum = ldexp(1.0, unbiased - 10);
+    double r = nearbyint(ax / quantum) * quantum;   /* ties to even */
+    return x < 0 ? -r : r;
+}
+
+static uint16_t rd16(const uint8_t *p)
+{
+    return (uint16_t)(p[0] | ((uint16_t)p[1] << 8));
+}
+
+static int64_t row_bytes(int type, int64_t n)
+{
+    switch (type) {
+    case ORACLE_F32: return 4 * n;
+    case ORACLE_F16:
+    case ORACLE_BF16: return 2 * n;
+    case ORACLE_Q8_0: return n / QK * 34;
+    case ORACLE_Q4_0: return n / QK * 18;
+    default: return -1;
+    }
+}
+
+/* One element j of a row of `type`. */
+static double elem(int type, const uint8_t *row, int64_t j)
+{
+    switch (type) {
+    case ORACLE_F32: {
+        float f;
+        memcpy(&f, row + 4 * j, 4);
+        return (double)f;
+    }
+    case ORACLE_F16:
+        return oracle_half_to_double(rd16(row + 2 * j));
+    case ORACLE_BF16:
+        return oracle_bf16_to_double(rd16(row + 2 * j));
+    case ORACLE_Q8_0: {
+        const uint8_t *blk = row + (j / QK) * 34;
+        double d = oracle_half_to_double(rd16(blk));
+        int8_t q = (int8_t)blk[2 + j % QK];
+        return d * (double)q;
+    }
+    case ORACLE_Q4_0: {
+        const uint8_t *blk = row + (j / QK) * 18;
+        double d = oracle_half_to_double(rd16(blk));
+        int jj = (int)(j % QK);
+        uint8_t byte = blk[2 + (jj & 15)];
+        int v = jj < 16 ? (byte & 0x0f) : (byte >> 4);
+        return d * (double)(v - 8);
+    }
+    default:
+        return NAN;
+    }
+}
+
+int oracle_dequant_row(int type, const void *row, int64_t n, double *out)
+{
+    if (!row || !out || n < 0 || row_bytes(type, n) < 0) return -1;
+    if ((type == ORACLE_Q8_0 || type == ORACLE_Q4_0) && n % QK) return -1;
+    for (int64_t j = 0; j < n; ++j) out[j] = elem(type, (const uint8_t *)row, j);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* OUT_PROD                                                           */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int64_t M, K, N, ne02, ne03, ne12, ne13, dps2, dps3, rb;
+} shape_t;
+
+static int check_shape(int a_type, const int64_t ne_a[4], const int64_t ne_b[4],
+                       shape_t *s)
+{
+    if (!ne_a || !ne_b) return -1;
+    for (int i = 0; i < 4; ++i)
+        if (ne_a[i] < 0 || ne_b[i] < 0) return -1;
+    s->M = ne_a[0]; s->K = ne_a[1]; s->ne02 = ne_a[2]; s->ne03 = ne_a[3];
+    s->N = ne_b[0]; s->ne12 = ne_b[2]; s->ne13 = ne_b[3];
+    if (ne_b[1] != s->K) return -1;
+    if (s->ne02 == 0 || s->ne03 == 0) return -1;
+    if (s->ne12 % s->ne02 || s->ne13 % s->ne03) return -1;
+    s->dps2 = s->ne12 / s->ne02;
+    s->dps3 = s->ne13 / s->ne03;
+    if (a_type == ORACLE_Q8_0 || a_type == ORACLE_Q4_0) {
+        if (s->M % QK) return -1;
+    } else if (a_type != ORACLE_F32 && a_type != ORACLE_F16 && a_type != ORACLE_BF16) {
+        return -1;
+    }
+    s->rb = row_bytes(a_type, s->M);
+    return 0;
+}
+
+static void set_threads(int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/* a row (all M elements) for reduction index k of src0 slice (j2, j3) */
+static const uint8_t *a_row(const void *a, const shape_t *s, int64_t k,
+                            int64_t j2, int64_t j3)
+{
+    int64_t r = (j3 * s->ne02 + j2) * s->K + k;
+    return (const uint8_t *)a + r * s->rb;
+}
+
+static double b_at(const float *b, const shape_t *s, int64_t n, int64_t k,
+                   int64_t i2, int64_t i3)
+{
+    return (double)b[((i3 * s->ne12 + i2) * s->K + k) * s->N + n];
+}
+
+static int out_prod_impl(const void *a, int a_type, const float *b,
+                         const int64_t ne_a[4], const int64_t ne_b[4],
+                         float *dst, double *dst_f64, double *abssum,
+                         int nthreads, int half_staged)
+{
+    shape_t s;
+    if (check_shape(a_type, ne_a, ne_b, &s)) return -1;
+    if (!dst && !dst_f64 && !abssum) return -1;
+    const int64_t nslice = s.ne12 * s.ne13;
+    if (s.M == 0 || s.N == 0 || nslice == 0) return 0;
+    if ((!a || !b) && s.K > 0) return -1;
+    set_threads(nthreads);
+
+    /* One work item per (slice, n): every dst element has one writer and its
+     * sum runs over k in ascending order. */
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)s.M * sizeof(double));
+        double *sab = (double *)malloc((size_t)s.M * sizeof(double));
+        double *arow = (double *)malloc((size_t)s.M * sizeof(double));
+        if (!acc || !sab || !arow) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t w = 0; w < nslice * s.N; ++w) {
+            if (!acc || !sab || !arow) continue;
+            const int64_t n = w % s.N;
+            const int64_t sl = w / s.N;
+            const int64_t i2 = sl % s.ne12, i3 = sl / s.ne12;
+            const int64_t j2 = i2 / s.dps2, j3 = i3 / s.dps3;
+            for (int64_t m = 0; m < s.M; ++m) acc[m] = sab[m] = 0.0;
+            for (int64_t k = 0; k < s.K; ++k) {
+                const uint8_t *row = a_row(a, &s, k, j2, j3);
+                for (int64_t m = 0; m < s.M; ++m) arow[m] = elem(a_type, row, m);
+                double y = b_at(b, &s, n, k, i2, i3);
+                if (half_staged) {
+                    y = oracle_round_to_half(y);
+                    for (int64_t m = 0; m < s.M; ++m)
+                        arow[m] = oracle_round_to_half(arow[m]);
+                }
+                for (int64_t m = 0; m < s.M; ++m) {
+                    double p = arow[m] * y;
+                    acc[m] += p;
+                    sab[m] += fabs(p);
+                }
+            }
+            const int64_t base = (sl * s.N + n) * s.M;
+            for (int64_t m = 0; m < s.M; ++m) {
+                if (dst) dst[base + m] = (float)acc[m];
+                if (dst_f64) dst_f64[base + m] = acc[m];
+                if (abssum) abssum[base + m] = sab[m];
+            }
+        }
+        free(acc);
+        free(sab);
+        free(arow);
+    }
+    return failed ? -1 : 0;
+}
+
+int oracle_out_prod(const void *a, int a_type, const float *b,
+                    const int64_t ne_a[4], const int64_t ne_b[4],
+                    float *dst, double *dst_f64, double *abssum, int nthreads)
+{
+    return out_prod_impl(a, a_type, b, ne_a, ne_b, dst, dst_f64, abssum,
+                         nthreads, 0);
+}
+
+int oracle_out_prod_fp16_staged(const void *a, int a_type, const float *b,
+                                const int64_t ne_a[4], const int64_t ne_b[4],
+                                float *dst, int nthreads)
+{
+    return out_prod_impl(a, a_type, b, ne_a, ne_b, dst, NULL, NULL, nthreads, 1);
+}
+
+int oracle_out_prod_at(const void *a, int a_type, const float *b,
+                       const int64_t ne_a[4], const int64_t ne_b[4],
+                       const int64_t *coords, int64_t n_pts,
+                       double *val, double *abssum, int nthreads)
+{
+    shape_t s;
+    if (check_shape(a_type, ne_a, ne_b, &s)) return -1;
+    if (n_pts < 0 || (n_pts > 0 && !coords)) return -1;
+    for (int64_t p = 0; p < n_pts; ++p) {
+        const int64_t *c = coords + 4 * p;
+        if (c[0] < 0 || c[0] >= s.M || c[1] < 0 || c[1] >= s.N ||
+            c[2] < 0 || c[2] >= s.ne12 || c[3] < 0 || c[3] >= s.ne13)
+            return -1;
+    }
+    if ((!a || !b) && s.K > 0 && n_pts > 0) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t p = 0; p < n_pts; ++p) {
+        const int64_t m = coords[4 * p + 0], n = coords[4 * p + 1];
+        const int64_t i2 = coords[4 * p + 2], i3 = coords[4 * p + 3];
+        const int64_t j2 = i2 / s.dps2, j3 = i3 / s.dps3;
+        double acc = 0.0, sab = 0.0;
+        for (int64_t k = 0; k < s.K; ++k) {
+            double x = elem(a_type, a_row(a, &s, k, j2, j3), m);
+            double prod = x * b_at(b, &s, n, k, i2, i3);
+            acc += prod;
+            sab += fabs(prod);
+        }
+        if (val) val[p] = acc;
+        if (abssum) abssum[p] = sab;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* MUL_MAT_ID_BACK                                                    */
+/* ------------------------------------------------------------------ */
+
+static int check_mmid(int w_type, const int32_t *ids, const int64_t ne_w[3],
+                      const int64_t ne_ids[2])
+{
+    if (!ne_w || !ne_ids) return -1;
+    if (w_type != ORACLE_F32 && w_type != ORACLE_BF16 && w_type != ORACLE_F16)
+        return -1;
+    for (int i = 0; i < 3; ++i) if (ne_w[i] < 0) return -1;
+    if (ne_ids[0] < 0 || ne_ids[1] < 0) return -1;
+    const int64_t nslot = ne_ids[0] * ne_ids[1];
+    if (nslot > 0 && !ids) return -1;
+    for (int64_t s = 0; s < nslot; ++s)
+        if (ids[s] < 0 || ids[s] >= ne_w[2]) return -1;
+    return 0;
+}
+
+static double w_at(const void *W, int w_type, const int64_t ne_w[3], int64_t e,
+                   int64_t k, int64_t r)
+{
+    const int64_t K = ne_w[0], N = ne_w[1];
+    const int64_t idx = (e * N + r) * K + k;
+    if (w_type == ORACLE_F32) return (double)((const float *)W)[idx];
+    uint16_t h = ((const uint16_t *)W)[idx];
+    return w_type == ORACLE_BF16 ? oracle_bf16_to_double(h) : oracle_half_to_double(h);
+}
+
+int oracle_mul_mat_id_back(const void *W, int w_type, const int32_t *ids,
+                           const float *g, const int64_t ne_w[3],
+                           const int64_t ne_ids[2], float *dx, double *dx_f64,
+                           double *abssum, int nthreads)
+{
+    if (check_mmid(w_type, ids, ne_w, ne_ids)) return -1;
+    const int64_t K = ne_w[0], N = ne_w[1];
+    const int64_t n_used = ne_ids[0], n_tok = ne_ids[1];
+    const int64_t nslot = n_used * n_tok;
+    if (nslot == 0 || K == 0) return 0;
+    if ((!W || !g) && N > 0) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t s = 0; s < nslot; ++s) {
+        /* slot s = t*n_used + i; g and dx use the same slot order */
+        const int64_t e = ids[s];
+        const float *gs = g + s * N;
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0, sab = 0.0;
+            for (int64_t r = 0; r < N; ++r) {
+                double p = w_at(W, w_type, ne_w, e, k, r) * (double)gs[r];
+                acc += p;
+                sab += fabs(p);
+            }
+            if (dx) dx[s * K + k] = (float)acc;
+            if (dx_f64) dx_f64[s * K + k] = acc;
+            if (abssum) abssum[s * K + k] = sab;
+        }
+    }
+    return 0;
+}
+
+int oracle_mul_mat_id_back_at(const void *W, int w_type, const int32_t *ids,
+                              const float *g, const int64_t ne_w[3],
+                              const int64_t ne_ids[2], const int64_t *coords,
+                              int64_t n_pts, double *val, double *abssum,
+                              int nthreads)
+{
+    if (check_mmid(w_type, ids, ne_w, ne_ids)) return -1;
+    const int64_t K = ne_w[0], N = ne_w[1];
+    const int64_t n_used = ne_ids[0], n_tok = ne_ids[1];
+    if (n_pts < 0 || (n_pts > 0 && !coords)) return -1;
+    for (int64_t p = 0; p < n_pts; ++p) {
+        const int64_t *c = coords + 3 * p;
+        if (c[0] < 0 || c[0] >= K || c[1] < 0 || c[1] >= n_used || c[2] < 0 ||
+            c[2] >= n_tok)
+            return -1;
+    }
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t p = 0; p < n_pts; ++p) {
+        const int64_t k = coords[3 * p], i = coords[3 * p + 1], t = coords[3 * p + 2];
+        const int64_t s = t * n_used + i;
+        const int64_t e = ids[s];
+        double acc = 0.0, sab = 0.0;
+        for (int64_t r = 0; r < N; ++r) {
+            double prod = w_at(W, w_type, ne_w, e, k, r) * (double)g[s * N + r];
+            acc += prod;
+            sab += fabs(prod);
+        }
+        if (val) val[p] = acc;
+        if (abssum) abssum[p] = sab;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* forward MUL_MAT (for the finite-difference check of the backward)  */
+/* ------------------------------------------------------------------ */
+
+int oracle_mul_mat(const double *W, const double *x, int64_t K, int64_t R,
+                   int64_t T, double *y)
+{
+    if (!W || !x || !y || K < 0 || R < 0 || T < 0) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t r = 0; r < R; ++r) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) acc += W[r * K + k] * x[t * K + k];
+            y[t * R + r] = acc;
+        }
+    return 0;
+}

@@ -1,0 +1,97 @@
+/*
+ * oracle.h -- plain CPU oracle for OUT_PROD and MUL_MAT_ID_BACK.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The product path (the
+ * CUDA library) never links, loads or calls it, and it shares no code, header,
+ * table or constant with that path.
+ *
+ * Every sum is accumulated in fp64 in ascending order of the reduced index;
+ * every product of two f32 (or dequantised) values is exact in fp64.
+ *
+ * Tensor layout is ggml's: ne[0] is the fastest dimension, all contiguous.
+ *   a   (src0): ne_a = {M, K, ne02, ne03}, element a[m,k,j2,j3]
+ *   b   (src1): ne_b = {N, K, ne12, ne13}, element b[n,k,i2,i3]
+ *   dst       : {M, N, ne12, ne13},        element dst[m,n,i2,i3]
+ * Quantised src0 stores each row of M elements as M/32 blocks of 32.
+ *
+ * Return codes: 0 = ok, -1 = bad argument (null, shape, type, broadcast).
+ */
+#ifndef OOP_ORACLE_H
+#define OOP_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    ORACLE_F32 = 0,
+    ORACLE_F16 = 1,
+    ORACLE_Q4_0 = 2,
+    ORACLE_Q8_0 = 8,
+    ORACLE_BF16 = 30
+};
+
+/* IEEE 754 binary16 bit pattern -> its exact value (Inf/NaN included). */
+double oracle_half_to_double(uint16_t h);
+/* bfloat16 bit pattern (the top half of a binary32) -> its exact value. */
+double oracle_bf16_to_double(uint16_t h);
+/* Round a double to the nearest binary16 value (ties to even; beyond the
+ * largest finite half, 65504, by more than half an ulp -> +-Inf). */
+double oracle_round_to_half(double x);
+
+/* Dequantise n consecutive elements (n a multiple of 32 for q8_0/q4_0) of one
+ * row of `type` starting at `row` into out[0..n). */
+int oracle_dequant_row(int type, const void *row, int64_t n, double *out);
+
+/* OUT_PROD, the whole tensor.  dst (f32) and, when not NULL, dst_f64 (the
+ * unrounded fp64 sum) and abssum (sum_k |a*b|) are written for every element.
+ * nthreads <= 0 uses every core OpenMP offers. */
+int oracle_out_prod(const void *a, int a_type, const float *b,
+                    const int64_t ne_a[4], const int64_t ne_b[4],
+                    float *dst, double *dst_f64, double *abssum, int nthreads);
+
+/* OUT_PROD at chosen elements: coords holds n_pts rows of (m, n, i2, i3).
+ * val[p] = fp64 sum, abssum[p] = sum |a*b| (either may be NULL). */
+int oracle_out_prod_at(const void *a, int a_type, const float *b,
+                       const int64_t ne_a[4], const int64_t ne_b[4],
+                       const int64_t *coords, int64_t n_pts,
+                       double *val, double *abssum, int nthreads);
+
+/* Mutation used only to show the overflow gate bites: identical to
+ * oracle_out_prod except that every a and b value is first rounded to
+ * binary16 (so magnitudes past 65504 become Inf), the staging defect the
+ * pages fixed. */
+int oracle_out_prod_fp16_staged(const void *a, int a_type, const float *b,
+                                const int64_t ne_a[4], const int64_t ne_b[4],
+                                float *dst, int nthreads);
+
+/* MUL_MAT_ID_BACK.  W: ne_w = {K, N, E} (k fastest), f32 or bf16;
+ * ids: int32 [n_tokens][n_used] (slot fastest), ids[t*n_used + i];
+ * g: f32 {N, n_used, n_tokens}; dx: f32 {K, n_used, n_tokens}.
+ *   dx[k,i,t] = sum_r W[k, r, ids[i,t]] * g[r, i, t]
+ * An id outside [0, E) makes the call fail (-1) before anything is written. */
+int oracle_mul_mat_id_back(const void *W, int w_type, const int32_t *ids,
+                           const float *g, const int64_t ne_w[3],
+                           const int64_t ne_ids[2], float *dx, double *dx_f64,
+                           double *abssum, int nthreads);
+
+/* MUL_MAT_ID_BACK at chosen elements: coords rows of (k, i, t). */
+int oracle_mul_mat_id_back_at(const void *W, int w_type, const int32_t *ids,
+                              const float *g, const int64_t ne_w[3],
+                              const int64_t ne_ids[2], const int64_t *coords,
+                              int64_t n_pts, double *val, double *abssum,
+                              int nthreads);
+
+/* Forward MUL_MAT in fp64: W {K, R} (k fastest), x {K, T};
+ * y[r,t] = sum_k W[k,r] * x[k,t], y {R, T} (r fastest). */
+int oracle_mul_mat(const double *W, const double *x, int64_t K, int64_t R,
+                   int64_t T, double *y);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
