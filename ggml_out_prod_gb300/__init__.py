@@ -1,0 +1,275 @@
+"""GB300 OUT_PROD and MUL_MAT_ID_BACK: a thin Python binding of ``liboop.so``.
+
+The binding only marshals arguments: torch tensors give device pointers, ggml
+``ne`` and the current stream; every step of the computation runs in the CUDA
+library.  There is no fallback: if the library is not built, or the device is
+not an sm_103 GPU, calls raise.
+
+Layout: a ggml tensor with ne = {ne0, ne1, ne2, ne3} is a contiguous torch
+tensor of shape (ne3, ne2, ne1, ne0) (trailing dims may be dropped); a
+quantised src0 is a uint8 tensor whose last axis holds one row's bytes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+TYPE_F32 = 0
+TYPE_Q4_0 = 2
+TYPE_Q8_0 = 8
+TYPE_BF16 = 30
+
+PATH_AUTO = 0
+PATH_SKINNY = 1
+PATH_TCGEN05 = 2
+PATH_SIMT = 3
+
+HAS_TCGEN05 = True
+TCGEN05_LAUNCHES_PER_CALL = 2     # TF32 split of src1, then the tile kernel
+
+OK = 0
+ERR_NULL = -1
+ERR_TYPE = -2
+ERR_SHAPE = -3
+ERR_BROADCAST = -4
+ERR_ALIGN = -5
+ERR_WORKSPACE = -6
+ERR_CUDA = -7
+ERR_BAD_ID = -8
+ERR_DEVICE_TIMEOUT = -9
+ERR_DEVICE = -10
+ERR_PATH = -11
+
+_QK = 32
+_BLOCK_BYTES = {TYPE_Q8_0: 34, TYPE_Q4_0: 18}
+
+_lock = threading.Lock()
+_lib = None
+
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_vp = ctypes.c_void_p
+
+EXPORTS = (
+    "oop_out_prod", "oop_out_prod_ex", "oop_out_prod_workspace_size",
+    "oop_mul_mat_id_back", "oop_mul_mat_id_back_workspace_size",
+    "oop_device_status", "oop_status_string", "oop_version", "oop_debug_inject_timeout",
+)
+
+
+class OopError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.SO
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build the CUDA library first "
+                    "(ggml_out_prod_gb300.build()); there is no CPU fallback")
+            L = ctypes.CDLL(path)
+            L.oop_out_prod_workspace_size.restype = ctypes.c_size_t
+            L.oop_out_prod_workspace_size.argtypes = [ctypes.c_int, _i64p, _i64p]
+            L.oop_out_prod.restype = ctypes.c_int
+            L.oop_out_prod.argtypes = [_vp, ctypes.c_int, _vp, _vp, _i64p, _i64p, _i64p,
+                                       _vp, ctypes.c_size_t, _vp]
+            L.oop_out_prod_ex.restype = ctypes.c_int
+            L.oop_out_prod_ex.argtypes = [_vp, ctypes.c_int, _vp, _vp, _i64p, _i64p, _i64p,
+                                          _vp, ctypes.c_size_t, _vp, ctypes.c_int]
+            L.oop_mul_mat_id_back_workspace_size.restype = ctypes.c_size_t
+            L.oop_mul_mat_id_back_workspace_size.argtypes = [ctypes.c_int, _i64p, _i64p]
+            L.oop_mul_mat_id_back.restype = ctypes.c_int
+            L.oop_mul_mat_id_back.argtypes = [_vp, ctypes.c_int, _vp, _vp, _vp, _i64p, _i64p,
+                                              _vp, ctypes.c_size_t, _vp]
+            L.oop_device_status.restype = ctypes.c_int
+            L.oop_device_status.argtypes = [_vp, ctypes.c_int]
+            L.oop_status_string.restype = ctypes.c_char_p
+            L.oop_status_string.argtypes = [ctypes.c_int]
+            L.oop_version.restype = ctypes.c_int
+            L.oop_version.argtypes = []
+            L.oop_debug_inject_timeout.restype = ctypes.c_int
+            L.oop_debug_inject_timeout.argtypes = [ctypes.c_int]
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().oop_status_string(int(status)).decode()
+
+
+def _ne(v):
+    v = list(v)
+    return (ctypes.c_int64 * len(v))(*[int(x) for x in v])
+
+
+# ---------------------------------------------------------------------------
+# C-ABI mirrors (plain pointers and sizes)
+# ---------------------------------------------------------------------------
+
+def oop_out_prod_workspace_size(a_type, ne_a, ne_b) -> int:
+    return int(lib().oop_out_prod_workspace_size(int(a_type), _ne(ne_a), _ne(ne_b)))
+
+
+def oop_out_prod(a, a_type, b, dst, ne_a, ne_b, ne_dst, workspace, workspace_bytes, stream,
+                 path=PATH_AUTO) -> int:
+    return int(lib().oop_out_prod_ex(a, int(a_type), b, dst, _ne(ne_a), _ne(ne_b), _ne(ne_dst),
+                                     workspace, int(workspace_bytes), stream, int(path)))
+
+
+def oop_mul_mat_id_back_workspace_size(w_type, ne_w, ne_ids) -> int:
+    return int(lib().oop_mul_mat_id_back_workspace_size(int(w_type), _ne(ne_w), _ne(ne_ids)))
+
+
+def oop_mul_mat_id_back(W, w_type, ids, g, dx, ne_w, ne_ids, workspace, workspace_bytes,
+                        stream) -> int:
+    return int(lib().oop_mul_mat_id_back(W, int(w_type), ids, g, dx, _ne(ne_w), _ne(ne_ids),
+                                         workspace, int(workspace_bytes), stream))
+
+
+def oop_device_status(stream=None, clear=True) -> int:
+    return int(lib().oop_device_status(stream, 1 if clear else 0))
+
+
+# ---------------------------------------------------------------------------
+# torch-level convenience (argument marshalling only)
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() else None
+
+
+def ne_of(t, type_id=TYPE_F32, ne0=None):
+    """ggml ne of a contiguous tensor in this layout."""
+    shp = (1,) * (4 - t.dim()) + tuple(t.shape)
+    if type_id in _BLOCK_BYTES:
+        if ne0 is None:
+            ne0 = shp[3] // _BLOCK_BYTES[type_id] * _QK
+        return (ne0, shp[2], shp[1], shp[0])
+    return (shp[3], shp[2], shp[1], shp[0])
+
+
+def _check_cuda(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _workspace(nbytes, device, workspace):
+    torch = _torch()
+    if nbytes == 0:
+        return None
+    if workspace is not None:
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def out_prod(a, b, a_type=None, ne_a=None, out=None, workspace=None, stream=None,
+             path=PATH_AUTO):
+    """dst = OUT_PROD(a, b) on a's device and the current (or given) stream.
+
+    a: float32 tensor, or uint8 q8_0/q4_0 rows (give ``a_type``); b: float32.
+    Returns dst, float32 of shape (ne13, ne12, N, M)."""
+    torch = _torch()
+    if a_type is None:
+        a_type = TYPE_F32
+    _check_cuda(a, "a")
+    _check_cuda(b, "b")
+    if b.dtype != torch.float32:
+        raise ValueError("b must be float32")
+    if a_type == TYPE_F32 and a.dtype != torch.float32:
+        raise ValueError("f32 src0 must be a float32 tensor")
+    if a_type in _BLOCK_BYTES and a.dtype != torch.uint8:
+        raise ValueError("quantised src0 must be a uint8 tensor of block bytes")
+    if ne_a is None:
+        ne_a = ne_of(a, a_type)
+    ne_b = ne_of(b)
+    ne_dst = (ne_a[0], ne_b[0], ne_b[2], ne_b[3])
+    if out is None:
+        out = torch.empty((ne_dst[3], ne_dst[2], ne_dst[1], ne_dst[0]), dtype=torch.float32,
+                          device=a.device)
+    _check_cuda(out, "out")
+    nws = oop_out_prod_workspace_size(a_type, ne_a, ne_b)
+    ws = _workspace(nws, a.device, workspace)
+    rc = oop_out_prod(_ptr(a), a_type, _ptr(b), _ptr(out), ne_a, ne_b, ne_dst, _ptr(ws),
+                      ws.numel() if ws is not None else 0, _stream_ptr(stream), path)
+    if rc != OK:
+        raise OopError(rc, "oop_out_prod")
+    return out
+
+
+def mul_mat_id_back(W, ids, g, w_type=None, out=None, workspace=None, stream=None):
+    """dx = MUL_MAT_ID_BACK(W, ids, g).
+
+    W: float32 (E, N, K) or bf16 bits / torch.bfloat16 (E, N, K); ids: int32
+    (n_tokens, n_used); g: float32 (n_tokens, n_used, N).  Returns dx float32
+    (n_tokens, n_used, K)."""
+    torch = _torch()
+    for t, n in ((W, "W"), (ids, "ids"), (g, "g")):
+        _check_cuda(t, n)
+    if w_type is None:
+        w_type = TYPE_F32 if W.dtype == torch.float32 else TYPE_BF16
+    if ids.dtype != torch.int32 or g.dtype != torch.float32:
+        raise ValueError("ids must be int32 and g float32")
+    E, N, K = W.shape
+    n_tok, n_used = ids.shape
+    if tuple(g.shape) != (n_tok, n_used, N):
+        raise ValueError("g must be (n_tokens, n_used, N)")
+    if out is None:
+        out = torch.empty((n_tok, n_used, K), dtype=torch.float32, device=W.device)
+    _check_cuda(out, "out")
+    ne_w, ne_ids = (K, N, E), (n_used, n_tok)
+    nws = oop_mul_mat_id_back_workspace_size(w_type, ne_w, ne_ids)
+    ws = _workspace(nws, W.device, workspace)
+    rc = oop_mul_mat_id_back(_ptr(W), w_type, _ptr(ids), _ptr(g), _ptr(out), ne_w, ne_ids,
+                             _ptr(ws), ws.numel() if ws is not None else 0,
+                             _stream_ptr(stream))
+    if rc != OK:
+        raise OopError(rc, "oop_mul_mat_id_back")
+    return out
+
+
+def device_status(stream=None, clear=True) -> int:
+    return oop_device_status(_stream_ptr(stream), clear)
+
+
+def out_prod_host(a_host, b_host, a_type=None, device="cuda", path=PATH_AUTO):
+    """OUT_PROD from host tensors: copies in (pinned memory, non-blocking),
+    runs on the device, copies the result back; returns a host tensor."""
+    torch = _torch()
+    a = a_host.to(device, non_blocking=True)
+    b = b_host.to(device, non_blocking=True)
+    d = out_prod(a, b, a_type=a_type, path=path)
+    out = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
+    out.copy_(d, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return out

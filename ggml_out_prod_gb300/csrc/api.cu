@@ -1,0 +1,275 @@
+// api.cu -- the C ABI: argument checks, kernel choice, device status word.
+//
+// Every check runs on the host before anything is enqueued, so a rejected
+// call leaves the stream untouched.  The shape contract is ggml's OUT_PROD
+// contract ("metal: OUT_PROD runs batched, broadcast and narrow shapes on the
+// GPU", review comment, first bullet): dst = {a.ne0, b.ne0, b.ne2, b.ne3},
+// b.ne2 % a.ne2 == 0 and b.ne3 % a.ne3 == 0.
+#include <mutex>
+
+#include "oop_internal.cuh"
+
+namespace oop {
+namespace {
+
+// One status word per device, written by kernels through a pointer.
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_status_ptr[kMaxDevices];
+int g_device_ok[kMaxDevices];      // 0 unknown, 1 sm_103, -1 other
+
+int current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return OOP_ERR_CUDA;
+    if (*dev < 0 || *dev >= kMaxDevices) return OOP_ERR_DEVICE;
+    return OOP_OK;
+}
+
+// Checks the device is sm_103 and returns its status-word address.
+int device_setup(int **status) {
+    int dev = 0;
+    int rc = current_device(&dev);
+    if (rc != OOP_OK) return rc;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_device_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return OOP_ERR_CUDA;
+        g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        if (g_device_ok[dev] == 1) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+                g_device_ok[dev] = 0;
+                return OOP_ERR_CUDA;
+            }
+            g_status_ptr[dev] = static_cast<int *>(p);
+        }
+    }
+    if (g_device_ok[dev] != 1) return OOP_ERR_DEVICE;
+    *status = g_status_ptr[dev];
+    return OOP_OK;
+}
+
+bool aligned(const void *p, uintptr_t n) { return reinterpret_cast<uintptr_t>(p) % n == 0; }
+
+int64_t row_bytes(int type, int64_t n) {
+    switch (type) {
+    case OOP_TYPE_F32: return 4 * n;
+    case OOP_TYPE_BF16: return 2 * n;
+    case OOP_TYPE_Q8_0: return n / kQK * kQ8Bytes;
+    case OOP_TYPE_Q4_0: return n / kQK * kQ4Bytes;
+    default: return -1;
+    }
+}
+
+// Shape checks shared by the size query and the call.
+int check_out_prod_shape(int a_type, const int64_t ne_a[4], const int64_t ne_b[4],
+                         OutProdShape *s) {
+    if (!ne_a || !ne_b) return OOP_ERR_NULL;
+    for (int i = 0; i < 4; ++i)
+        if (ne_a[i] < 0 || ne_b[i] < 0) return OOP_ERR_SHAPE;
+    if (a_type != OOP_TYPE_F32 && a_type != OOP_TYPE_Q8_0 && a_type != OOP_TYPE_Q4_0)
+        return OOP_ERR_TYPE;
+    if (ne_a[1] != ne_b[1]) return OOP_ERR_SHAPE;
+    if (ne_a[2] < 1 || ne_a[3] < 1) return OOP_ERR_BROADCAST;
+    if (ne_b[2] % ne_a[2] != 0 || ne_b[3] % ne_a[3] != 0) return OOP_ERR_BROADCAST;
+    if (a_type != OOP_TYPE_F32 && ne_a[0] % kQK != 0) return OOP_ERR_SHAPE;
+    // element counts must fit comfortably in int64 arithmetic
+    const double big = 9.0e18;
+    if (static_cast<double>(ne_a[0]) * ne_a[1] * ne_a[2] * ne_a[3] * 4.0 > big ||
+        static_cast<double>(ne_b[0]) * ne_b[1] * ne_b[2] * ne_b[3] * 4.0 > big ||
+        static_cast<double>(ne_a[0]) * ne_b[0] * ne_b[2] * ne_b[3] * 4.0 > big)
+        return OOP_ERR_SHAPE;
+    if (ne_b[2] * ne_b[3] > 65535) return OOP_ERR_SHAPE;   // slices ride grid.z
+    s->M = ne_a[0];
+    s->K = ne_a[1];
+    s->N = ne_b[0];
+    s->ne02 = ne_a[2];
+    s->ne03 = ne_a[3];
+    s->ne12 = ne_b[2];
+    s->ne13 = ne_b[3];
+    s->dps2 = s->ne12 / s->ne02;
+    s->dps3 = s->ne13 / s->ne03;
+    s->a_type = a_type;
+    s->a_row_bytes = row_bytes(a_type, s->M);
+    return OOP_OK;
+}
+
+bool skinny_ok(const OutProdShape &s) { return s.a_type == OOP_TYPE_F32 && s.N >= 1 && s.N <= 32; }
+
+int choose_path(const OutProdShape &s, int path) {
+    if (path == OOP_PATH_AUTO) return skinny_ok(s) ? OOP_PATH_SKINNY : OOP_PATH_TCGEN05;
+    return path;
+}
+
+size_t workspace_for(const OutProdShape &s, int path) {
+    if (path == OOP_PATH_TCGEN05) return tc_workspace_bytes(s);
+    return 0;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? OOP_OK : OOP_ERR_CUDA; }
+
+}  // namespace
+}  // namespace oop
+
+using namespace oop;
+
+extern "C" {
+
+size_t oop_out_prod_workspace_size(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
+    OutProdShape s = {};
+    if (check_out_prod_shape(a_type, ne_a, ne_b, &s) != OOP_OK) return 0;
+    // cover every path a caller may pick with oop_out_prod_ex
+    size_t w = workspace_for(s, OOP_PATH_TCGEN05);
+    return w;
+}
+
+int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst, const int64_t ne_a[4],
+                    const int64_t ne_b[4], const int64_t ne_dst[4], void *workspace,
+                    size_t workspace_bytes, void *stream, int path) {
+    OutProdShape s = {};
+    int rc = check_out_prod_shape(a_type, ne_a, ne_b, &s);
+    if (rc != OOP_OK) return rc;
+    if (!ne_dst) return OOP_ERR_NULL;
+    if (ne_dst[0] != s.M || ne_dst[1] != s.N || ne_dst[2] != s.ne12 || ne_dst[3] != s.ne13)
+        return OOP_ERR_SHAPE;
+    if (path < OOP_PATH_AUTO || path > OOP_PATH_SIMT) return OOP_ERR_PATH;
+
+    const int64_t n_dst = s.M * s.N * s.ne12 * s.ne13;
+    if (n_dst == 0) return OOP_OK;
+    if (!dst) return OOP_ERR_NULL;
+    if (!aligned(dst, 4)) return OOP_ERR_ALIGN;
+    if (s.K > 0) {
+        if (!a || !b) return OOP_ERR_NULL;
+        if (!aligned(b, 4)) return OOP_ERR_ALIGN;
+        if (!aligned(a, a_type == OOP_TYPE_F32 ? 4 : 2)) return OOP_ERR_ALIGN;
+    }
+    int *status = nullptr;
+    rc = device_setup(&status);
+    if (rc != OOP_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const int chosen = choose_path(s, path);
+    if (chosen == OOP_PATH_SKINNY && !skinny_ok(s)) return OOP_ERR_PATH;
+    const size_t need = workspace_for(s, chosen);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+        return OOP_ERR_WORKSPACE;
+
+    if (s.K == 0)   // an empty sum
+        return cuda_rc(cudaMemsetAsync(dst, 0, static_cast<size_t>(n_dst) * sizeof(float), st));
+
+    s.a_vec16 = aligned(a, 16) && (s.a_row_bytes % 16 == 0);
+    s.b_vec16 = aligned(b, 16) && (s.N % 4 == 0);
+    s.dst_vec16 = aligned(dst, 16) && (s.M % 4 == 0);
+
+    cudaError_t e;
+    switch (chosen) {
+    case OOP_PATH_SKINNY:
+        e = launch_skinny(static_cast<const float *>(a), b, dst, s, st);
+        break;
+    case OOP_PATH_TCGEN05:
+        e = launch_dense_tc(a, b, dst, s, workspace, status, st);
+        if (e == cudaErrorNotSupported) return OOP_ERR_PATH;
+        break;
+    case OOP_PATH_SIMT:
+        e = launch_dense_simt(a, b, dst, s, st);
+        break;
+    default:
+        return OOP_ERR_PATH;
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_rc(e);
+}
+
+int oop_out_prod(const void *a, int a_type, const float *b, float *dst, const int64_t ne_a[4],
+                 const int64_t ne_b[4], const int64_t ne_dst[4], void *workspace,
+                 size_t workspace_bytes, void *stream) {
+    return oop_out_prod_ex(a, a_type, b, dst, ne_a, ne_b, ne_dst, workspace, workspace_bytes,
+                           stream, OOP_PATH_AUTO);
+}
+
+size_t oop_mul_mat_id_back_workspace_size(int w_type, const int64_t ne_w[3],
+                                          const int64_t ne_ids[2]) {
+    (void)w_type;
+    (void)ne_w;
+    (void)ne_ids;
+    return 0;
+}
+
+int oop_mul_mat_id_back(const void *W, int w_type, const int32_t *ids, const float *g, float *dx,
+                        const int64_t ne_w[3], const int64_t ne_ids[2], void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    if (!ne_w || !ne_ids) return OOP_ERR_NULL;
+    if (w_type != OOP_TYPE_F32 && w_type != OOP_TYPE_BF16) return OOP_ERR_TYPE;
+    for (int i = 0; i < 3; ++i)
+        if (ne_w[i] < 0) return OOP_ERR_SHAPE;
+    if (ne_ids[0] < 0 || ne_ids[1] < 0) return OOP_ERR_SHAPE;
+    MmidShape s = {ne_w[0], ne_w[1], ne_w[2], ne_ids[0], ne_ids[1], w_type};
+    const double big = 9.0e18;
+    if (static_cast<double>(s.K) * s.N * s.E * 4.0 > big ||
+        static_cast<double>(s.K) * s.n_used * s.n_tok * 4.0 > big ||
+        static_cast<double>(s.N) * s.n_used * s.n_tok * 4.0 > big)
+        return OOP_ERR_SHAPE;
+    const int64_t slots = s.n_used * s.n_tok;
+    if (slots == 0 || s.K == 0) return OOP_OK;
+    if (!dx || !ids) return OOP_ERR_NULL;
+    if (!aligned(dx, 4) || !aligned(ids, 4)) return OOP_ERR_ALIGN;
+    if (s.N > 0) {
+        if (!W || !g) return OOP_ERR_NULL;
+        if (!aligned(g, 4) || !aligned(W, w_type == OOP_TYPE_F32 ? 4 : 2)) return OOP_ERR_ALIGN;
+    }
+    if (s.N > 48 * 1024) return OOP_ERR_SHAPE;   // g's slot column is staged on chip
+    int *status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != OOP_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_mmid_per_slot(W, ids, g, dx, s, status, st);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_rc(e);
+}
+
+int oop_device_status(void *stream, int clear) {
+    int *status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != OOP_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return OOP_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return OOP_ERR_CUDA;
+    if (clear && v != 0) {
+        if (cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return OOP_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return OOP_ERR_CUDA;
+    }
+    return v;
+}
+
+const char *oop_status_string(int status) {
+    switch (status) {
+    case OOP_OK: return "ok";
+    case OOP_ERR_NULL: return "a required pointer is NULL";
+    case OOP_ERR_TYPE: return "unsupported element type";
+    case OOP_ERR_SHAPE: return "shape mismatch or unsupported size";
+    case OOP_ERR_BROADCAST: return "b.ne2/b.ne3 not divisible by a.ne2/a.ne3";
+    case OOP_ERR_ALIGN: return "pointer below its element alignment";
+    case OOP_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case OOP_ERR_CUDA: return "CUDA runtime error";
+    case OOP_ERR_BAD_ID: return "expert id out of range (slot zeroed)";
+    case OOP_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+    case OOP_ERR_DEVICE: return "current device is not sm_103";
+    case OOP_ERR_PATH: return "the requested kernel cannot take this call";
+    default: return "unknown status";
+    }
+}
+
+int oop_version(void) { return (0 << 16) | 1; }
+
+int oop_debug_inject_timeout(int enable) {
+    tc_set_inject(enable ? 1 : 0);
+    return OOP_OK;
+}
+
+}  // extern "C"

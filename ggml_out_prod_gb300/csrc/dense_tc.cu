@@ -1,0 +1,476 @@
+// dense_tc.cu -- tensor-core OUT_PROD for sm_103a (tcgen05, 3xTF32).
+//
+// Per dst slice: D[n][m] = sum_k A[k][m] * B[k][n], A = src0 (f32, or q8_0 /
+// q4_0 dequantised in registers), B = the f32 gradient src1.  The gradient can
+// reach ~1.5e5, so no operand is ever rounded to a 16-bit format ("metal:
+// OUT_PROD multiplies in float staging; a training gradient overflowed half");
+// instead each operand is split into two TF32 terms that keep fp32's 8-bit
+// exponent: x = hi + lo (+ r, |r| <= 2^-22 |x|), and the product is
+// a_hi*b_hi + a_hi*b_lo + a_lo*b_hi (the a_lo*b_lo term is ~2^-22 relative).
+//
+// Launches per call:
+//  1. bsplit: b[slice][k][n] -> bhi, blo [slice][n][Kp] (K-major TF32 words,
+//     Kp = K rounded up to 4) in the caller's workspace;
+//  2. the tile kernel, one 128 (m) x 128 (n) dst tile per CTA, every head x
+//     batch slice in the same grid (grid.y = slice, src0 slice i2/dps2,
+//     i3/dps3 -- the broadcast map of "metal: OUT_PROD runs batched,
+//     broadcast and narrow shapes on the GPU").
+//
+// Tile kernel roles (448 threads):
+//  warp 0      TMA: bhi/blo tiles (32 k x 128 n, 128-byte swizzle) -> smem
+//  warp 1      TMEM allocation; one thread issues tcgen05.mma (M128 N128 K8)
+//  warps 2-5   src0 producer: load, dequantise, split, write the K-major
+//              swizzled A images a_hi / a_lo to smem
+//  warps 6-13  fold + epilogue: TMEM -> registers -> dst
+//
+// Accumulation.  The tensor core adds each MMA's products into its fp32
+// accumulator with an error of up to about one ulp of the accumulator (it
+// does not round to nearest), so a long sum dominated by one 1e5-sized
+// gradient entry drifts past the 2e-6 * sum|a*b| bound.  Three measures keep
+// the error at a few ulps of the result:
+//  * the two small cross terms a_lo*b_hi + a_hi*b_lo go to their own
+//    accumulator D2, whose magnitude is ~2^-11 of the result, so its
+//    accumulation error is negligible; it runs over the whole K;
+//  * the big term a_hi*b_hi goes to D1, restarted every `chunk_kb` k-blocks
+//    (so at most 4*chunk_kb MMAs accumulate into it);
+//  * the fold warps add each finished D1 chunk into a Kahan pair: the sum S
+//    lives in TMEM, the compensation C in registers (64 columns per thread).
+// TMEM columns: [0,128) D1 buffer 0, [128,256) D1 buffer 1, [256,384) D2,
+// [384,512) S; the MMA fills one D1 buffer while the fold drains the other.
+//
+// Every wait is bounded (1 s of globaltimer); running out records
+// OOP_ERR_DEVICE_TIMEOUT, sets a CTA-wide abort flag, drains the copies and
+// MMAs already issued, frees TMEM and returns.  Nothing traps.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "oop_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace oop {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 32;                      // tf32 per 128-byte swizzle row
+constexpr int STAGES = 3;
+constexpr int THREADS = 448;
+constexpr int FOLD_THREADS = 256;
+constexpr int A_IMG = BM * BK * 4;          // 16 KB
+constexpr int B_IMG = BN * BK * 4;          // 16 KB
+constexpr int STAGE_BYTES = 2 * A_IMG + 2 * B_IMG;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_D2 = 2 * BN, COL_S = 3 * BN;
+constexpr uint64_t WAIT_NS = 1000000000ull;
+
+struct Bars {
+    uint64_t bfull[STAGES];   // TMA bytes of stage s landed
+    uint64_t afull[STAGES];   // the 128 src0-producer threads wrote stage s
+    uint64_t empty[STAGES];   // MMAs reading stage s completed
+    uint64_t accf[2];         // D1 buffer b holds a finished chunk
+    uint64_t acce[2];         // D1 buffer b was drained by the fold
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + sizeof(Bars) + 1024;
+
+struct TcParams {
+    const uint8_t *a;
+    float *dst;
+    int *status;
+    int64_t M, K, N, ne02, ne12, dps2, dps3, a_row_bytes;
+    int num_kb, chunk_kb, mtiles, ntiles, inject;
+};
+
+template <int TYPE>
+__device__ __forceinline__ float load_a(const uint8_t *row, int64_t m) {
+    if constexpr (TYPE == OOP_TYPE_F32) {
+        return __ldg(reinterpret_cast<const float *>(row) + m);
+    } else if constexpr (TYPE == OOP_TYPE_Q8_0) {
+        const uint8_t *blk = row + (m >> 5) * kQ8Bytes;
+        const uint16_t d = __ldg(reinterpret_cast<const unsigned short *>(blk));
+        const int8_t q = static_cast<int8_t>(__ldg(blk + 2 + (m & 31)));
+        return half_bits_to_float(d) * static_cast<float>(q);
+    } else {
+        const uint8_t *blk = row + (m >> 5) * kQ4Bytes;
+        const uint16_t d = __ldg(reinterpret_cast<const unsigned short *>(blk));
+        const int j = static_cast<int>(m & 31);
+        const uint8_t byte = __ldg(blk + 2 + (j & 15));
+        const int v = j < 16 ? (byte & 0x0f) : (byte >> 4);
+        return half_bits_to_float(d) * static_cast<float>(v - 8);
+    }
+}
+
+template <int TYPE>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_out_prod_kernel(const __grid_constant__ CUtensorMap map_bhi,
+                       const __grid_constant__ CUtensorMap map_blo, const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Bars *bars = reinterpret_cast<Bars *>(smem + STAGES * STAGE_BYTES);
+    volatile int *abort = &bars->abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int mt = blockIdx.x % p.mtiles;
+    const int nt = blockIdx.x / p.mtiles;
+    const int64_t slice = blockIdx.y;
+    const int64_t i2 = slice % p.ne12, i3 = slice / p.ne12;
+    const int64_t j2 = i2 / p.dps2, j3 = i3 / p.dps3;
+    const int nchunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&bars->bfull[s], 1);
+            ptx::mbar_init(&bars->afull[s], 128);
+            ptx::mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bars->accf[b], 1);
+            ptx::mbar_init(&bars->acce[b], FOLD_THREADS);
+        }
+        ptx::mbar_init(&bars->mma_done, 1);
+        bars->abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&map_bhi);
+        ptx::prefetch_tmap(&map_blo);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    bool timed_out = false;
+
+    if (warp == 0) {
+        // ---------------- TMA producer: B tiles ----------------
+        if (lane == 0) {
+            int last_kb[STAGES];
+            for (int s = 0; s < STAGES; ++s) last_kb[s] = -1;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t ph = (kb / STAGES) & 1;
+                if (!ptx::mbar_wait_bounded(&bars->empty[s], ph ^ 1, abort, true, WAIT_NS,
+                                            &timed_out))
+                    break;
+                if (p.inject == 1 && kb == 0) continue;   // test hook: drop one stage
+                uint8_t *st = smem + s * STAGE_BYTES;
+                ptx::mbar_arrive_expect_tx(&bars->bfull[s], 2 * B_IMG);
+                ptx::tma_load_3d(st + 2 * A_IMG, &map_bhi, &bars->bfull[s], kb * BK, nt * BN,
+                                 static_cast<int>(slice));
+                ptx::tma_load_3d(st + 2 * A_IMG + B_IMG, &map_blo, &bars->bfull[s], kb * BK,
+                                 nt * BN, static_cast<int>(slice));
+                last_kb[s] = kb;
+            }
+            // copies in flight must land before the CTA's smem is released
+            for (int s = 0; s < STAGES; ++s)
+                if (last_kb[s] >= 0)
+                    ptx::mbar_wait_bounded(&bars->bfull[s], (last_kb[s] / STAGES) & 1, abort,
+                                           false, WAIT_NS, &timed_out);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
+            int kb = 0;
+            bool ok = true;
+            for (int q = 0; q < nchunks && ok; ++q) {
+                const int buf = q & 1;
+                const uint32_t use = static_cast<uint32_t>(q >> 1);
+                if (!ptx::mbar_wait_bounded(&bars->acce[buf], (use & 1) ^ 1, abort, true,
+                                            WAIT_NS, &timed_out)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d1 = tmem + static_cast<uint32_t>(buf * BN);
+                const uint32_t d2 = tmem + COL_D2;
+                const int kb_first = q * p.chunk_kb;
+                const int kb_end = min(p.num_kb, kb_first + p.chunk_kb);
+                for (; kb < kb_end; ++kb) {
+                    const int s = kb % STAGES;
+                    const uint32_t ph = (kb / STAGES) & 1;
+                    if (!ptx::mbar_wait_bounded(&bars->bfull[s], ph, abort, true, WAIT_NS,
+                                                &timed_out) ||
+                        !ptx::mbar_wait_bounded(&bars->afull[s], ph, abort, true, WAIT_NS,
+                                                &timed_out)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t st = ptx::smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t ahi = st, alo = st + A_IMG;
+                    const uint32_t bhi = st + 2 * A_IMG, blo = st + 2 * A_IMG + B_IMG;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 8; ++kk) {
+                        const uint32_t off = kk * 32;   // 8 tf32 along k
+                        const uint32_t acc2 = (kb == 0 && kk == 0) ? 0u : 1u;
+                        const uint32_t acc1 = (kb == kb_first && kk == 0) ? 0u : 1u;
+                        ptx::mma_tf32(d2, ptx::sw128_kmajor_desc(alo + off),
+                                      ptx::sw128_kmajor_desc(bhi + off), idesc, acc2);
+                        ptx::mma_tf32(d2, ptx::sw128_kmajor_desc(ahi + off),
+                                      ptx::sw128_kmajor_desc(blo + off), idesc, 1u);
+                        ptx::mma_tf32(d1, ptx::sw128_kmajor_desc(ahi + off),
+                                      ptx::sw128_kmajor_desc(bhi + off), idesc, acc1);
+                    }
+                    ptx::mma_commit(&bars->empty[s]);
+                }
+                if (!ok) break;
+                ptx::mma_commit(&bars->accf[buf]);
+            }
+            // every MMA issued must finish before TMEM is released
+            ptx::mma_commit(&bars->mma_done);
+            ptx::mbar_wait_bounded(&bars->mma_done, 0, abort, false, WAIT_NS, &timed_out);
+        }
+    } else if (warp < 6) {
+        // ---------------- src0 producer ----------------
+        const int r = (warp - 2) * 32 + lane;              // row of the A image
+        const int64_t m = static_cast<int64_t>(mt) * BM + r;
+        const bool mok = m < p.M;
+        const uint8_t *a_slice = p.a + (j3 * p.ne02 + j2) * p.K * p.a_row_bytes;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (kb / STAGES) & 1;
+            float x[BK];
+#pragma unroll
+            for (int j = 0; j < BK; ++j) {
+                const int64_t k = static_cast<int64_t>(kb) * BK + j;
+                x[j] = (mok && k < p.K) ? load_a<TYPE>(a_slice + k * p.a_row_bytes, m) : 0.f;
+            }
+            if (!ptx::mbar_wait_bounded(&bars->empty[s], ph ^ 1, abort, true, WAIT_NS,
+                                        &timed_out))
+                break;
+            uint8_t *ahi = smem + s * STAGE_BYTES;
+            uint8_t *alo = ahi + A_IMG;
+#pragma unroll
+            for (int c = 0; c < BK / 4; ++c) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ptx::split_tf32(x[4 * c + e], h[e], l[e]);
+                const int off = r * 128 + ((c ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(ahi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(alo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&bars->afull[s]);
+        }
+    } else {
+        // ---------------- fold + epilogue ----------------
+        const int quad = warp & 3;                          // TMEM lanes 32*quad ..
+        const int half = (warp - 6) >> 2;                   // columns 64*half ..
+        const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+        const uint32_t col0 = static_cast<uint32_t>(64 * half);
+        const int64_t m = static_cast<int64_t>(mt) * BM + 32 * quad + lane;
+        float *dst = p.dst + slice * p.N * p.M;
+        float cmp[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) cmp[j] = 0.f;
+        for (int q = 0; q < nchunks; ++q) {
+            const int buf = q & 1;
+            const uint32_t use = static_cast<uint32_t>(q >> 1);
+            if (!ptx::mbar_wait_bounded(&bars->accf[buf], use & 1, abort, true, WAIT_NS,
+                                        &timed_out))
+                break;
+            ptx::tc_fence_after();
+            const bool first = q == 0, last = q == nchunks - 1;
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc) {
+                const uint32_t col = col0 + pc * 16;
+                uint32_t xv[16], sv[16], dv[16];
+                ptx::tmem_ld16(tmem + lane_off + buf * BN + col, xv);
+                if (!first) ptx::tmem_ld16(tmem + lane_off + COL_S + col, sv);
+                if (last) ptx::tmem_ld16(tmem + lane_off + COL_D2 + col, dv);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float sj;
+                    if (first) {
+                        sj = __uint_as_float(xv[j]);
+                    } else {
+                        // Kahan: the running sum is S - C
+                        const float s0 = __uint_as_float(sv[j]);
+                        const float y = __uint_as_float(xv[j]) - cmp[pc * 16 + j];
+                        const float t = s0 + y;
+                        cmp[pc * 16 + j] = (t - s0) - y;
+                        sj = t;
+                    }
+                    sv[j] = __float_as_uint(sj);
+                }
+                if (last) {
+                    if (m < p.M) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int64_t n = static_cast<int64_t>(nt) * BN + col + j;
+                            if (n < p.N)
+                                dst[n * p.M + m] = __uint_as_float(sv[j]) +
+                                                   (__uint_as_float(dv[j]) - cmp[pc * 16 + j]);
+                        }
+                    }
+                } else {
+                    ptx::tmem_st16(tmem + lane_off + COL_S + col, sv);
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bars->acce[buf]);
+        }
+    }
+
+    if (timed_out) record_status(p.status, OOP_ERR_DEVICE_TIMEOUT);
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// b[slice][k][n] (n fastest) -> bhi, blo [slice][n][Kp] (k fastest), TF32
+// split, zero padding for k in [K, Kp).
+__global__ void __launch_bounds__(256) bsplit_kernel(const float *__restrict__ b,
+                                                     uint32_t *__restrict__ bhi,
+                                                     uint32_t *__restrict__ blo, int64_t K,
+                                                     int64_t N, int64_t Kp) {
+    __shared__ float tile[32][33];
+    const int64_t slice = blockIdx.z;
+    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.y) * 32;
+    const float *bs = b + slice * K * N;
+    const int tx = threadIdx.x, ty = threadIdx.y;
+#pragma unroll
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t k = k0 + i, n = n0 + tx;
+        tile[i][tx] = (k < K && n < N) ? __ldg(bs + k * N + n) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t n = n0 + i, k = k0 + tx;
+        if (n < N && k < Kp) {
+            uint32_t h, l;
+            ptx::split_tf32(tile[tx][i], h, l);
+            const int64_t o = (slice * N + n) * Kp + k;
+            bhi[o] = h;
+            blo[o] = l;
+        }
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap *map, void *base, int64_t Kp, int64_t N, int64_t slices) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(Kp), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(slices)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(Kp * 4),
+                             static_cast<cuuint64_t>(N * Kp * 4)};
+    cuuint32_t box[3] = {BK, BN, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int64_t padded_k(int64_t K) { return (K + 3) / 4 * 4; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int g_inject = 0;
+#ifndef OOP_TC_CHUNK_KB
+#define OOP_TC_CHUNK_KB 2
+#endif
+int g_chunk_kb = OOP_TC_CHUNK_KB;      // k-blocks (of 32) per D1 accumulation
+
+}  // namespace
+
+void tc_set_inject(int v) { g_inject = v; }
+void tc_set_chunk_kb(int v) { g_chunk_kb = v < 1 ? 1 : v; }
+
+size_t tc_workspace_bytes(const OutProdShape &s) {
+    const size_t one = align256(static_cast<size_t>(s.ne12 * s.ne13) *
+                                static_cast<size_t>(s.N) * static_cast<size_t>(padded_k(s.K)) * 4);
+    return 2 * one;
+}
+
+cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const OutProdShape &s,
+                            void *workspace, int *status, cudaStream_t stream) {
+    const int64_t slices = s.ne12 * s.ne13;
+    const int64_t Kp = padded_k(s.K);
+    const size_t one = tc_workspace_bytes(s) / 2;
+    uint32_t *bhi = static_cast<uint32_t *>(workspace);
+    uint32_t *blo = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + one);
+
+    const int64_t gk = (Kp + 31) / 32, gn = (s.N + 31) / 32;
+    if (gk > 0x7fffffffLL || gn > 65535 || slices > 65535) return cudaErrorInvalidConfiguration;
+    bsplit_kernel<<<dim3(static_cast<unsigned>(gk), static_cast<unsigned>(gn),
+                         static_cast<unsigned>(slices)),
+                    dim3(32, 8), 0, stream>>>(b, bhi, blo, s.K, s.N, Kp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    CUtensorMap mhi, mlo;
+    if (!make_map(&mhi, bhi, Kp, s.N, slices) || !make_map(&mlo, blo, Kp, s.N, slices))
+        return cudaErrorInvalidValue;
+
+    TcParams p = {};
+    p.a = static_cast<const uint8_t *>(a);
+    p.dst = dst;
+    p.status = status;
+    p.M = s.M;
+    p.K = s.K;
+    p.N = s.N;
+    p.ne02 = s.ne02;
+    p.ne12 = s.ne12;
+    p.dps2 = s.dps2;
+    p.dps3 = s.dps3;
+    p.a_row_bytes = s.a_row_bytes;
+    p.num_kb = static_cast<int>((s.K + BK - 1) / BK);
+    p.chunk_kb = g_chunk_kb;
+    const int64_t mtiles = (s.M + BM - 1) / BM, ntiles = (s.N + BN - 1) / BN;
+    if (mtiles * ntiles > 0x7fffffffLL || (s.K + BK - 1) / BK > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    p.mtiles = static_cast<int>(mtiles);
+    p.ntiles = static_cast<int>(ntiles);
+    p.inject = g_inject;
+    g_inject = 0;
+
+    auto launch = [&](auto kern) -> cudaError_t {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(SMEM_BYTES));
+        if (err != cudaSuccess) return err;
+        kern<<<dim3(static_cast<unsigned>(mtiles * ntiles), static_cast<unsigned>(slices)),
+               THREADS, SMEM_BYTES, stream>>>(mhi, mlo, p);
+        return cudaGetLastError();
+    };
+    switch (s.a_type) {
+    case OOP_TYPE_F32: return launch(tc_out_prod_kernel<OOP_TYPE_F32>);
+    case OOP_TYPE_Q8_0: return launch(tc_out_prod_kernel<OOP_TYPE_Q8_0>);
+    case OOP_TYPE_Q4_0: return launch(tc_out_prod_kernel<OOP_TYPE_Q4_0>);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace oop

@@ -1,0 +1,72 @@
+// oop_internal.cuh -- shared declarations of the CUDA library (not part of
+// the public C ABI; the public header is include/oop.h).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "oop.h"
+
+namespace oop {
+
+constexpr int kQK = 32;           // elements per q8_0 / q4_0 block
+constexpr int kQ8Bytes = 34;      // fp16 scale + 32 int8
+constexpr int kQ4Bytes = 18;      // fp16 scale + 16 packed bytes
+
+// One OUT_PROD call after validation.  Slice (i2, i3) of dst reads src0
+// slice (i2/dps2, i3/dps3): the CPU backend's broadcast map ("metal: OUT_PROD
+// runs batched, broadcast and narrow shapes on the GPU", review comment).
+struct OutProdShape {
+    int64_t M, K, N;
+    int64_t ne02, ne03, ne12, ne13;
+    int64_t dps2, dps3;
+    int64_t a_row_bytes;          // bytes of one src0 row of M elements
+    int a_type;
+    bool a_vec16;                 // a base and row stride 16-byte aligned
+    bool b_vec16;                 // b base and row stride 16-byte aligned
+    bool dst_vec16;               // dst base and row stride 16-byte aligned
+};
+
+struct MmidShape {
+    int64_t K, N, E, n_used, n_tok;
+    int w_type;
+};
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// First error wins; later errors do not overwrite it.
+__device__ __forceinline__ void record_status(int *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---- kernels (each .cu file owns its launcher) ----------------------------
+
+// Skinny-N OUT_PROD: f32 src0, N <= 32.
+cudaError_t launch_skinny(const float *a, const float *b, float *dst,
+                          const OutProdShape &s, cudaStream_t stream);
+
+// CUDA-core tiled OUT_PROD, any src0 type.
+cudaError_t launch_dense_simt(const void *a, const float *b, float *dst,
+                              const OutProdShape &s, cudaStream_t stream);
+
+// Tensor-core OUT_PROD (tcgen05, 3xTF32).
+size_t tc_workspace_bytes(const OutProdShape &s);
+void tc_set_inject(int v);   // test hook: the next tensor-core launch drops one TMA stage
+cudaError_t launch_dense_tc(const void *a, const float *b, float *dst,
+                            const OutProdShape &s, void *workspace,
+                            int *status, cudaStream_t stream);
+
+// MUL_MAT_ID_BACK, one CTA per routed slot.
+cudaError_t launch_mmid_per_slot(const void *W, const int32_t *ids,
+                                 const float *g, float *dx, const MmidShape &s,
+                                 int *status, cudaStream_t stream);
+
+}  // namespace oop

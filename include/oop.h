@@ -1,0 +1,158 @@
+/*
+ * oop.h -- GB300 (sm_103a) OUT_PROD and MUL_MAT_ID_BACK, C ABI.
+ *
+ * OUT_PROD is the operation that carries the whole matmul backward in ggml
+ * training: both gradients of a MUL_MAT are out-products ("metal: OUT_PROD
+ * multiplies in float staging; a training gradient overflowed half", scope
+ * paragraph: src0's gradient is out_prod(src1, grad), src1's is
+ * out_prod(src0, grad^T)).  MUL_MAT_ID_BACK is the MoE input gradient ("Metal
+ * kernel_mul_mat_id_back", first bullet).
+ *
+ * Layout (ggml's): ne[0] is the fastest dimension; every tensor is dense and
+ * contiguous.  M = a.ne0, K = a.ne1 = b.ne1, N = b.ne0.
+ *
+ * Memory: every pointer passed to a compute entry point is a DEVICE pointer
+ * on the current CUDA device, owned by the caller and left owned by the
+ * caller.  The library allocates nothing per call and keeps no state except
+ * one status word per device (see oop_device_status).
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ * work is enqueued on it in order; no entry point synchronises except
+ * oop_device_status.
+ *
+ * Errors: arguments are checked on the host before anything is enqueued; a
+ * failed check returns a negative oop_status and enqueues nothing.  Faults the
+ * device detects while running (an expert id out of range, a bounded wait that
+ * ran out) are recorded in the device status word and never trap.
+ */
+#ifndef OOP_H
+#define OOP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  The numbers are ggml's public type ids, so a ggml caller
+ * passes its own tensor type unchanged. */
+typedef enum {
+    OOP_TYPE_F32 = 0,
+    OOP_TYPE_Q4_0 = 2,  /* 18-byte blocks of 32: fp16 d, 16 bytes; byte j holds
+                           element j (low nibble) and j+16 (high nibble);
+                           value = d * (nibble - 8) */
+    OOP_TYPE_Q8_0 = 8,  /* 34-byte blocks of 32: fp16 d, 32 int8 q; value = d*q */
+    OOP_TYPE_BF16 = 30
+} oop_type;
+
+typedef enum {
+    OOP_OK = 0,
+    OOP_ERR_NULL = -1,           /* a required pointer is NULL */
+    OOP_ERR_TYPE = -2,           /* unsupported element type for this operand */
+    OOP_ERR_SHAPE = -3,          /* negative size, K mismatch, wrong dst ne, M % 32 */
+    OOP_ERR_BROADCAST = -4,      /* b.ne2 % a.ne2 or b.ne3 % a.ne3 non-zero */
+    OOP_ERR_ALIGN = -5,          /* a pointer below its element's alignment */
+    OOP_ERR_WORKSPACE = -6,      /* workspace NULL or smaller than required */
+    OOP_ERR_CUDA = -7,           /* a CUDA runtime call or launch failed */
+    OOP_ERR_BAD_ID = -8,         /* device: an expert id outside [0, E) */
+    OOP_ERR_DEVICE_TIMEOUT = -9, /* device: a bounded wait ran out */
+    OOP_ERR_DEVICE = -10,        /* the current device is not sm_103 */
+    OOP_ERR_PATH = -11           /* oop_out_prod_ex: that kernel cannot take this call */
+} oop_status;
+
+/* Kernel selection for oop_out_prod_ex. */
+typedef enum {
+    OOP_PATH_AUTO = 0,    /* what oop_out_prod does */
+    OOP_PATH_SKINNY = 1,  /* CUDA-core skinny-N kernel: f32 src0, N <= 32 */
+    OOP_PATH_TCGEN05 = 2, /* tensor-core kernel (3xTF32 split), any src0 type */
+    OOP_PATH_SIMT = 3     /* CUDA-core tiled kernel, any src0 type (for checks) */
+} oop_path;
+
+/*
+ * OUT_PROD.  The operation of "metal: OUT_PROD runs batched, broadcast and
+ * narrow shapes on the GPU" (review comment, first bullet):
+ *
+ *   dst[m, n, i2, i3] = sum_k a[m, k, i2/dps2, i3/dps3] * b[n, k, i2, i3]
+ *
+ *   ne_a   = {M, K, ne02, ne03}   a (src0): f32, q8_0 or q4_0
+ *   ne_b   = {N, K, ne12, ne13}   b (src1): f32
+ *   ne_dst = {M, N, ne12, ne13}   dst: f32, OVERWRITTEN (not accumulated)
+ *   dps2 = ne12/ne02 and dps3 = ne13/ne03 must divide exactly.
+ *
+ * Quantised a needs M % 32 == 0 (its blocks run along ne0).  Alignment: f32
+ * pointers 4 bytes, quantised a 2 bytes; 16-byte alignment enables the vector
+ * paths.  K == 0 writes zeros (an empty sum); any other zero size is a no-op.
+ * b may hold values far beyond binary16's range: no operand is ever rounded to
+ * fp16.  Precision: every finite input gives a finite result within
+ * 2e-6 * sum_k |a*b| of the exact sum.
+ *
+ * workspace: device scratch of at least oop_out_prod_workspace_size(...)
+ * bytes, 256-byte aligned (NULL allowed when that size is 0).  Its contents on
+ * entry do not matter; the call may overwrite all of it.  Two calls in flight
+ * at once must not share one workspace.
+ */
+size_t oop_out_prod_workspace_size(int a_type, const int64_t ne_a[4],
+                                   const int64_t ne_b[4]);
+
+int oop_out_prod(const void *a, int a_type, const float *b, float *dst,
+                 const int64_t ne_a[4], const int64_t ne_b[4],
+                 const int64_t ne_dst[4], void *workspace,
+                 size_t workspace_bytes, void *stream);
+
+/* oop_out_prod with the kernel chosen by the caller (oop_path); a path that
+ * cannot take the call returns OOP_ERR_PATH.  The workspace rule is the same
+ * (oop_out_prod_workspace_size covers every path). */
+int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst,
+                    const int64_t ne_a[4], const int64_t ne_b[4],
+                    const int64_t ne_dst[4], void *workspace,
+                    size_t workspace_bytes, void *stream, int path);
+
+/*
+ * MUL_MAT_ID_BACK, the MoE input gradient ("Metal kernel_mul_mat_id_back",
+ * first bullet): for every routed slot (i, t) with expert e = ids[i, t],
+ *
+ *   dx[k, i, t] = sum_r W[k, r, e] * g[r, i, t]
+ *
+ *   ne_w   = {K, N, E}             W: f32 or bf16, k fastest
+ *   ne_ids = {n_used, n_tokens}    ids: int32, slot i fastest
+ *   g:  f32 {N, n_used, n_tokens}
+ *   dx: f32 {K, n_used, n_tokens}, OVERWRITTEN; one writer per element.
+ *
+ * An id outside [0, E) zeroes that slot's dx and records OOP_ERR_BAD_ID in the
+ * device status word.  workspace as for oop_out_prod.
+ */
+size_t oop_mul_mat_id_back_workspace_size(int w_type, const int64_t ne_w[3],
+                                          const int64_t ne_ids[2]);
+
+int oop_mul_mat_id_back(const void *W, int w_type, const int32_t *ids,
+                        const float *g, float *dx, const int64_t ne_w[3],
+                        const int64_t ne_ids[2], void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream`, then returns the current device's status word
+ * (OOP_OK, or the first device-side error recorded since it was last
+ * cleared); clears it when `clear` is non-zero.  Returns OOP_ERR_CUDA if the
+ * synchronisation itself fails. */
+int oop_device_status(void *stream, int clear);
+
+/* A static English description of a status code. */
+const char *oop_status_string(int status);
+
+/* Library version, (major << 16) | minor. */
+int oop_version(void);
+
+/* Test hook for the device-side failure path (no counterpart on the pages).
+ * With enable != 0, the NEXT tensor-core OUT_PROD launch on this process
+ * skips one of its TMA copies, so its MMA thread's bounded wait runs out
+ * (after about one second); the kernel then records OOP_ERR_DEVICE_TIMEOUT in
+ * the device status word, releases its tensor memory and returns without
+ * trapping.  dst is left unspecified by that call.  The flag is consumed by
+ * that one launch.  Returns OOP_OK. */
+int oop_debug_inject_timeout(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OOP_H */
