@@ -17,11 +17,15 @@
 //     broadcast and narrow shapes on the GPU").
 //
 // Tile kernel roles (448 threads):
-//  warp 0      TMA: bhi/blo tiles (32 k x 128 n, 128-byte swizzle) -> smem
+//  warp 0      TMA: raw src0 rows (32 k x one m-tile of f32 words or q8_0 /
+//              q4_0 blocks) into a ring, bhi/blo tiles (32 k x 128 n,
+//              128-byte swizzle) into the operand stages
 //  warp 1      TMEM allocation; one thread issues tcgen05.mma (M128 N128 K8)
-//  warps 2-5   src0 producer: load, dequantise, split, write the K-major
-//              swizzled A images a_hi / a_lo to smem
+//  warps 2-5   src0 producer: raw ring -> dequantise -> split -> the K-major
+//              swizzled A images a_hi / a_lo of the operand stage
 //  warps 6-13  fold + epilogue: TMEM -> registers -> dst
+// When src0's rows are not 16-byte aligned (TMA's rule), the producer loads
+// src0 from global memory itself instead of from the ring.
 //
 // Accumulation.  The tensor core adds each MMA's products into its fp32
 // accumulator with an error of up to about one ulp of the accumulator (it
@@ -63,19 +67,55 @@ constexpr int STAGE_BYTES = 2 * A_IMG + 2 * B_IMG;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_D2 = 2 * BN, COL_S = 3 * BN;
 constexpr uint64_t WAIT_NS = 1000000000ull;
+constexpr int MAX_RSTAGES = 4;
+
+// Raw src0 staging per type: one TMA box covers 32 k rows of one m-tile.
+// Quantised rows: the tile's 4 blocks (136 or 72 bytes) start 0 or 8 bytes
+// past a 16-byte boundary, so the box is 8 bytes wider than the blocks.
+template <int TYPE>
+struct RawA;
+template <>
+struct RawA<OOP_TYPE_F32> {
+    static constexpr int BLOCK = 0;
+    static constexpr int BOX_X = BM;                 // f32 elements
+    static constexpr int ROW_BYTES = BM * 4;         // bytes per staged k row
+    static constexpr int SLOT = ROW_BYTES * BK;      // 16 KB
+    static constexpr int RSTAGES = 2;
+};
+template <>
+struct RawA<OOP_TYPE_Q8_0> {
+    static constexpr int BLOCK = kQ8Bytes;
+    static constexpr int BOX_X = 4 * kQ8Bytes + 8;   // 144 bytes
+    static constexpr int ROW_BYTES = BOX_X;
+    static constexpr int SLOT = 5120;                // 144 * 32 rounded to 1 KB
+    static constexpr int RSTAGES = 4;
+};
+template <>
+struct RawA<OOP_TYPE_Q4_0> {
+    static constexpr int BLOCK = kQ4Bytes;
+    static constexpr int BOX_X = 4 * kQ4Bytes + 8;   // 80 bytes
+    static constexpr int ROW_BYTES = BOX_X;
+    static constexpr int SLOT = 3072;                // 80 * 32 rounded to 1 KB
+    static constexpr int RSTAGES = 4;
+};
 
 struct Bars {
-    uint64_t bfull[STAGES];   // TMA bytes of stage s landed
-    uint64_t afull[STAGES];   // the 128 src0-producer threads wrote stage s
-    uint64_t empty[STAGES];   // MMAs reading stage s completed
-    uint64_t accf[2];         // D1 buffer b holds a finished chunk
-    uint64_t acce[2];         // D1 buffer b was drained by the fold
+    uint64_t bfull[STAGES];       // TMA bytes of operand stage s landed
+    uint64_t afull[STAGES];       // the 128 src0-producer threads wrote stage s
+    uint64_t empty[STAGES];       // MMAs reading stage s completed
+    uint64_t rfull[MAX_RSTAGES];  // raw src0 slot r landed
+    uint64_t rempty[MAX_RSTAGES]; // raw src0 slot r consumed by the producer
+    uint64_t accf[2];             // D1 buffer b holds a finished chunk
+    uint64_t acce[2];             // D1 buffer b was drained by the fold
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + sizeof(Bars) + 1024;
+template <int TYPE>
+constexpr size_t smem_bytes() {
+    return STAGES * STAGE_BYTES + RawA<TYPE>::RSTAGES * RawA<TYPE>::SLOT + sizeof(Bars) + 1024;
+}
 
 struct TcParams {
     const uint8_t *a;
@@ -104,14 +144,38 @@ __device__ __forceinline__ float load_a(const uint8_t *row, int64_t m) {
     }
 }
 
+// Element r (row of the m-tile) of a staged raw k row.  `off0` is where the
+// tile's first block starts inside the staged row.
 template <int TYPE>
+__device__ __forceinline__ float staged_a(const uint8_t *srow, int r, int off0) {
+    if constexpr (TYPE == OOP_TYPE_F32) {
+        return reinterpret_cast<const float *>(srow)[r];
+    } else if constexpr (TYPE == OOP_TYPE_Q8_0) {
+        const uint8_t *blk = srow + off0 + (r >> 5) * kQ8Bytes;
+        const uint16_t d = *reinterpret_cast<const uint16_t *>(blk);
+        const int8_t q = static_cast<int8_t>(blk[2 + (r & 31)]);
+        return half_bits_to_float(d) * static_cast<float>(q);
+    } else {
+        const uint8_t *blk = srow + off0 + (r >> 5) * kQ4Bytes;
+        const uint16_t d = *reinterpret_cast<const uint16_t *>(blk);
+        const int j = r & 31;
+        const uint8_t byte = blk[2 + (j & 15)];
+        const int v = j < 16 ? (byte & 0x0f) : (byte >> 4);
+        return half_bits_to_float(d) * static_cast<float>(v - 8);
+    }
+}
+
+template <int TYPE, bool TMA_A>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_out_prod_kernel(const __grid_constant__ CUtensorMap map_bhi,
-                       const __grid_constant__ CUtensorMap map_blo, const TcParams p) {
+                       const __grid_constant__ CUtensorMap map_blo,
+                       const __grid_constant__ CUtensorMap map_a, const TcParams p) {
+    using Raw = RawA<TYPE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Bars *bars = reinterpret_cast<Bars *>(smem + STAGES * STAGE_BYTES);
+    uint8_t *ring = smem + STAGES * STAGE_BYTES;
+    Bars *bars = reinterpret_cast<Bars *>(ring + Raw::RSTAGES * Raw::SLOT);
     volatile int *abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5;
@@ -121,13 +185,27 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t slice = blockIdx.y;
     const int64_t i2 = slice % p.ne12, i3 = slice / p.ne12;
     const int64_t j2 = i2 / p.dps2, j3 = i3 / p.dps3;
+    const int64_t a_row0 = (j3 * p.ne02 + j2) * p.K;     // first src0 row of the slice
     const int nchunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
+    // where this m-tile starts inside a raw row
+    int box_x = 0, off0 = 0;
+    if constexpr (TYPE == OOP_TYPE_F32) {
+        box_x = mt * BM;
+    } else {
+        const int byte0 = mt * 4 * Raw::BLOCK;
+        box_x = byte0 & ~15;
+        off0 = byte0 - box_x;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&bars->bfull[s], 1);
             ptx::mbar_init(&bars->afull[s], 128);
             ptx::mbar_init(&bars->empty[s], 1);
+        }
+        for (int r = 0; r < Raw::RSTAGES; ++r) {
+            ptx::mbar_init(&bars->rfull[r], 1);
+            ptx::mbar_init(&bars->rempty[r], 128);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&bars->accf[b], 1);
@@ -140,6 +218,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&map_bhi);
         ptx::prefetch_tmap(&map_blo);
+        if constexpr (TMA_A) ptx::prefetch_tmap(&map_a);
     }
     if (warp == 1) {
         ptx::tmem_alloc(&bars->tmem_base, TMEM_COLS);
@@ -152,11 +231,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool timed_out = false;
 
     if (warp == 0) {
-        // ---------------- TMA producer: B tiles ----------------
+        // ---------------- TMA producer ----------------
         if (lane == 0) {
-            int last_kb[STAGES];
-            for (int s = 0; s < STAGES; ++s) last_kb[s] = -1;
+            int last_b[STAGES], last_r[MAX_RSTAGES];
+            for (int s = 0; s < STAGES; ++s) last_b[s] = -1;
+            for (int r = 0; r < MAX_RSTAGES; ++r) last_r[r] = -1;
             for (int kb = 0; kb < p.num_kb; ++kb) {
+                if constexpr (TMA_A) {
+                    const int r = kb % Raw::RSTAGES;
+                    const uint32_t rph = (kb / Raw::RSTAGES) & 1;
+                    if (!ptx::mbar_wait_bounded(&bars->rempty[r], rph ^ 1, abort, true, WAIT_NS,
+                                                &timed_out))
+                        break;
+                    ptx::mbar_arrive_expect_tx(&bars->rfull[r],
+                                               static_cast<uint32_t>(Raw::ROW_BYTES * BK));
+                    ptx::tma_load_2d(ring + r * Raw::SLOT, &map_a, &bars->rfull[r], box_x,
+                                     static_cast<int>(a_row0 + static_cast<int64_t>(kb) * BK));
+                    last_r[r] = kb;
+                }
                 const int s = kb % STAGES;
                 const uint32_t ph = (kb / STAGES) & 1;
                 if (!ptx::mbar_wait_bounded(&bars->empty[s], ph ^ 1, abort, true, WAIT_NS,
@@ -169,13 +261,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                                  static_cast<int>(slice));
                 ptx::tma_load_3d(st + 2 * A_IMG + B_IMG, &map_blo, &bars->bfull[s], kb * BK,
                                  nt * BN, static_cast<int>(slice));
-                last_kb[s] = kb;
+                last_b[s] = kb;
             }
             // copies in flight must land before the CTA's smem is released
             for (int s = 0; s < STAGES; ++s)
-                if (last_kb[s] >= 0)
-                    ptx::mbar_wait_bounded(&bars->bfull[s], (last_kb[s] / STAGES) & 1, abort,
+                if (last_b[s] >= 0)
+                    ptx::mbar_wait_bounded(&bars->bfull[s], (last_b[s] / STAGES) & 1, abort,
                                            false, WAIT_NS, &timed_out);
+            for (int r = 0; r < Raw::RSTAGES; ++r)
+                if (last_r[r] >= 0)
+                    ptx::mbar_wait_bounded(&bars->rfull[r], (last_r[r] / Raw::RSTAGES) & 1,
+                                           abort, false, WAIT_NS, &timed_out);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -236,15 +332,31 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r = (warp - 2) * 32 + lane;              // row of the A image
         const int64_t m = static_cast<int64_t>(mt) * BM + r;
         const bool mok = m < p.M;
-        const uint8_t *a_slice = p.a + (j3 * p.ne02 + j2) * p.K * p.a_row_bytes;
+        const uint8_t *a_slice = p.a + a_row0 * p.a_row_bytes;
         for (int kb = 0; kb < p.num_kb; ++kb) {
             const int s = kb % STAGES;
             const uint32_t ph = (kb / STAGES) & 1;
             float x[BK];
+            if constexpr (TMA_A) {
+                const int rs = kb % Raw::RSTAGES;
+                const uint32_t rph = (kb / Raw::RSTAGES) & 1;
+                if (!ptx::mbar_wait_bounded(&bars->rfull[rs], rph, abort, true, WAIT_NS,
+                                            &timed_out))
+                    break;
+                const uint8_t *slot = ring + rs * Raw::SLOT;
 #pragma unroll
-            for (int j = 0; j < BK; ++j) {
-                const int64_t k = static_cast<int64_t>(kb) * BK + j;
-                x[j] = (mok && k < p.K) ? load_a<TYPE>(a_slice + k * p.a_row_bytes, m) : 0.f;
+                for (int j = 0; j < BK; ++j) {
+                    const int64_t k = static_cast<int64_t>(kb) * BK + j;
+                    const float v = staged_a<TYPE>(slot + j * Raw::ROW_BYTES, r, off0);
+                    x[j] = (mok && k < p.K) ? v : 0.f;
+                }
+                ptx::mbar_arrive(&bars->rempty[rs]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < BK; ++j) {
+                    const int64_t k = static_cast<int64_t>(kb) * BK + j;
+                    x[j] = (mok && k < p.K) ? load_a<TYPE>(a_slice + k * p.a_row_bytes, m) : 0.f;
+                }
             }
             if (!ptx::mbar_wait_bounded(&bars->empty[s], ph ^ 1, abort, true, WAIT_NS,
                                         &timed_out))
@@ -379,7 +491,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap *map, void *base, int64_t Kp, int64_t N, int64_t slices) {
+// bhi / blo: [slices][N][Kp] words, boxes of 32 k x 128 n, 128-byte swizzle.
+bool make_b_map(CUtensorMap *map, void *base, int64_t Kp, int64_t N, int64_t slices) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(Kp), static_cast<cuuint64_t>(N),
@@ -394,6 +507,31 @@ bool make_map(CUtensorMap *map, void *base, int64_t Kp, int64_t N, int64_t slice
            CUDA_SUCCESS;
 }
 
+// raw src0: rows of `a_row_bytes` (all slices stacked), boxes of 32 rows.
+template <int TYPE>
+bool make_a_map(CUtensorMap *map, const void *base, const OutProdShape &s) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int64_t rows = s.K * s.ne02 * s.ne03;
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(RawA<TYPE>::BOX_X), BK};
+    cuuint32_t estr[2] = {1, 1};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.a_row_bytes)};
+    if constexpr (TYPE == OOP_TYPE_F32) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.M), static_cast<cuuint64_t>(rows)};
+        return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    } else {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.a_row_bytes),
+                              static_cast<cuuint64_t>(rows)};
+        return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+}
+
 int64_t padded_k(int64_t K) { return (K + 3) / 4 * 4; }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -404,10 +542,35 @@ int g_inject = 0;
 #endif
 int g_chunk_kb = OOP_TC_CHUNK_KB;      // k-blocks (of 32) per D1 accumulation
 
+template <int TYPE>
+cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap &mhi,
+                         const CUtensorMap &mlo, const TcParams &p, int64_t grid_x,
+                         int64_t slices, cudaStream_t stream) {
+    // TMA needs a 16-byte aligned base and row stride, and rows that fit int32.
+    const bool tma_a = reinterpret_cast<uintptr_t>(a) % 16 == 0 && s.a_row_bytes % 16 == 0 &&
+                       s.K * s.ne02 * s.ne03 < (1LL << 31);
+    CUtensorMap ma;
+    if (tma_a) {
+        if (!make_a_map<TYPE>(&ma, a, s)) return cudaErrorInvalidValue;
+    } else {
+        ma = mhi;   // unused by the kernel
+    }
+    constexpr size_t smem = smem_bytes<TYPE>();
+    static_assert(smem <= 232448, "shared memory budget");
+    auto run = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        kern<<<dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(slices)), THREADS, smem,
+               stream>>>(mhi, mlo, ma, p);
+        return cudaGetLastError();
+    };
+    return tma_a ? run(tc_out_prod_kernel<TYPE, true>) : run(tc_out_prod_kernel<TYPE, false>);
+}
+
 }  // namespace
 
 void tc_set_inject(int v) { g_inject = v; }
-void tc_set_chunk_kb(int v) { g_chunk_kb = v < 1 ? 1 : v; }
 
 size_t tc_workspace_bytes(const OutProdShape &s) {
     const size_t one = align256(static_cast<size_t>(s.ne12 * s.ne13) *
@@ -432,7 +595,7 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     if (e != cudaSuccess) return e;
 
     CUtensorMap mhi, mlo;
-    if (!make_map(&mhi, bhi, Kp, s.N, slices) || !make_map(&mlo, blo, Kp, s.N, slices))
+    if (!make_b_map(&mhi, bhi, Kp, s.N, slices) || !make_b_map(&mlo, blo, Kp, s.N, slices))
         return cudaErrorInvalidValue;
 
     TcParams p = {};
@@ -447,29 +610,25 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     p.dps2 = s.dps2;
     p.dps3 = s.dps3;
     p.a_row_bytes = s.a_row_bytes;
-    p.num_kb = static_cast<int>((s.K + BK - 1) / BK);
-    p.chunk_kb = g_chunk_kb;
     const int64_t mtiles = (s.M + BM - 1) / BM, ntiles = (s.N + BN - 1) / BN;
     if (mtiles * ntiles > 0x7fffffffLL || (s.K + BK - 1) / BK > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
+    p.num_kb = static_cast<int>((s.K + BK - 1) / BK);
+    p.chunk_kb = g_chunk_kb;
     p.mtiles = static_cast<int>(mtiles);
     p.ntiles = static_cast<int>(ntiles);
     p.inject = g_inject;
     g_inject = 0;
 
-    auto launch = [&](auto kern) -> cudaError_t {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(SMEM_BYTES));
-        if (err != cudaSuccess) return err;
-        kern<<<dim3(static_cast<unsigned>(mtiles * ntiles), static_cast<unsigned>(slices)),
-               THREADS, SMEM_BYTES, stream>>>(mhi, mlo, p);
-        return cudaGetLastError();
-    };
     switch (s.a_type) {
-    case OOP_TYPE_F32: return launch(tc_out_prod_kernel<OOP_TYPE_F32>);
-    case OOP_TYPE_Q8_0: return launch(tc_out_prod_kernel<OOP_TYPE_Q8_0>);
-    case OOP_TYPE_Q4_0: return launch(tc_out_prod_kernel<OOP_TYPE_Q4_0>);
-    default: return cudaErrorInvalidValue;
+    case OOP_TYPE_F32:
+        return launch_typed<OOP_TYPE_F32>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
+    case OOP_TYPE_Q8_0:
+        return launch_typed<OOP_TYPE_Q8_0>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
+    case OOP_TYPE_Q4_0:
+        return launch_typed<OOP_TYPE_Q4_0>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
+    default:
+        return cudaErrorInvalidValue;
     }
 }
 
