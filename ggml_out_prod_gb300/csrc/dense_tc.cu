@@ -152,16 +152,16 @@ __device__ __forceinline__ float staged_a(const uint8_t *srow, int r, int off0) 
         return reinterpret_cast<const float *>(srow)[r];
     } else if constexpr (TYPE == OOP_TYPE_Q8_0) {
         const uint8_t *blk = srow + off0 + (r >> 5) * kQ8Bytes;
-        const uint16_t d = *reinterpret_cast<const uint16_t *>(blk);
-        const int8_t q = static_cast<int8_t>(blk[2 + (r & 31)]);
-        return half_bits_to_float(d) * static_cast<float>(q);
+        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
+        const int q = static_cast<int8_t>(blk[2 + (r & 31)]);
+        return ptx::scaled_small_int(d, q);
     } else {
         const uint8_t *blk = srow + off0 + (r >> 5) * kQ4Bytes;
-        const uint16_t d = *reinterpret_cast<const uint16_t *>(blk);
+        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
         const int j = r & 31;
         const uint8_t byte = blk[2 + (j & 15)];
         const int v = j < 16 ? (byte & 0x0f) : (byte >> 4);
-        return half_bits_to_float(d) * static_cast<float>(v - 8);
+        return ptx::scaled_small_int(d, v - 8);
     }
 }
 
@@ -337,6 +337,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int s = kb % STAGES;
             const uint32_t ph = (kb / STAGES) & 1;
             float x[BK];
+            const bool kfull = (kb + 1) * BK <= p.K;
             if constexpr (TMA_A) {
                 const int rs = kb % Raw::RSTAGES;
                 const uint32_t rph = (kb / Raw::RSTAGES) & 1;
@@ -344,12 +345,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                                             &timed_out))
                     break;
                 const uint8_t *slot = ring + rs * Raw::SLOT;
+                // one path per warp: the producer warps never diverge
+                if (__all_sync(0xffffffffu, mok) && kfull) {
 #pragma unroll
-                for (int j = 0; j < BK; ++j) {
-                    const int64_t k = static_cast<int64_t>(kb) * BK + j;
-                    const float v = staged_a<TYPE>(slot + j * Raw::ROW_BYTES, r, off0);
-                    x[j] = (mok && k < p.K) ? v : 0.f;
+                    for (int j = 0; j < BK; ++j)
+                        x[j] = staged_a<TYPE>(slot + j * Raw::ROW_BYTES, r, off0);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < BK; ++j) {
+                        const int64_t k = static_cast<int64_t>(kb) * BK + j;
+                        const float v = staged_a<TYPE>(slot + j * Raw::ROW_BYTES, r, off0);
+                        x[j] = (mok && k < p.K) ? v : 0.f;
+                    }
                 }
+                __syncwarp();
                 ptx::mbar_arrive(&bars->rempty[rs]);
             } else {
 #pragma unroll
@@ -358,20 +367,32 @@ __global__ void __launch_bounds__(THREADS, 1)
                     x[j] = (mok && k < p.K) ? load_a<TYPE>(a_slice + k * p.a_row_bytes, m) : 0.f;
                 }
             }
+            __syncwarp();
             if (!ptx::mbar_wait_bounded(&bars->empty[s], ph ^ 1, abort, true, WAIT_NS,
                                         &timed_out))
                 break;
+            __syncwarp();
             uint8_t *ahi = smem + s * STAGE_BYTES;
             uint8_t *alo = ahi + A_IMG;
 #pragma unroll
             for (int c = 0; c < BK / 4; ++c) {
                 uint32_t h[4], l[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ptx::split_tf32(x[4 * c + e], h[e], l[e]);
+                for (int e = 0; e < 4; ++e) {
+                    if constexpr (TYPE == OOP_TYPE_F32) {
+                        ptx::split_tf32(x[4 * c + e], h[e], l[e]);
+                    } else {
+                        // d*q has at most 18 significant bits: x - hi is
+                        // already a TF32 value, no second rounding needed
+                        h[e] = ptx::tf32_round_bits(__float_as_uint(x[4 * c + e]));
+                        l[e] = __float_as_uint(x[4 * c + e] - __uint_as_float(h[e]));
+                    }
+                }
                 const int off = r * 128 + ((c ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4 *>(ahi + off) = make_uint4(h[0], h[1], h[2], h[3]);
                 *reinterpret_cast<uint4 *>(alo + off) = make_uint4(l[0], l[1], l[2], l[3]);
             }
+            __syncwarp();
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(&bars->afull[s]);
         }
@@ -383,9 +404,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t col0 = static_cast<uint32_t>(64 * half);
         const int64_t m = static_cast<int64_t>(mt) * BM + 32 * quad + lane;
         float *dst = p.dst + slice * p.N * p.M;
-        float cmp[64];
+        uint64_t cmp[32];                                   // Kahan compensations, in pairs
 #pragma unroll
-        for (int j = 0; j < 64; ++j) cmp[j] = 0.f;
+        for (int j = 0; j < 32; ++j) cmp[j] = 0;
         for (int q = 0; q < nchunks; ++q) {
             const int buf = q & 1;
             const uint32_t use = static_cast<uint32_t>(q >> 1);
@@ -397,40 +418,54 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int pc = 0; pc < 4; ++pc) {
                 const uint32_t col = col0 + pc * 16;
-                uint32_t xv[16], sv[16], dv[16];
-                ptx::tmem_ld16(tmem + lane_off + buf * BN + col, xv);
-                if (!first) ptx::tmem_ld16(tmem + lane_off + COL_S + col, sv);
-                if (last) ptx::tmem_ld16(tmem + lane_off + COL_D2 + col, dv);
-                ptx::tmem_wait_ld();
+                // tcgen05.ld/st are warp-collective (.sync.aligned): the lanes
+                // must be converged after the divergent stores of the last piece
+                __syncwarp();
+                uint32_t xv[16], sv[16];
+                if (first)
+                    ptx::tmem_ld16_wait(tmem + lane_off + buf * BN + col, xv);
+                else
+                    ptx::tmem_ld16x2_wait(tmem + lane_off + buf * BN + col, xv,
+                                          tmem + lane_off + COL_S + col, sv);
+                if (!first) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    float sj;
-                    if (first) {
-                        sj = __uint_as_float(xv[j]);
-                    } else {
-                        // Kahan: the running sum is S - C
-                        const float s0 = __uint_as_float(sv[j]);
-                        const float y = __uint_as_float(xv[j]) - cmp[pc * 16 + j];
-                        const float t = s0 + y;
-                        cmp[pc * 16 + j] = (t - s0) - y;
-                        sj = t;
+                    for (int j = 0; j < 16; j += 2) {
+                        // Kahan on two columns at once: the running sum is S - C
+                        uint64_t &c2 = cmp[pc * 8 + j / 2];
+                        const uint64_t s2 = ptx::pack2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1]));
+                        const uint64_t x2 = ptx::pack2(__uint_as_float(xv[j]), __uint_as_float(xv[j + 1]));
+                        const uint64_t y2 = ptx::sub2(x2, c2);
+                        const uint64_t t2 = ptx::add2(s2, y2);
+                        c2 = ptx::sub2(ptx::sub2(t2, s2), y2);
+                        float t0, t1;
+                        ptx::unpack2(t2, t0, t1);
+                        xv[j] = __float_as_uint(t0);
+                        xv[j + 1] = __float_as_uint(t1);
                     }
-                    sv[j] = __float_as_uint(sj);
                 }
+                // xv now holds S for these 16 columns
                 if (last) {
+                    uint32_t (&dv)[16] = sv;                // D2, the cross terms
+                    __syncwarp();
+                    ptx::tmem_ld16_wait(tmem + lane_off + COL_D2 + col, dv);
                     if (m < p.M) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
+                        for (int j = 0; j < 16; j += 2) {
+                            float c0, c1;
+                            ptx::unpack2(cmp[pc * 8 + j / 2], c0, c1);
                             const int64_t n = static_cast<int64_t>(nt) * BN + col + j;
                             if (n < p.N)
-                                dst[n * p.M + m] = __uint_as_float(sv[j]) +
-                                                   (__uint_as_float(dv[j]) - cmp[pc * 16 + j]);
+                                dst[n * p.M + m] = __uint_as_float(xv[j]) + (__uint_as_float(dv[j]) - c0);
+                            if (n + 1 < p.N)
+                                dst[(n + 1) * p.M + m] =
+                                    __uint_as_float(xv[j + 1]) + (__uint_as_float(dv[j + 1]) - c1);
                         }
                     }
                 } else {
-                    ptx::tmem_st16(tmem + lane_off + COL_S + col, sv);
+                    ptx::tmem_st16(tmem + lane_off + COL_S + col, xv);
                 }
             }
+            __syncwarp();
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bars->acce[buf]);

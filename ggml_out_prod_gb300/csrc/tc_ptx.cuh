@@ -42,12 +42,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
+    // The suspend-time hint lets a waiting thread sleep in hardware (it wakes
+    // when the phase completes) instead of re-issuing the test.
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
         : "memory");
     return ok != 0;
 }
@@ -62,7 +64,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31) == 0) {
+        if ((it & 3) == 0) {
             if (honor_abort && *abort) return false;
             if (globaltimer() - t0 > limit_ns) {
                 *abort = 1;
@@ -203,6 +205,39 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+// tcgen05.ld fills its destination registers asynchronously; the compiler
+// cannot see that, so the load and its wait sit in ONE asm statement and the
+// registers are defined only once the data is there.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Two 16-column loads, one wait.
+__device__ __forceinline__ void tmem_ld16x2_wait(uint32_t ta, uint32_t (&a)[16], uint32_t tb,
+                                                 uint32_t (&b)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]),
+          "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]),
+          "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]),
+          "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]),
+          "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -236,13 +271,57 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
 
 // ---- numerics ---------------------------------------------------------------
 
+// Round an fp32 bit pattern to the nearest TF32 value, ties away from zero:
+// add half of the lowest kept bit (bit 13) to the magnitude, clear the 13
+// dropped bits.  Exact integer arithmetic on the full-rate ALU; valid for
+// every finite x below 2^128 * (1 - 2^-12) in magnitude.
+__device__ __forceinline__ uint32_t tf32_round_bits(uint32_t xb) {
+    return (xb + 0x1000u) & 0xFFFFE000u;
+}
+
 // x = hi + lo + r with hi, lo TF32 (low 13 bits zero): hi = x rounded to
 // nearest TF32, lo = (x - hi) rounded to nearest TF32 (x - hi is exact in
 // f32), |r| <= 2^-22 |x|.  Never passes through a 16-bit format.
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    hi = tf32_round_bits(__float_as_uint(x));
     const float rest = x - __uint_as_float(hi);
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(rest));
+    lo = tf32_round_bits(__float_as_uint(rest));
+}
+
+// Two fp32 lanes in one 64-bit register (sm_100 packed arithmetic).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// A small integer (|v| < 2^22) as float: place it in the mantissa of
+// 1.5 * 2^23 (whose ulp is 1) and subtract that constant.  Exact.
+__device__ __forceinline__ float small_int_to_float(int v) {
+    return __int_as_float(0x4B400000 + v) - 12582912.0f;
+}
+
+// d * v for a small integer v, exactly: with f = 1.5 * 2^23 + v (exact),
+// d * f - d * 1.5 * 2^23 is formed in one fused multiply-add, whose single
+// rounding is exact because d * v fits in fp32 (d has 11 significant bits).
+__device__ __forceinline__ float scaled_small_int(float d, int v) {
+    return fmaf(d, __int_as_float(0x4B400000 + v), d * -12582912.0f);
 }
 
 }  // namespace ptx

@@ -137,6 +137,27 @@ def test_edge_shapes_f32(op, orc, ne_a, ne_b):
     _check_whole(op, orc, a, F32, b, ne_a, ne_b, what=f"edge {ne_a} {ne_b}")
 
 
+@pytest.mark.parametrize("tid,M,K,N", [(F32, 300, 1000, 130), (F32, 300, 1024, 256),
+                                       (Q8, 320, 300, 200), (Q4, 288, 200, 70)])
+def test_ragged_tiles_repeatable(op, orc, tid, M, K, N):
+    """Ragged m-, n- and k-tiles on the tensor-core path: every repeat inside
+    the bound and bit-identical to the first (the summation order is fixed)."""
+    import torch
+    ne_a, ne_b = (M, K, 1, 1), (N, K, 1, 1)
+    a = synth.make_a(tid, ne_a, 90, std=0.02 if tid != F32 else 1.0)
+    b = synth.make_b(ne_b, 91, std=1e3 if tid != F32 else 1.0, outliers=True)
+    ref = orc.out_prod(a, tid, b, ne_a, ne_b)
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    first = None
+    for _ in range(12):
+        out = op.out_prod(ta, tb, a_type=tid, ne_a=ne_a, path=op.PATH_TCGEN05).cpu().numpy()
+        assert_parity(out, ref["f64"], ref["abs"], f"ragged {tid} {M}x{K}x{N}")
+        if first is None:
+            first = out
+        else:
+            assert np.array_equal(first.view(np.uint32), out.view(np.uint32)), "not repeatable"
+
+
 def test_integer_inputs_exact(op, orc):
     rng = np.random.default_rng(3)
     ne_a, ne_b = (96, 77, 2, 1), (20, 77, 4, 1)
