@@ -57,13 +57,17 @@ EXPORTS = (
     "oop_out_prod", "oop_out_prod_ex", "oop_out_prod_workspace_size",
     "oop_mul_mat_id_back", "oop_mul_mat_id_back_workspace_size",
     "oop_device_status", "oop_status_string", "oop_version", "oop_debug_inject_timeout",
+    "oop_last_cuda_error",
 )
 
 
 class OopError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} ({status})")
+        msg = f"{where}: {status_string(status)} ({status})"
+        if status == ERR_CUDA:
+            msg += ": " + lib().oop_last_cuda_error().decode()
+        super().__init__(msg)
 
 
 def library_path() -> str:
@@ -104,6 +108,8 @@ def lib():
             L.oop_status_string.argtypes = [ctypes.c_int]
             L.oop_version.restype = ctypes.c_int
             L.oop_version.argtypes = []
+            L.oop_last_cuda_error.restype = ctypes.c_char_p
+            L.oop_last_cuda_error.argtypes = []
             L.oop_debug_inject_timeout.restype = ctypes.c_int
             L.oop_debug_inject_timeout.argtypes = [ctypes.c_int]
             _lib = L

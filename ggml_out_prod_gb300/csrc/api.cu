@@ -109,7 +109,13 @@ size_t workspace_for(const OutProdShape &s, int path) {
     return 0;
 }
 
-int cuda_rc(cudaError_t e) { return e == cudaSuccess ? OOP_OK : OOP_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+int cuda_rc(cudaError_t e) {
+    if (e == cudaSuccess) return OOP_OK;
+    g_last_cuda = e;
+    return OOP_ERR_CUDA;
+}
 
 }  // namespace
 }  // namespace oop
@@ -266,6 +272,8 @@ const char *oop_status_string(int status) {
 }
 
 int oop_version(void) { return (0 << 16) | 1; }
+
+const char *oop_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda); }
 
 int oop_debug_inject_timeout(int enable) {
     tc_set_inject(enable ? 1 : 0);

@@ -139,6 +139,10 @@ int oop_device_status(void *stream, int clear);
 /* A static English description of a status code. */
 const char *oop_status_string(int status);
 
+/* The CUDA runtime's description of the error behind the calling thread's
+ * most recent OOP_ERR_CUDA ("no error" if there was none).  Static string. */
+const char *oop_last_cuda_error(void);
+
 /* Library version, (major << 16) | minor. */
 int oop_version(void);
 
