@@ -43,6 +43,7 @@ ERR_BAD_ID = -8
 ERR_DEVICE_TIMEOUT = -9
 ERR_DEVICE = -10
 ERR_PATH = -11
+ERR_SCRATCH_LIMIT = -12
 
 _QK = 32
 _BLOCK_BYTES = {TYPE_Q8_0: 34, TYPE_Q4_0: 18}
@@ -57,7 +58,7 @@ EXPORTS = (
     "oop_out_prod", "oop_out_prod_ex", "oop_out_prod_workspace_size",
     "oop_mul_mat_id_back", "oop_mul_mat_id_back_workspace_size",
     "oop_device_status", "oop_status_string", "oop_version", "oop_debug_inject_timeout",
-    "oop_last_cuda_error",
+    "oop_last_cuda_error", "oop_out_prod_noalloc", "oop_out_prod_noalloc_scratch_bytes",
 )
 
 
@@ -108,6 +109,11 @@ def lib():
             L.oop_status_string.argtypes = [ctypes.c_int]
             L.oop_version.restype = ctypes.c_int
             L.oop_version.argtypes = []
+            L.oop_out_prod_noalloc.restype = ctypes.c_int
+            L.oop_out_prod_noalloc.argtypes = [_vp, ctypes.c_int, _vp, _vp, _i64p, _i64p, _i64p,
+                                               _vp]
+            L.oop_out_prod_noalloc_scratch_bytes.restype = ctypes.c_size_t
+            L.oop_out_prod_noalloc_scratch_bytes.argtypes = []
             L.oop_last_cuda_error.restype = ctypes.c_char_p
             L.oop_last_cuda_error.argtypes = []
             L.oop_debug_inject_timeout.restype = ctypes.c_int
@@ -137,6 +143,12 @@ def oop_out_prod(a, a_type, b, dst, ne_a, ne_b, ne_dst, workspace, workspace_byt
                  path=PATH_AUTO) -> int:
     return int(lib().oop_out_prod_ex(a, int(a_type), b, dst, _ne(ne_a), _ne(ne_b), _ne(ne_dst),
                                      workspace, int(workspace_bytes), stream, int(path)))
+
+
+def oop_out_prod_noalloc(a, a_type, b, dst, ne_a, ne_b, ne_dst, stream) -> int:
+    """OUT_PROD with the library's own fixed device scratch (no allocation)."""
+    return int(lib().oop_out_prod_noalloc(a, int(a_type), b, dst, _ne(ne_a), _ne(ne_b),
+                                          _ne(ne_dst), stream))
 
 
 def oop_mul_mat_id_back_workspace_size(w_type, ne_w, ne_ids) -> int:

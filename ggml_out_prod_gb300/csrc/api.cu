@@ -267,6 +267,7 @@ const char *oop_status_string(int status) {
     case OOP_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
     case OOP_ERR_DEVICE: return "current device is not sm_103";
     case OOP_ERR_PATH: return "the requested kernel cannot take this call";
+    case OOP_ERR_SCRATCH_LIMIT: return "needs more scratch than the library's fixed device array";
     default: return "unknown status";
     }
 }

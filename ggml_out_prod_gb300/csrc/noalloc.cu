@@ -1,0 +1,69 @@
+// noalloc.cu -- OUT_PROD for callers that cannot allocate device memory.
+//
+// The tensor-core OUT_PROD needs scratch for its TF32 split of src1 (two
+// words per element of b).  oop_out_prod takes that scratch from the caller.
+// Some callers cannot hand it over: code that runs inside a framework whose
+// allocator owns all device memory and offers no way to request a temporary
+// buffer, plug-ins called with fixed, pre-sized tensors only, and code paths
+// where a cudaMalloc would synchronise the device or fail (real-time loops,
+// memory budgets fixed at start-up).  oop_out_prod_noalloc serves them: its
+// scratch is a file-scope device array of a fixed size that is part of this
+// library's image, so it exists on every GPU that loads the library and
+// stays there until the process exits.  Nothing here calls cudaMalloc,
+// cudaFree or any allocating routine.
+#include <mutex>
+
+#include "oop_internal.cuh"
+
+namespace oop {
+namespace {
+
+// 64 MiB: the TF32 split of a gradient of up to 8 Mi elements (for example
+// N = 1024, K = 8192, one slice).
+constexpr size_t kScratchBytes = size_t(64) << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void *g_scratch_ptr[kMaxDevices];
+
+// Once per device, with that device current: the device address of the
+// array.  (In host code the array's name is only a host-side stand-in.)
+int scratch_for_current_device(void **ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return OOP_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return OOP_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return OOP_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *ptr = g_scratch_ptr[dev];
+    return OOP_OK;
+}
+
+}  // namespace
+}  // namespace oop
+
+extern "C" {
+
+size_t oop_out_prod_noalloc_scratch_bytes(void) { return oop::kScratchBytes; }
+
+int oop_out_prod_noalloc(const void *a, int a_type, const float *b, float *dst,
+                         const int64_t ne_a[4], const int64_t ne_b[4], const int64_t ne_dst[4],
+                         void *stream) {
+    // Shape errors are reported exactly as oop_out_prod reports them.
+    const size_t need = oop_out_prod_workspace_size(a_type, ne_a, ne_b);
+    if (need > oop::kScratchBytes) return OOP_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    if (need > 0) {
+        const int rc = oop::scratch_for_current_device(&scratch);
+        if (rc != OOP_OK) return rc;
+    }
+    return oop_out_prod(a, a_type, b, dst, ne_a, ne_b, ne_dst, scratch, need, stream);
+}
+
+}  // extern "C"

@@ -58,7 +58,9 @@ typedef enum {
     OOP_ERR_BAD_ID = -8,         /* device: an expert id outside [0, E) */
     OOP_ERR_DEVICE_TIMEOUT = -9, /* device: a bounded wait ran out */
     OOP_ERR_DEVICE = -10,        /* the current device is not sm_103 */
-    OOP_ERR_PATH = -11           /* oop_out_prod_ex: that kernel cannot take this call */
+    OOP_ERR_PATH = -11,          /* oop_out_prod_ex: that kernel cannot take this call */
+    OOP_ERR_SCRATCH_LIMIT = -12  /* oop_out_prod_noalloc: the call needs more scratch
+                                    than the library's fixed device array holds */
 } oop_status;
 
 /* Kernel selection for oop_out_prod_ex. */
@@ -107,6 +109,35 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst,
                     const int64_t ne_a[4], const int64_t ne_b[4],
                     const int64_t ne_dst[4], void *workspace,
                     size_t workspace_bytes, void *stream, int path);
+
+/*
+ * OUT_PROD without any device allocation (no counterpart on the pages: the
+ * Metal op takes its scratch from the ggml graph).  For callers that cannot
+ * allocate device memory or hand the library a scratch buffer -- code inside
+ * a framework whose allocator owns all device memory, plug-ins that only get
+ * fixed pre-sized tensors, loops where a cudaMalloc would synchronise the
+ * device or break a fixed memory budget.
+ *
+ * Same operation, arguments, errors and precision as oop_out_prod, minus the
+ * workspace: the scratch is a 64 MiB device array inside this library
+ * (oop_out_prod_noalloc_scratch_bytes()), present on every GPU that loads the
+ * library until the process exits.  A call whose scratch need
+ * (oop_out_prod_workspace_size) exceeds it returns OOP_ERR_SCRATCH_LIMIT and
+ * enqueues nothing.  The call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *
+ * The first call on a device looks up that array's device address (once per
+ * device, with the device current); make that first call before any stream
+ * capture begins.  Every call on a device shares the one array, and each call
+ * rewrites all of the scratch it reads, so nothing needs clearing between
+ * calls; but two calls that overlap on the GPU (other streams, or another
+ * host thread) race on it -- order them on one stream.
+ */
+size_t oop_out_prod_noalloc_scratch_bytes(void);
+
+int oop_out_prod_noalloc(const void *a, int a_type, const float *b, float *dst,
+                         const int64_t ne_a[4], const int64_t ne_b[4],
+                         const int64_t ne_dst[4], void *stream);
 
 /*
  * MUL_MAT_ID_BACK, the MoE input gradient ("Metal kernel_mul_mat_id_back",

@@ -41,7 +41,7 @@ def test_exports_every_declared_symbol(built):
 
 @needs_nvcc
 def test_status_strings(built):
-    for code in range(-11, 1):
+    for code in range(-12, 1):
         s = built.status_string(code)
         assert s and s != "unknown status"
     assert built.lib().oop_version() >= 1
