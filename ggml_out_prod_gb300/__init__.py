@@ -56,7 +56,7 @@ _vp = ctypes.c_void_p
 
 EXPORTS = (
     "oop_out_prod", "oop_out_prod_ex", "oop_out_prod_workspace_size",
-    "oop_mul_mat_id_back", "oop_mul_mat_id_back_workspace_size",
+    "oop_mul_mat_id_back", "oop_mul_mat_id_back_ex", "oop_mul_mat_id_back_workspace_size",
     "oop_device_status", "oop_status_string", "oop_version", "oop_debug_inject_timeout",
     "oop_last_cuda_error", "oop_out_prod_noalloc", "oop_out_prod_noalloc_scratch_bytes",
 )
@@ -103,6 +103,9 @@ def lib():
             L.oop_mul_mat_id_back.restype = ctypes.c_int
             L.oop_mul_mat_id_back.argtypes = [_vp, ctypes.c_int, _vp, _vp, _vp, _i64p, _i64p,
                                               _vp, ctypes.c_size_t, _vp]
+            L.oop_mul_mat_id_back_ex.restype = ctypes.c_int
+            L.oop_mul_mat_id_back_ex.argtypes = [_vp, ctypes.c_int, _vp, _vp, _vp, _i64p, _i64p,
+                                                 _vp, ctypes.c_size_t, _vp, ctypes.c_int]
             L.oop_device_status.restype = ctypes.c_int
             L.oop_device_status.argtypes = [_vp, ctypes.c_int]
             L.oop_status_string.restype = ctypes.c_char_p
@@ -156,9 +159,9 @@ def oop_mul_mat_id_back_workspace_size(w_type, ne_w, ne_ids) -> int:
 
 
 def oop_mul_mat_id_back(W, w_type, ids, g, dx, ne_w, ne_ids, workspace, workspace_bytes,
-                        stream) -> int:
-    return int(lib().oop_mul_mat_id_back(W, int(w_type), ids, g, dx, _ne(ne_w), _ne(ne_ids),
-                                         workspace, int(workspace_bytes), stream))
+                        stream, path=PATH_AUTO) -> int:
+    return int(lib().oop_mul_mat_id_back_ex(W, int(w_type), ids, g, dx, _ne(ne_w), _ne(ne_ids),
+                                            workspace, int(workspace_bytes), stream, int(path)))
 
 
 def oop_device_status(stream=None, clear=True) -> int:
@@ -245,7 +248,8 @@ def out_prod(a, b, a_type=None, ne_a=None, out=None, workspace=None, stream=None
     return out
 
 
-def mul_mat_id_back(W, ids, g, w_type=None, out=None, workspace=None, stream=None):
+def mul_mat_id_back(W, ids, g, w_type=None, out=None, workspace=None, stream=None,
+                    path=PATH_AUTO):
     """dx = MUL_MAT_ID_BACK(W, ids, g).
 
     W: float32 (E, N, K) or bf16 bits / torch.bfloat16 (E, N, K); ids: int32
@@ -270,7 +274,7 @@ def mul_mat_id_back(W, ids, g, w_type=None, out=None, workspace=None, stream=Non
     ws = _workspace(nws, W.device, workspace)
     rc = oop_mul_mat_id_back(_ptr(W), w_type, _ptr(ids), _ptr(g), _ptr(out), ne_w, ne_ids,
                              _ptr(ws), ws.numel() if ws is not None else 0,
-                             _stream_ptr(stream))
+                             _stream_ptr(stream), path)
     if rc != OK:
         raise OopError(rc, "oop_mul_mat_id_back")
     return out

@@ -196,30 +196,49 @@ int oop_out_prod(const void *a, int a_type, const float *b, float *dst, const in
                            stream, OOP_PATH_AUTO);
 }
 
-size_t oop_mul_mat_id_back_workspace_size(int w_type, const int64_t ne_w[3],
-                                          const int64_t ne_ids[2]) {
-    (void)w_type;
-    (void)ne_w;
-    (void)ne_ids;
-    return 0;
-}
+}  // extern "C"
 
-int oop_mul_mat_id_back(const void *W, int w_type, const int32_t *ids, const float *g, float *dx,
-                        const int64_t ne_w[3], const int64_t ne_ids[2], void *workspace,
-                        size_t workspace_bytes, void *stream) {
-    (void)workspace;
-    (void)workspace_bytes;
+namespace oop {
+namespace {
+
+int check_mmid_shape(int w_type, const int64_t ne_w[3], const int64_t ne_ids[2], MmidShape *s) {
     if (!ne_w || !ne_ids) return OOP_ERR_NULL;
     if (w_type != OOP_TYPE_F32 && w_type != OOP_TYPE_BF16) return OOP_ERR_TYPE;
     for (int i = 0; i < 3; ++i)
         if (ne_w[i] < 0) return OOP_ERR_SHAPE;
     if (ne_ids[0] < 0 || ne_ids[1] < 0) return OOP_ERR_SHAPE;
-    MmidShape s = {ne_w[0], ne_w[1], ne_w[2], ne_ids[0], ne_ids[1], w_type};
+    *s = MmidShape{ne_w[0], ne_w[1], ne_w[2], ne_ids[0], ne_ids[1], w_type};
     const double big = 9.0e18;
-    if (static_cast<double>(s.K) * s.N * s.E * 4.0 > big ||
-        static_cast<double>(s.K) * s.n_used * s.n_tok * 4.0 > big ||
-        static_cast<double>(s.N) * s.n_used * s.n_tok * 4.0 > big)
+    if (static_cast<double>(s->K) * s->N * s->E * 4.0 > big ||
+        static_cast<double>(s->K) * s->n_used * s->n_tok * 4.0 > big ||
+        static_cast<double>(s->N) * s->n_used * s->n_tok * 4.0 > big)
         return OOP_ERR_SHAPE;
+    if (s->E > 6144) return OOP_ERR_SHAPE;        // routing keeps per-expert counts on chip
+    if (s->n_used * s->n_tok > 0x7fffffffLL) return OOP_ERR_SHAPE;
+    return OOP_OK;
+}
+
+}  // namespace
+}  // namespace oop
+
+extern "C" {
+
+size_t oop_mul_mat_id_back_workspace_size(int w_type, const int64_t ne_w[3],
+                                          const int64_t ne_ids[2]) {
+    oop::MmidShape s = {};
+    if (oop::check_mmid_shape(w_type, ne_w, ne_ids, &s) != OOP_OK) return 0;
+    if (s.n_used * s.n_tok == 0 || s.K == 0 || s.E == 0) return 0;
+    return oop::tc_mmid_workspace_bytes(s);
+}
+
+int oop_mul_mat_id_back_ex(const void *W, int w_type, const int32_t *ids, const float *g,
+                           float *dx, const int64_t ne_w[3], const int64_t ne_ids[2],
+                           void *workspace, size_t workspace_bytes, void *stream, int path) {
+    oop::MmidShape s = {};
+    int rc = oop::check_mmid_shape(w_type, ne_w, ne_ids, &s);
+    if (rc != OOP_OK) return rc;
+    if (path != OOP_PATH_AUTO && path != OOP_PATH_TCGEN05 && path != OOP_PATH_SIMT)
+        return OOP_ERR_PATH;
     const int64_t slots = s.n_used * s.n_tok;
     if (slots == 0 || s.K == 0) return OOP_OK;
     if (!dx || !ids) return OOP_ERR_NULL;
@@ -228,14 +247,30 @@ int oop_mul_mat_id_back(const void *W, int w_type, const int32_t *ids, const flo
         if (!W || !g) return OOP_ERR_NULL;
         if (!aligned(g, 4) || !aligned(W, w_type == OOP_TYPE_F32 ? 4 : 2)) return OOP_ERR_ALIGN;
     }
-    if (s.N > 48 * 1024) return OOP_ERR_SHAPE;   // g's slot column is staged on chip
     int *status = nullptr;
-    int rc = device_setup(&status);
+    rc = device_setup(&status);
     if (rc != OOP_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_mmid_per_slot(W, ids, g, dx, s, status, st);
+    const bool per_slot = path == OOP_PATH_SIMT || s.N == 0 || s.E == 0;
+    if (!per_slot) {
+        const size_t need = oop::tc_mmid_workspace_bytes(s);
+        if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+            return OOP_ERR_WORKSPACE;
+        cudaError_t e = oop::launch_mmid_tc(W, ids, g, dx, s, workspace, status, st);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        return cuda_rc(e);
+    }
+    if (s.N > 48 * 1024) return OOP_ERR_SHAPE;   // g's slot column is staged on chip
+    cudaError_t e = oop::launch_mmid_per_slot(W, ids, g, dx, s, status, st);
     if (e == cudaSuccess) e = cudaGetLastError();
     return cuda_rc(e);
+}
+
+int oop_mul_mat_id_back(const void *W, int w_type, const int32_t *ids, const float *g, float *dx,
+                        const int64_t ne_w[3], const int64_t ne_ids[2], void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    return oop_mul_mat_id_back_ex(W, w_type, ids, g, dx, ne_w, ne_ids, workspace,
+                                  workspace_bytes, stream, OOP_PATH_AUTO);
 }
 
 int oop_device_status(void *stream, int clear) {

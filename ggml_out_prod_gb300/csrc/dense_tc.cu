@@ -83,6 +83,14 @@ struct RawA<OOP_TYPE_F32> {
     static constexpr int RSTAGES = 2;
 };
 template <>
+struct RawA<OOP_TYPE_BF16> {
+    static constexpr int BLOCK = 0;
+    static constexpr int BOX_X = BM;                 // bf16 elements
+    static constexpr int ROW_BYTES = BM * 2;
+    static constexpr int SLOT = ROW_BYTES * BK;      // 8 KB
+    static constexpr int RSTAGES = 4;
+};
+template <>
 struct RawA<OOP_TYPE_Q8_0> {
     static constexpr int BLOCK = kQ8Bytes;
     static constexpr int BOX_X = 4 * kQ8Bytes + 8;   // 144 bytes
@@ -113,6 +121,9 @@ struct Bars {
 };
 
 template <int TYPE>
+constexpr bool elementwise_type() { return TYPE == OOP_TYPE_F32 || TYPE == OOP_TYPE_BF16; }
+
+template <int TYPE>
 constexpr size_t smem_bytes() {
     return STAGES * STAGE_BYTES + RawA<TYPE>::RSTAGES * RawA<TYPE>::SLOT + sizeof(Bars) + 1024;
 }
@@ -123,12 +134,21 @@ struct TcParams {
     int *status;
     int64_t M, K, N, ne02, ne12, dps2, dps3, a_row_bytes;
     int num_kb, chunk_kb, mtiles, ntiles, inject;
+    // grouped mode (MUL_MAT_ID_BACK): slices are experts, src1 rows are the
+    // routed slots sorted by expert, dst rows are scattered back to slots
+    const int *grp_count;         // [E] slots routed to each expert
+    const int *grp_offset;        // [E] first sorted slot of each expert
+    const int *grp_rows;          // [slots] sorted slot -> dst row
+    const int *grp_tiles;         // work list: (expert << 16) | n-tile
+    const int *grp_ntiles;        // valid entries in grp_tiles
 };
 
 template <int TYPE>
 __device__ __forceinline__ float load_a(const uint8_t *row, int64_t m) {
     if constexpr (TYPE == OOP_TYPE_F32) {
         return __ldg(reinterpret_cast<const float *>(row) + m);
+    } else if constexpr (TYPE == OOP_TYPE_BF16) {
+        return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short *>(row) + m));
     } else if constexpr (TYPE == OOP_TYPE_Q8_0) {
         const uint8_t *blk = row + (m >> 5) * kQ8Bytes;
         const uint16_t d = __ldg(reinterpret_cast<const unsigned short *>(blk));
@@ -150,6 +170,8 @@ template <int TYPE>
 __device__ __forceinline__ float staged_a(const uint8_t *srow, int r, int off0) {
     if constexpr (TYPE == OOP_TYPE_F32) {
         return reinterpret_cast<const float *>(srow)[r];
+    } else if constexpr (TYPE == OOP_TYPE_BF16) {
+        return bf16_bits_to_float(reinterpret_cast<const uint16_t *>(srow)[r]);
     } else if constexpr (TYPE == OOP_TYPE_Q8_0) {
         const uint8_t *blk = srow + off0 + (r >> 5) * kQ8Bytes;
         const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
@@ -165,7 +187,7 @@ __device__ __forceinline__ float staged_a(const uint8_t *srow, int r, int off0) 
     }
 }
 
-template <int TYPE, bool TMA_A>
+template <int TYPE, bool TMA_A, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_out_prod_kernel(const __grid_constant__ CUtensorMap map_bhi,
                        const __grid_constant__ CUtensorMap map_blo,
@@ -181,15 +203,29 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int mt = blockIdx.x % p.mtiles;
-    const int nt = blockIdx.x / p.mtiles;
-    const int64_t slice = blockIdx.y;
+    int nt;
+    int64_t slice;
+    int64_t ncols = p.N;          // valid columns of this tile's slice
+    int64_t brow0 = 0;            // grouped: first src1 row of this tile
+    if constexpr (GROUPED) {
+        const int t = blockIdx.x / p.mtiles;
+        if (t >= *p.grp_ntiles) return;              // whole CTA: no work left
+        const int packed = p.grp_tiles[t];
+        slice = packed >> 16;
+        nt = packed & 0xFFFF;
+        ncols = p.grp_count[slice];
+        brow0 = p.grp_offset[slice] + static_cast<int64_t>(nt) * BN;
+    } else {
+        nt = blockIdx.x / p.mtiles;
+        slice = blockIdx.y;
+    }
     const int64_t i2 = slice % p.ne12, i3 = slice / p.ne12;
     const int64_t j2 = i2 / p.dps2, j3 = i3 / p.dps3;
     const int64_t a_row0 = (j3 * p.ne02 + j2) * p.K;     // first src0 row of the slice
     const int nchunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
     // where this m-tile starts inside a raw row
     int box_x = 0, off0 = 0;
-    if constexpr (TYPE == OOP_TYPE_F32) {
+    if constexpr (elementwise_type<TYPE>()) {
         box_x = mt * BM;
     } else {
         const int byte0 = mt * 4 * Raw::BLOCK;
@@ -257,10 +293,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (p.inject == 1 && kb == 0) continue;   // test hook: drop one stage
                 uint8_t *st = smem + s * STAGE_BYTES;
                 ptx::mbar_arrive_expect_tx(&bars->bfull[s], 2 * B_IMG);
-                ptx::tma_load_3d(st + 2 * A_IMG, &map_bhi, &bars->bfull[s], kb * BK, nt * BN,
-                                 static_cast<int>(slice));
-                ptx::tma_load_3d(st + 2 * A_IMG + B_IMG, &map_blo, &bars->bfull[s], kb * BK,
-                                 nt * BN, static_cast<int>(slice));
+                if constexpr (GROUPED) {
+                    ptx::tma_load_2d(st + 2 * A_IMG, &map_bhi, &bars->bfull[s], kb * BK,
+                                     static_cast<int>(brow0));
+                    ptx::tma_load_2d(st + 2 * A_IMG + B_IMG, &map_blo, &bars->bfull[s], kb * BK,
+                                     static_cast<int>(brow0));
+                } else {
+                    ptx::tma_load_3d(st + 2 * A_IMG, &map_bhi, &bars->bfull[s], kb * BK,
+                                     nt * BN, static_cast<int>(slice));
+                    ptx::tma_load_3d(st + 2 * A_IMG + B_IMG, &map_blo, &bars->bfull[s], kb * BK,
+                                     nt * BN, static_cast<int>(slice));
+                }
                 last_b[s] = kb;
             }
             // copies in flight must land before the CTA's smem is released
@@ -382,8 +425,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if constexpr (TYPE == OOP_TYPE_F32) {
                         ptx::split_tf32(x[4 * c + e], h[e], l[e]);
                     } else {
-                        // d*q has at most 18 significant bits: x - hi is
-                        // already a TF32 value, no second rounding needed
+                        // d*q has at most 18 significant bits and a bf16 value
+                        // 8: x - hi is already a TF32 value (zero for bf16),
+                        // no second rounding needed
                         h[e] = ptx::tf32_round_bits(__float_as_uint(x[4 * c + e]));
                         l[e] = __float_as_uint(x[4 * c + e] - __uint_as_float(h[e]));
                     }
@@ -403,7 +447,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
         const uint32_t col0 = static_cast<uint32_t>(64 * half);
         const int64_t m = static_cast<int64_t>(mt) * BM + 32 * quad + lane;
-        float *dst = p.dst + slice * p.N * p.M;
+        float *dst = GROUPED ? p.dst : p.dst + slice * p.N * p.M;
+        const int64_t tile_cols = ncols - static_cast<int64_t>(nt) * BN;   // valid columns here
         uint64_t cmp[32];                                   // Kahan compensations, in pairs
 #pragma unroll
         for (int j = 0; j < 32; ++j) cmp[j] = 0;
@@ -453,11 +498,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int j = 0; j < 16; j += 2) {
                             float c0, c1;
                             ptx::unpack2(cmp[pc * 8 + j / 2], c0, c1);
-                            const int64_t n = static_cast<int64_t>(nt) * BN + col + j;
-                            if (n < p.N)
-                                dst[n * p.M + m] = __uint_as_float(xv[j]) + (__uint_as_float(dv[j]) - c0);
-                            if (n + 1 < p.N)
-                                dst[(n + 1) * p.M + m] =
+                            const int64_t jc = static_cast<int64_t>(col) + j;   // column in tile
+                            int64_t r0 = -1, r1 = -1;                            // dst rows
+                            if constexpr (GROUPED) {
+                                if (jc < tile_cols) r0 = p.grp_rows[brow0 + jc];
+                                if (jc + 1 < tile_cols) r1 = p.grp_rows[brow0 + jc + 1];
+                            } else {
+                                if (jc < tile_cols) r0 = static_cast<int64_t>(nt) * BN + jc;
+                                if (jc + 1 < tile_cols) r1 = static_cast<int64_t>(nt) * BN + jc + 1;
+                            }
+                            if (r0 >= 0)
+                                dst[r0 * p.M + m] = __uint_as_float(xv[j]) + (__uint_as_float(dv[j]) - c0);
+                            if (r1 >= 0)
+                                dst[r1 * p.M + m] =
                                     __uint_as_float(xv[j + 1]) + (__uint_as_float(dv[j + 1]) - c1);
                         }
                     }
@@ -512,6 +565,77 @@ __global__ void __launch_bounds__(256) bsplit_kernel(const float *__restrict__ b
     }
 }
 
+// ---- MUL_MAT_ID_BACK as a grouped product ----------------------------------
+// Routing, one CTA: count the slots of each expert, lay them out sorted by
+// expert, build the (expert, n-tile) work list.  A slot with an id outside
+// [0, E) gets a zero dx row and OOP_ERR_BAD_ID in the status word.  The order
+// of slots inside an expert does not matter: every dx row is computed alone.
+struct RouteWs {
+    int *count, *offset, *ntiles, *tiles, *rows;
+};
+
+__global__ void __launch_bounds__(1024) mmid_route_kernel(const int32_t *__restrict__ ids,
+                                                          int64_t nslot, int E, int64_t Kw,
+                                                          float *dx, RouteWs w, int *status) {
+    extern __shared__ int sh[];                   // [E] counts, then [E] cursors
+    int *cnt = sh, *cur = sh + E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    for (int64_t s = threadIdx.x; s < nslot; s += blockDim.x) {
+        const int e = ids[s];
+        if (e >= 0 && e < E) {
+            atomicAdd(&cnt[e], 1);
+        } else {
+            record_status(status, OOP_ERR_BAD_ID);
+            for (int64_t k = 0; k < Kw; ++k) dx[s * Kw + k] = 0.f;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0, nt = 0;
+        for (int e = 0; e < E; ++e) {
+            w.count[e] = cnt[e];
+            w.offset[e] = acc;
+            cur[e] = acc;
+            for (int t = 0; t * BN < cnt[e]; ++t) w.tiles[nt++] = (e << 16) | t;
+            acc += cnt[e];
+        }
+        *w.ntiles = nt;
+    }
+    __syncthreads();
+    for (int64_t s = threadIdx.x; s < nslot; s += blockDim.x) {
+        const int e = ids[s];
+        if (e >= 0 && e < E) w.rows[atomicAdd(&cur[e], 1)] = static_cast<int>(s);
+    }
+}
+
+// Sorted slot j: g[rows[j]][0..R) -> ghi, glo [j][Kp], TF32 split, zero
+// padding for r in [R, Kp).  Rows past the routed total are left alone: the
+// tile kernel never stores the columns they feed.
+__global__ void __launch_bounds__(256) mmid_gsplit_kernel(const float *__restrict__ g,
+                                                          const int *__restrict__ rows,
+                                                          const int *__restrict__ count, int E,
+                                                          uint32_t *__restrict__ ghi,
+                                                          uint32_t *__restrict__ glo, int64_t R,
+                                                          int64_t Kp) {
+    const int64_t j = blockIdx.x;
+    __shared__ int total;
+    if (threadIdx.x == 0) {
+        int t = 0;
+        for (int e = 0; e < E; ++e) t += count[e];
+        total = t;
+    }
+    __syncthreads();
+    if (j >= total) return;
+    const float *src = g + static_cast<int64_t>(rows[j]) * R;
+    for (int64_t r = threadIdx.x; r < Kp; r += blockDim.x) {
+        uint32_t h = 0, l = 0;
+        if (r < R) ptx::split_tf32(__ldg(src + r), h, l);
+        ghi[j * Kp + r] = h;
+        glo[j * Kp + r] = l;
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -542,6 +666,20 @@ bool make_b_map(CUtensorMap *map, void *base, int64_t Kp, int64_t N, int64_t sli
            CUDA_SUCCESS;
 }
 
+// grouped src1: [rows][Kp] words, boxes of 32 k x 128 rows, 128-byte swizzle.
+bool make_b_map_2d(CUtensorMap *map, void *base, int64_t Kp, int64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(Kp), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(Kp * 4)};
+    cuuint32_t box[2] = {BK, BN};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // raw src0: rows of `a_row_bytes` (all slices stacked), boxes of 32 rows.
 template <int TYPE>
 bool make_a_map(CUtensorMap *map, const void *base, const OutProdShape &s) {
@@ -551,9 +689,11 @@ bool make_a_map(CUtensorMap *map, const void *base, const OutProdShape &s) {
     cuuint32_t box[2] = {static_cast<cuuint32_t>(RawA<TYPE>::BOX_X), BK};
     cuuint32_t estr[2] = {1, 1};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.a_row_bytes)};
-    if constexpr (TYPE == OOP_TYPE_F32) {
+    if constexpr (elementwise_type<TYPE>()) {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.M), static_cast<cuuint64_t>(rows)};
-        return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims,
+        const CUtensorMapDataType dt = TYPE == OOP_TYPE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        return fn(map, dt, 2, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -577,7 +717,7 @@ int g_inject = 0;
 #endif
 int g_chunk_kb = OOP_TC_CHUNK_KB;      // k-blocks (of 32) per D1 accumulation
 
-template <int TYPE>
+template <int TYPE, bool GROUPED>
 cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap &mhi,
                          const CUtensorMap &mlo, const TcParams &p, int64_t grid_x,
                          int64_t slices, cudaStream_t stream) {
@@ -600,7 +740,8 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
                stream>>>(mhi, mlo, ma, p);
         return cudaGetLastError();
     };
-    return tma_a ? run(tc_out_prod_kernel<TYPE, true>) : run(tc_out_prod_kernel<TYPE, false>);
+    return tma_a ? run(tc_out_prod_kernel<TYPE, true, GROUPED>)
+                 : run(tc_out_prod_kernel<TYPE, false, GROUPED>);
 }
 
 }  // namespace
@@ -657,14 +798,126 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
 
     switch (s.a_type) {
     case OOP_TYPE_F32:
-        return launch_typed<OOP_TYPE_F32>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
+        return launch_typed<OOP_TYPE_F32, false>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
     case OOP_TYPE_Q8_0:
-        return launch_typed<OOP_TYPE_Q8_0>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
+        return launch_typed<OOP_TYPE_Q8_0, false>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
     case OOP_TYPE_Q4_0:
-        return launch_typed<OOP_TYPE_Q4_0>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
+        return launch_typed<OOP_TYPE_Q4_0, false>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
     default:
         return cudaErrorInvalidValue;
     }
+}
+
+// ---- MUL_MAT_ID_BACK launcher ------------------------------------------------
+
+namespace {
+
+struct MmidPlan {
+    int64_t nslot, Kp, max_tiles, mtiles;
+    size_t off_count, off_offset, off_ntiles, off_tiles, off_rows, off_ghi, off_glo, total;
+};
+
+MmidPlan plan_mmid(const MmidShape &s) {
+    MmidPlan t = {};
+    t.nslot = s.n_used * s.n_tok;
+    t.Kp = padded_k(s.N);
+    t.max_tiles = (t.nslot + BN - 1) / BN + s.E;
+    t.mtiles = (s.K + BM - 1) / BM;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += align256(bytes);
+        return at;
+    };
+    t.off_count = take(sizeof(int) * static_cast<size_t>(s.E));
+    t.off_offset = take(sizeof(int) * static_cast<size_t>(s.E));
+    t.off_ntiles = take(sizeof(int));
+    t.off_tiles = take(sizeof(int) * static_cast<size_t>(t.max_tiles));
+    t.off_rows = take(sizeof(int) * static_cast<size_t>(t.nslot));
+    t.off_ghi = take(4 * static_cast<size_t>(t.nslot) * static_cast<size_t>(t.Kp));
+    t.off_glo = take(4 * static_cast<size_t>(t.nslot) * static_cast<size_t>(t.Kp));
+    t.total = o;
+    return t;
+}
+
+}  // namespace
+
+size_t tc_mmid_workspace_bytes(const MmidShape &s) { return plan_mmid(s).total; }
+
+cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, float *dx,
+                           const MmidShape &s, void *workspace, int *status,
+                           cudaStream_t stream) {
+    const MmidPlan t = plan_mmid(s);
+    if (s.E > 32767 || s.E < 1 || t.nslot > 0x7fffffffLL || t.max_tiles * t.mtiles > 0x7fffffffLL ||
+        s.K * s.N * s.E >= (1LL << 40))
+        return cudaErrorInvalidConfiguration;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    RouteWs rw;
+    rw.count = reinterpret_cast<int *>(ws + t.off_count);
+    rw.offset = reinterpret_cast<int *>(ws + t.off_offset);
+    rw.ntiles = reinterpret_cast<int *>(ws + t.off_ntiles);
+    rw.tiles = reinterpret_cast<int *>(ws + t.off_tiles);
+    rw.rows = reinterpret_cast<int *>(ws + t.off_rows);
+    uint32_t *ghi = reinterpret_cast<uint32_t *>(ws + t.off_ghi);
+    uint32_t *glo = reinterpret_cast<uint32_t *>(ws + t.off_glo);
+
+    const size_t route_smem = 2 * sizeof(int) * static_cast<size_t>(s.E);
+    if (route_smem > 48 * 1024) return cudaErrorInvalidConfiguration;
+    mmid_route_kernel<<<1, 1024, route_smem, stream>>>(ids, t.nslot, static_cast<int>(s.E), s.K,
+                                                        dx, rw, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    mmid_gsplit_kernel<<<static_cast<unsigned>(t.nslot), 256, 0, stream>>>(
+        g, rw.rows, rw.count, static_cast<int>(s.E), ghi, glo, s.N, t.Kp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    CUtensorMap mhi, mlo;
+    if (!make_b_map_2d(&mhi, ghi, t.Kp, t.nslot) || !make_b_map_2d(&mlo, glo, t.Kp, t.nslot))
+        return cudaErrorInvalidValue;
+
+    // W as src0: slice e has rows r (K = N of W) of K_w elements (M)
+    OutProdShape os = {};
+    os.M = s.K;
+    os.K = s.N;
+    os.N = t.nslot;
+    os.ne02 = s.E;
+    os.ne03 = 1;
+    os.ne12 = s.E;
+    os.ne13 = 1;
+    os.dps2 = 1;
+    os.dps3 = 1;
+    os.a_type = s.w_type;
+    os.a_row_bytes = s.K * (s.w_type == OOP_TYPE_F32 ? 4 : 2);
+
+    TcParams p = {};
+    p.a = static_cast<const uint8_t *>(W);
+    p.dst = dx;
+    p.status = status;
+    p.M = os.M;
+    p.K = os.K;
+    p.N = os.N;
+    p.ne02 = os.ne02;
+    p.ne12 = os.ne12;
+    p.dps2 = 1;
+    p.dps3 = 1;
+    p.a_row_bytes = os.a_row_bytes;
+    p.num_kb = static_cast<int>((os.K + BK - 1) / BK);
+    p.chunk_kb = g_chunk_kb;
+    p.mtiles = static_cast<int>(t.mtiles);
+    p.ntiles = 0;
+    p.inject = 0;
+    p.grp_count = rw.count;
+    p.grp_offset = rw.offset;
+    p.grp_rows = rw.rows;
+    p.grp_tiles = rw.tiles;
+    p.grp_ntiles = rw.ntiles;
+    const int64_t grid_x = t.mtiles * t.max_tiles;
+    if (s.w_type == OOP_TYPE_F32)
+        return launch_typed<OOP_TYPE_F32, true>(W, os, mhi, mlo, p, grid_x, 1, stream);
+    if (s.w_type == OOP_TYPE_BF16)
+        return launch_typed<OOP_TYPE_BF16, true>(W, os, mhi, mlo, p, grid_x, 1, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace oop

@@ -64,6 +64,12 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst,
                             const OutProdShape &s, void *workspace,
                             int *status, cudaStream_t stream);
 
+// MUL_MAT_ID_BACK as a grouped tensor-core product (slots sorted by expert).
+size_t tc_mmid_workspace_bytes(const MmidShape &s);
+cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, float *dx,
+                           const MmidShape &s, void *workspace, int *status,
+                           cudaStream_t stream);
+
 // MUL_MAT_ID_BACK, one CTA per routed slot.
 cudaError_t launch_mmid_per_slot(const void *W, const int32_t *ids,
                                  const float *g, float *dx, const MmidShape &s,

@@ -150,8 +150,11 @@ int oop_out_prod_noalloc(const void *a, int a_type, const float *b, float *dst,
  *   g:  f32 {N, n_used, n_tokens}
  *   dx: f32 {K, n_used, n_tokens}, OVERWRITTEN; one writer per element.
  *
+ * The default kernel sorts the slots by expert on the device and runs the
+ * tensor-core product per expert (same 3xTF32 scheme and bound as OUT_PROD);
+ * it needs oop_mul_mat_id_back_workspace_size(...) bytes of workspace.
  * An id outside [0, E) zeroes that slot's dx and records OOP_ERR_BAD_ID in the
- * device status word.  workspace as for oop_out_prod.
+ * device status word.  E <= 6144.
  */
 size_t oop_mul_mat_id_back_workspace_size(int w_type, const int64_t ne_w[3],
                                           const int64_t ne_ids[2]);
@@ -160,6 +163,14 @@ int oop_mul_mat_id_back(const void *W, int w_type, const int32_t *ids,
                         const float *g, float *dx, const int64_t ne_w[3],
                         const int64_t ne_ids[2], void *workspace,
                         size_t workspace_bytes, void *stream);
+
+/* oop_mul_mat_id_back with the kernel chosen by the caller: OOP_PATH_AUTO or
+ * OOP_PATH_TCGEN05 (grouped tensor-core product, needs the workspace) or
+ * OOP_PATH_SIMT (one CTA per routed slot, CUDA cores, no workspace). */
+int oop_mul_mat_id_back_ex(const void *W, int w_type, const int32_t *ids,
+                           const float *g, float *dx, const int64_t ne_w[3],
+                           const int64_t ne_ids[2], void *workspace,
+                           size_t workspace_bytes, void *stream, int path);
 
 /* Synchronises `stream`, then returns the current device's status word
  * (OOP_OK, or the first device-side error recorded since it was last
