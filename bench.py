@@ -43,7 +43,11 @@ WORKLOAD = (f"dense OUT_PROD q8_0 x f32 m{DENSE_M} k{DENSE_K} n{DENSE_N} "
             "(frozen quantised weight, gradient with 0.2% outliers to 1.5e5)")
 L2_FLUSH_BYTES = 512 << 20
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense ratio
-FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FMA/clk x 2 x max clock
+# DRAM bytes (read + write) of one launch of the tensor-core tile kernel on the
+# headline workload, from the ncu capture summarised in
+# profiles/tc_out_prod_q8_m5120_k5120_n1024.md; None until that capture
+# matches the kernel in this tree.
+TC_TRAFFIC_BYTES = None
 
 
 def _peaks():
@@ -169,6 +173,31 @@ def _barrier_max(torch, value, ws):
     return float(t.item())
 
 
+def _cublas_tf32(torch, device):
+    """cuBLAS TF32 GEMM throughput (context for the TF32 roofline)."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        n = 8192
+        x = torch.randn(n, n, device=device)
+        y = torch.randn(n, n, device=device)
+        for _ in range(3):
+            x @ y
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(5):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            x @ y
+            e.record()
+            torch.cuda.synchronize()
+            best = min(best, s.elapsed_time(e))
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def gpu_arm(args):
     import torch
 
@@ -185,7 +214,7 @@ def gpu_arm(args):
     op.lib()
     peaks, peak_kind = _peaks()
     timer = Timer(torch, device)
-    launches = 0
+    clocks = ClockSampler(device.index if device.index is not None else 0)
 
     # ---- headline: dense q8_0 OUT_PROD -------------------------------------
     a_np, b_np = synth.dense_quant(synth.TYPE_Q8_0, DENSE_M, DENSE_K, DENSE_N)
@@ -195,27 +224,44 @@ def gpu_arm(args):
     out = torch.empty((1, 1, DENSE_N, DENSE_M), dtype=torch.float32, device=device)
     nws = op.oop_out_prod_workspace_size(op.TYPE_Q8_0, ne_a, (DENSE_N, DENSE_K, 1, 1))
     ws_buf = torch.empty(max(nws, 1), dtype=torch.uint8, device=device)
-    dense_path = op.PATH_TCGEN05 if getattr(op, "HAS_TCGEN05", False) else op.PATH_SIMT
-    dense_launches = getattr(op, "TCGEN05_LAUNCHES_PER_CALL", 1) \
-        if dense_path == op.PATH_TCGEN05 else 1
-
-    def dense_step():
-        op.out_prod(a, b, a_type=op.TYPE_Q8_0, ne_a=ne_a, out=out, workspace=ws_buf,
-                    path=dense_path)
-
     flops = 2.0 * DENSE_M * DENSE_N * DENSE_K
-    clocks = ClockSampler(device.index if device.index is not None else 0)
+
+    def dense_call():
+        op.out_prod(a, b, a_type=op.TYPE_Q8_0, ne_a=ne_a, out=out, workspace=ws_buf,
+                    path=op.PATH_TCGEN05)
+
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    for _ in range(args.warmup):
+        timer.flush()
+        dense_call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = []
     t_region0 = time.perf_counter()
-    times = timer.run(dense_step, args.steps, args.warmup)
+    for _ in range(args.steps):
+        timer.flush()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        k0 = torch.cuda.Event(enable_timing=True)
+        k1 = torch.cuda.Event(enable_timing=True)
+        for e in (k0, k1):          # create the events before handing them over
+            e.record(stream)
+        op.profile_main_kernel(k0, k1)
+        s0.record(stream)
+        dense_call()
+        s1.record(stream)
+        evs.append((s0, s1, k0, k1))
+    torch.cuda.synchronize()
     region_s = time.perf_counter() - t_region0
-    clk = clocks.stop()
-    launches += args.steps * dense_launches
-    ms_step = statistics.mean(times)
+    step_ms = [s0.elapsed_time(s1) for s0, s1, _, _ in evs]
+    main_ms = [k0.elapsed_time(k1) for _, _, k0, k1 in evs]
+    launches = args.steps * op.TCGEN05_LAUNCHES_PER_CALL
+    ms_step = statistics.mean(step_ms)
+    ms_main = statistics.mean(main_ms)
     ms_step_max = _barrier_max(torch, ms_step, ws)
     value = ws * flops / (ms_step_max * 1e-3) / 1e12
 
@@ -223,17 +269,16 @@ def gpu_arm(args):
     a_host = torch.from_numpy(a_np).pin_memory()
     b_host = torch.from_numpy(b_np).pin_memory()
     for _ in range(max(1, args.warmup)):
-        op.out_prod_host(a_host, b_host, a_type=op.TYPE_Q8_0, device=device, path=dense_path)
+        op.out_prod_host(a_host, b_host, a_type=op.TYPE_Q8_0, device=device)
     torch.cuda.synchronize()
     e2e_t = []
     for _ in range(args.steps):
         timer.flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        op.out_prod_host(a_host, b_host, a_type=op.TYPE_Q8_0, device=device, path=dense_path)
+        op.out_prod_host(a_host, b_host, a_type=op.TYPE_Q8_0, device=device)
         e2e_t.append(time.perf_counter() - t0)
     e2e_s = _barrier_max(torch, statistics.mean(e2e_t), ws)
-    launches += 0   # e2e launches are outside the device-timed region
 
     # ---- the other rows of the path (same run) ----------------------------
     parts = {}
@@ -297,33 +342,36 @@ def gpu_arm(args):
         tW = torch.from_numpy(W.view(np.int16) if wt == synth.TYPE_BF16 else W).to(device)
         tids, tg = torch.from_numpy(ids).to(device), torch.from_numpy(g).to(device)
         o = torch.empty((512, 8, 2048), dtype=torch.float32, device=device)
-        t = timer.run(lambda: op.mul_mat_id_back(tW, tids, tg, w_type=wt, out=o), args.steps, 2)
-        us = statistics.mean(t) * 1e3
+        wsz = op.oop_mul_mat_id_back_workspace_size(wt, (2048, 768, 32), (8, 512))
+        wsb = torch.empty(max(wsz, 1), dtype=torch.uint8, device=device)
         fl = 2.0 * 2048 * 768 * 8 * 512
         byts = W.nbytes + g.nbytes + 4.0 * 2048 * 8 * 512 + ids.nbytes
-        parts[f"mul_mat_id_back_{nm}"] = {
-            "workload": f"E=32 W {nm} [2048, 768], 8 of 32 experts per token, 512 tokens",
-            "us": round(us, 3), "TFLOP/s": round(fl / (us * 1e-6) / 1e12, 3),
-            "GB/s": round(byts / (us * 1e-6) / 1e9, 1)}
-        del tW, tids, tg, o
+        entry = {"workload": f"E=32 W {nm} [2048, 768], 8 of 32 experts per token, 512 tokens"}
+        for path, pname in ((op.PATH_TCGEN05, "grouped_tcgen05"), (op.PATH_SIMT, "per_slot")):
+            t = timer.run(lambda: op.mul_mat_id_back(tW, tids, tg, w_type=wt, out=o, workspace=wsb,
+                                                     path=path), max(3, args.steps // 4), 2)
+            us = statistics.mean(t) * 1e3
+            entry[pname] = {"us": round(us, 3), "TFLOP/s": round(fl / (us * 1e-6) / 1e12, 3),
+                            "GB/s": round(byts / (us * 1e-6) / 1e9, 1)}
+        parts[f"mul_mat_id_back_{nm}"] = entry
+        del tW, tids, tg, o, wsb
 
+    clk = clocks.stop()
     assert op.device_status() == 0, "device status word set"
+    tf32_cublas = _cublas_tf32(torch, device)
 
-    # ---- roofline of the dominant kernel ----------------------------------
-    achieved = flops / (ms_step * 1e-3) / 1e12
-    if dense_path == op.PATH_TCGEN05:
-        peak = peaks["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "pipe_frac_3xtf32": round(3 * achieved / peak, 4),
-                "peak_note": f"TF32 = {peak_kind} bf16 burst x nominal 1.1/2.25",
-                "traffic": None, "kernel": "tcgen05 3xTF32 OUT_PROD"}
-    else:
-        peak = FP32_SIMT_PEAK_TFLOPS
-        roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "peak_note": "FP32 FMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz",
-                "traffic": None, "kernel": "CUDA-core tiled OUT_PROD"}
+    # ---- roofline of the dominant kernel (the tensor-core tile kernel) ----
+    achieved = flops / (ms_main * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
+    roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "pipe_frac_3xtf32": round(3 * achieved / peak, 4),
+            "peak_note": f"TF32 = {peak_kind} bf16 burst {peaks['bf16_tflops']} x nominal "
+                         f"1.1/2.25 (of {peak_kind}); cuBLAS TF32 8192^3 in this run: "
+                         f"{tf32_cublas:.0f} TFLOP/s",
+            "kernel": "tc_out_prod_kernel (tcgen05 3xTF32), algorithmic 2*M*N*K per launch",
+            "kernel_ms": round(ms_main, 4), "split_prepass_ms": round(ms_step - ms_main, 4),
+            "traffic": TC_TRAFFIC_BYTES}
 
     cpu = cpu_baseline(args.cpu_seconds) if rank == 0 and ws == 1 else None
     line = {
@@ -333,8 +381,7 @@ def gpu_arm(args):
         "data": "synthetic (seeded splitmix64 normals, q8_0-quantised weight, 0.2% outliers)",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{ws}",
                    "l2": "512 MB buffer written before every timed step",
-                   "precision": "3xTF32 split on tensor cores" if dense_path == op.PATH_TCGEN05
-                   else "fp32 FMA"},
+                   "precision": "3xTF32 split on tensor cores, fp32 accumulation with Kahan fold"},
         "e2e": {"value": round(ws * flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(a_np.nbytes + b_np.nbytes),
                 "d2h_bytes_per_step": int(4 * DENSE_M * DENSE_N)},

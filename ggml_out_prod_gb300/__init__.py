@@ -59,6 +59,7 @@ EXPORTS = (
     "oop_mul_mat_id_back", "oop_mul_mat_id_back_ex", "oop_mul_mat_id_back_workspace_size",
     "oop_device_status", "oop_status_string", "oop_version", "oop_debug_inject_timeout",
     "oop_last_cuda_error", "oop_out_prod_noalloc", "oop_out_prod_noalloc_scratch_bytes",
+    "oop_profile_main_kernel",
 )
 
 
@@ -117,6 +118,8 @@ def lib():
                                                _vp]
             L.oop_out_prod_noalloc_scratch_bytes.restype = ctypes.c_size_t
             L.oop_out_prod_noalloc_scratch_bytes.argtypes = []
+            L.oop_profile_main_kernel.restype = ctypes.c_int
+            L.oop_profile_main_kernel.argtypes = [_vp, _vp]
             L.oop_last_cuda_error.restype = ctypes.c_char_p
             L.oop_last_cuda_error.argtypes = []
             L.oop_debug_inject_timeout.restype = ctypes.c_int
@@ -278,6 +281,14 @@ def mul_mat_id_back(W, ids, g, w_type=None, out=None, workspace=None, stream=Non
     if rc != OK:
         raise OopError(rc, "oop_mul_mat_id_back")
     return out
+
+
+def profile_main_kernel(before, after) -> None:
+    """Have the next tensor-core launch record torch.cuda.Event `before` and
+    `after` around its main tile kernel (the events must exist already:
+    record each once first)."""
+    lib().oop_profile_main_kernel(ctypes.c_void_p(before.cuda_event),
+                                  ctypes.c_void_p(after.cuda_event))
 
 
 def device_status(stream=None, clear=True) -> int:

@@ -311,6 +311,11 @@ int oop_version(void) { return (0 << 16) | 1; }
 
 const char *oop_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda); }
 
+int oop_profile_main_kernel(void *before, void *after) {
+    tc_set_profile_events(static_cast<cudaEvent_t>(before), static_cast<cudaEvent_t>(after));
+    return OOP_OK;
+}
+
 int oop_debug_inject_timeout(int enable) {
     tc_set_inject(enable ? 1 : 0);
     return OOP_OK;

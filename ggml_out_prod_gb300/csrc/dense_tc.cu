@@ -712,6 +712,7 @@ int64_t padded_k(int64_t K) { return (K + 3) / 4 * 4; }
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int g_inject = 0;
+thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 #ifndef OOP_TC_CHUNK_KB
 #define OOP_TC_CHUNK_KB 2
 #endif
@@ -736,9 +737,15 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
+        cudaEvent_t before = g_ev_before, after = g_ev_after;
+        g_ev_before = g_ev_after = nullptr;
+        if (before && (e = cudaEventRecord(before, stream)) != cudaSuccess) return e;
         kern<<<dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(slices)), THREADS, smem,
                stream>>>(mhi, mlo, ma, p);
-        return cudaGetLastError();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (after && (e = cudaEventRecord(after, stream)) != cudaSuccess) return e;
+        return cudaSuccess;
     };
     return tma_a ? run(tc_out_prod_kernel<TYPE, true, GROUPED>)
                  : run(tc_out_prod_kernel<TYPE, false, GROUPED>);
@@ -747,6 +754,10 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
 }  // namespace
 
 void tc_set_inject(int v) { g_inject = v; }
+void tc_set_profile_events(cudaEvent_t before, cudaEvent_t after) {
+    g_ev_before = before;
+    g_ev_after = after;
+}
 
 size_t tc_workspace_bytes(const OutProdShape &s) {
     const size_t one = align256(static_cast<size_t>(s.ne12 * s.ne13) *

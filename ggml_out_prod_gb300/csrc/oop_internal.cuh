@@ -60,6 +60,7 @@ cudaError_t launch_dense_simt(const void *a, const float *b, float *dst,
 // Tensor-core OUT_PROD (tcgen05, 3xTF32).
 size_t tc_workspace_bytes(const OutProdShape &s);
 void tc_set_inject(int v);   // test hook: the next tensor-core launch drops one TMA stage
+void tc_set_profile_events(cudaEvent_t before, cudaEvent_t after);
 cudaError_t launch_dense_tc(const void *a, const float *b, float *dst,
                             const OutProdShape &s, void *workspace,
                             int *status, cudaStream_t stream);

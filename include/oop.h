@@ -188,6 +188,13 @@ const char *oop_last_cuda_error(void);
 /* Library version, (major << 16) | minor. */
 int oop_version(void);
 
+/* Measurement hook (no counterpart on the pages): the next tensor-core launch
+ * made by the calling thread (OUT_PROD or MUL_MAT_ID_BACK) records the
+ * cudaEvent_t `before` on its stream just before its main tile kernel and
+ * `after` just after it, so a caller can time that kernel alone, without the
+ * src1 split pre-pass.  The events are used once.  Returns OOP_OK. */
+int oop_profile_main_kernel(void *before, void *after);
+
 /* Test hook for the device-side failure path (no counterpart on the pages).
  * With enable != 0, the NEXT tensor-core OUT_PROD launch on this process
  * skips one of its TMA copies, so its MMA thread's bounded wait runs out
