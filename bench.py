@@ -45,9 +45,9 @@ L2_FLUSH_BYTES = 512 << 20
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # DRAM bytes (read + write) of one launch of the tensor-core tile kernel on the
 # headline workload, from the ncu capture summarised in
-# profiles/tc_out_prod_q8_m5120_k5120_n1024.md; None until that capture
-# matches the kernel in this tree.
-TC_TRAFFIC_BYTES = None
+# profiles/tc_out_prod_q8_m5120_k5120_n1024.md (to be set back to None as soon
+# as the kernel changes after that capture).
+TC_TRAFFIC_BYTES = 117_407_744
 
 
 def _peaks():
@@ -336,6 +336,50 @@ def gpu_arm(args):
             "us_per_slice_loop": round(statistics.mean(t2) * 1e3, 3),
             "launches_per_slice_loop": 16 * n_seq}
         del ta, tb, o, o2
+
+    # every dense shape, q8_0 and q4_0: whole call and tile kernel alone
+    for m, k in synth.DENSE_MK:
+        x = synth.normal(synth.tensor_seed(30), m * k, std=0.02).reshape(1, 1, k, m)
+        bn = synth.make_b((DENSE_N, k, 1, 1), 31, std=1e3, outliers=True)
+        tb = torch.from_numpy(bn).to(device)
+        o = torch.empty((1, 1, DENSE_N, m), dtype=torch.float32, device=device)
+        wsz = op.oop_out_prod_workspace_size(op.TYPE_Q8_0, (m, k, 1, 1), (DENSE_N, k, 1, 1))
+        wsb = torch.empty(max(wsz, 1), dtype=torch.uint8, device=device)
+        fl = 2.0 * m * DENSE_N * k
+        for tid, tname, quant in ((synth.TYPE_Q8_0, "q8_0", synth.quantize_q8_0),
+                                  (synth.TYPE_Q4_0, "q4_0", synth.quantize_q4_0)):
+            ta = torch.from_numpy(quant(x)).to(device)
+
+            def call():
+                op.out_prod(ta, tb, a_type=tid, ne_a=(m, k, 1, 1), out=o, workspace=wsb,
+                            path=op.PATH_TCGEN05)
+
+            for _ in range(3):
+                timer.flush()
+                call()
+            torch.cuda.synchronize()
+            rec = []
+            for _ in range(max(3, args.steps // 4)):
+                timer.flush()
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                ev[2].record(stream)
+                ev[3].record(stream)
+                op.profile_main_kernel(ev[2], ev[3])
+                ev[0].record(stream)
+                call()
+                ev[1].record(stream)
+                rec.append(ev)
+            torch.cuda.synchronize()
+            us_call = statistics.mean(e[0].elapsed_time(e[1]) for e in rec) * 1e3
+            us_kern = statistics.mean(e[2].elapsed_time(e[3]) for e in rec) * 1e3
+            peak_tf32 = peaks["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
+            parts[f"dense_{tname}_m{m}_k{k}_n{DENSE_N}"] = {
+                "us_call": round(us_call, 2), "us_tile_kernel": round(us_kern, 2),
+                "TFLOP/s_call": round(fl / (us_call * 1e-6) / 1e12, 2),
+                "TFLOP/s_tile_kernel": round(fl / (us_kern * 1e-6) / 1e12, 2),
+                "pipe_frac_3xtf32": round(3 * fl / (us_kern * 1e-6) / 1e12 / peak_tf32, 4)}
+            del ta
+        del tb, o, wsb, x
 
     for wt, nm in ((synth.TYPE_F32, "f32"), (synth.TYPE_BF16, "bf16")):
         W, ids, g = synth.moe_back(wt)
