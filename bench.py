@@ -45,9 +45,9 @@ L2_FLUSH_BYTES = 512 << 20
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # DRAM bytes (read + write) of one launch of the tensor-core tile kernel on the
 # headline workload, from the ncu capture summarised in
-# profiles/tc_out_prod_q8_m5120_k5120_n1024.md (to be set back to None as soon
-# as the kernel changes after that capture).
-TC_TRAFFIC_BYTES = 117_407_744
+# profiles/tc_out_prod_q8_m5120_k5120_n1024.md; None while that capture does
+# not match the kernel in this tree.
+TC_TRAFFIC_BYTES = None
 
 
 def _peaks():
@@ -241,6 +241,7 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     evs = []
+    launches = 0
     t_region0 = time.perf_counter()
     for _ in range(args.steps):
         timer.flush()
@@ -253,13 +254,13 @@ def gpu_arm(args):
         op.profile_main_kernel(k0, k1)
         s0.record(stream)
         dense_call()
+        launches += op.last_launch_count()
         s1.record(stream)
         evs.append((s0, s1, k0, k1))
     torch.cuda.synchronize()
     region_s = time.perf_counter() - t_region0
     step_ms = [s0.elapsed_time(s1) for s0, s1, _, _ in evs]
     main_ms = [k0.elapsed_time(k1) for _, _, k0, k1 in evs]
-    launches = args.steps * op.TCGEN05_LAUNCHES_PER_CALL
     ms_step = statistics.mean(step_ms)
     ms_main = statistics.mean(main_ms)
     ms_step_max = _barrier_max(torch, ms_step, ws)

@@ -29,7 +29,11 @@ PATH_TCGEN05 = 2
 PATH_SIMT = 3
 
 HAS_TCGEN05 = True
-TCGEN05_LAUNCHES_PER_CALL = 2     # TF32 split of src1, then the tile kernel
+
+# schedules of the tensor-core tile kernel (set_tc_schedule, a test hook)
+SCHEDULE_AUTO = 0
+SCHEDULE_DATA_PARALLEL = 1
+SCHEDULE_STREAM_K = 2
 
 OK = 0
 ERR_NULL = -1
@@ -59,7 +63,8 @@ EXPORTS = (
     "oop_mul_mat_id_back", "oop_mul_mat_id_back_ex", "oop_mul_mat_id_back_workspace_size",
     "oop_device_status", "oop_status_string", "oop_version", "oop_debug_inject_timeout",
     "oop_last_cuda_error", "oop_out_prod_noalloc", "oop_out_prod_noalloc_scratch_bytes",
-    "oop_profile_main_kernel",
+    "oop_profile_main_kernel", "oop_out_prod_workspace_min_size", "oop_debug_set_tc_schedule",
+    "oop_last_launch_count",
 )
 
 
@@ -124,6 +129,12 @@ def lib():
             L.oop_last_cuda_error.argtypes = []
             L.oop_debug_inject_timeout.restype = ctypes.c_int
             L.oop_debug_inject_timeout.argtypes = [ctypes.c_int]
+            L.oop_out_prod_workspace_min_size.restype = ctypes.c_size_t
+            L.oop_out_prod_workspace_min_size.argtypes = [ctypes.c_int, _i64p, _i64p]
+            L.oop_debug_set_tc_schedule.restype = ctypes.c_int
+            L.oop_debug_set_tc_schedule.argtypes = [ctypes.c_int]
+            L.oop_last_launch_count.restype = ctypes.c_int
+            L.oop_last_launch_count.argtypes = []
             _lib = L
     return _lib
 
@@ -143,6 +154,18 @@ def _ne(v):
 
 def oop_out_prod_workspace_size(a_type, ne_a, ne_b) -> int:
     return int(lib().oop_out_prod_workspace_size(int(a_type), _ne(ne_a), _ne(ne_b)))
+
+
+def oop_out_prod_workspace_min_size(a_type, ne_a, ne_b) -> int:
+    return int(lib().oop_out_prod_workspace_min_size(int(a_type), _ne(ne_a), _ne(ne_b)))
+
+
+def oop_debug_set_tc_schedule(mode) -> int:
+    return int(lib().oop_debug_set_tc_schedule(int(mode)))
+
+
+def oop_last_launch_count() -> int:
+    return int(lib().oop_last_launch_count())
 
 
 def oop_out_prod(a, a_type, b, dst, ne_a, ne_b, ne_dst, workspace, workspace_bytes, stream,
@@ -293,6 +316,19 @@ def profile_main_kernel(before, after) -> None:
 
 def device_status(stream=None, clear=True) -> int:
     return oop_device_status(_stream_ptr(stream), clear)
+
+
+def set_tc_schedule(mode) -> None:
+    """Pick the tensor-core tile kernel's schedule for the calls that follow
+    (SCHEDULE_AUTO, SCHEDULE_DATA_PARALLEL or SCHEDULE_STREAM_K)."""
+    rc = oop_debug_set_tc_schedule(mode)
+    if rc != OK:
+        raise OopError(rc, "oop_debug_set_tc_schedule")
+
+
+def last_launch_count() -> int:
+    """Kernels the last OUT_PROD / MUL_MAT_ID_BACK call on this thread enqueued."""
+    return oop_last_launch_count()
 
 
 def out_prod_host(a_host, b_host, a_type=None, device="cuda", path=PATH_AUTO):

@@ -10,6 +10,9 @@
 #include "oop_internal.cuh"
 
 namespace oop {
+
+thread_local int g_kernel_launches = 0;
+
 namespace {
 
 // One status word per device, written by kernels through a pointer.
@@ -104,8 +107,10 @@ int choose_path(const OutProdShape &s, int path) {
     return path;
 }
 
-size_t workspace_for(const OutProdShape &s, int path) {
-    if (path == OOP_PATH_TCGEN05) return tc_workspace_bytes(s);
+// The least workspace a path runs with (the tensor-core path runs its
+// data-parallel schedule on this much; stream-K needs tc_workspace_bytes).
+size_t workspace_min(const OutProdShape &s, int path) {
+    if (path == OOP_PATH_TCGEN05) return tc_workspace_min_bytes(s);
     return 0;
 }
 
@@ -128,13 +133,19 @@ size_t oop_out_prod_workspace_size(int a_type, const int64_t ne_a[4], const int6
     OutProdShape s = {};
     if (check_out_prod_shape(a_type, ne_a, ne_b, &s) != OOP_OK) return 0;
     // cover every path a caller may pick with oop_out_prod_ex
-    size_t w = workspace_for(s, OOP_PATH_TCGEN05);
-    return w;
+    return tc_workspace_bytes(s);
+}
+
+size_t oop_out_prod_workspace_min_size(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
+    OutProdShape s = {};
+    if (check_out_prod_shape(a_type, ne_a, ne_b, &s) != OOP_OK) return 0;
+    return workspace_min(s, OOP_PATH_TCGEN05);
 }
 
 int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst, const int64_t ne_a[4],
                     const int64_t ne_b[4], const int64_t ne_dst[4], void *workspace,
                     size_t workspace_bytes, void *stream, int path) {
+    g_kernel_launches = 0;
     OutProdShape s = {};
     int rc = check_out_prod_shape(a_type, ne_a, ne_b, &s);
     if (rc != OOP_OK) return rc;
@@ -159,7 +170,7 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst, const
 
     const int chosen = choose_path(s, path);
     if (chosen == OOP_PATH_SKINNY && !skinny_ok(s)) return OOP_ERR_PATH;
-    const size_t need = workspace_for(s, chosen);
+    const size_t need = workspace_min(s, chosen);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
         return OOP_ERR_WORKSPACE;
 
@@ -174,13 +185,15 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst, const
     switch (chosen) {
     case OOP_PATH_SKINNY:
         e = launch_skinny(static_cast<const float *>(a), b, dst, s, st);
+        if (e == cudaSuccess) g_kernel_launches = 1;
         break;
     case OOP_PATH_TCGEN05:
-        e = launch_dense_tc(a, b, dst, s, workspace, status, st);
+        e = launch_dense_tc(a, b, dst, s, workspace, workspace_bytes, status, st);
         if (e == cudaErrorNotSupported) return OOP_ERR_PATH;
         break;
     case OOP_PATH_SIMT:
         e = launch_dense_simt(a, b, dst, s, st);
+        if (e == cudaSuccess) g_kernel_launches = 1;
         break;
     default:
         return OOP_ERR_PATH;
@@ -234,6 +247,7 @@ size_t oop_mul_mat_id_back_workspace_size(int w_type, const int64_t ne_w[3],
 int oop_mul_mat_id_back_ex(const void *W, int w_type, const int32_t *ids, const float *g,
                            float *dx, const int64_t ne_w[3], const int64_t ne_ids[2],
                            void *workspace, size_t workspace_bytes, void *stream, int path) {
+    oop::g_kernel_launches = 0;
     oop::MmidShape s = {};
     int rc = oop::check_mmid_shape(w_type, ne_w, ne_ids, &s);
     if (rc != OOP_OK) return rc;
@@ -263,6 +277,7 @@ int oop_mul_mat_id_back_ex(const void *W, int w_type, const int32_t *ids, const 
     if (s.N > 48 * 1024) return OOP_ERR_SHAPE;   // g's slot column is staged on chip
     cudaError_t e = oop::launch_mmid_per_slot(W, ids, g, dx, s, status, st);
     if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) oop::g_kernel_launches = 1;
     return cuda_rc(e);
 }
 
@@ -320,5 +335,13 @@ int oop_debug_inject_timeout(int enable) {
     tc_set_inject(enable ? 1 : 0);
     return OOP_OK;
 }
+
+int oop_debug_set_tc_schedule(int mode) {
+    if (mode < 0 || mode > 2) return OOP_ERR_PATH;
+    tc_set_schedule(mode);
+    return OOP_OK;
+}
+
+int oop_last_launch_count(void) { return g_kernel_launches; }
 
 }  // extern "C"

@@ -1,52 +1,69 @@
 // dense_tc.cu -- tensor-core OUT_PROD for sm_103a (tcgen05, 3xTF32).
 //
-// Per dst slice: D[n][m] = sum_k A[k][m] * B[k][n], A = src0 (f32, or q8_0 /
-// q4_0 dequantised in registers), B = the f32 gradient src1.  The gradient can
-// reach ~1.5e5, so no operand is ever rounded to a 16-bit format ("metal:
-// OUT_PROD multiplies in float staging; a training gradient overflowed half");
-// instead each operand is split into two TF32 terms that keep fp32's 8-bit
-// exponent: x = hi + lo (+ r, |r| <= 2^-22 |x|), and the product is
-// a_hi*b_hi + a_hi*b_lo + a_lo*b_hi (the a_lo*b_lo term is ~2^-22 relative).
+// Per dst slice: D[n][m] = sum_k A[k][m] * B[k][n], A = src0 (f32, bf16, or
+// q8_0 / q4_0 dequantised in registers), B = the f32 gradient src1.  The
+// gradient can reach ~1.5e5, so no operand is ever rounded to a 16-bit format
+// ("metal: OUT_PROD multiplies in float staging; a training gradient
+// overflowed half"); instead each operand is split into two TF32 terms that
+// keep fp32's 8-bit exponent: x = hi + lo (+ r, |r| <= 2^-22 |x|), and the
+// product is a_hi*b_hi + a_hi*b_lo + a_lo*b_hi (a_lo*b_lo is ~2^-22 relative;
+// for bf16 src0 a_lo is zero and its product is skipped).
 //
 // Launches per call:
 //  1. bsplit: b[slice][k][n] -> bhi, blo [slice][n][Kp] (K-major TF32 words,
 //     Kp = K rounded up to 4) in the caller's workspace;
-//  2. the tile kernel, one 128 (m) x 128 (n) dst tile per CTA, every head x
-//     batch slice in the same grid (grid.y = slice, src0 slice i2/dps2,
-//     i3/dps3 -- the broadcast map of "metal: OUT_PROD runs batched,
-//     broadcast and narrow shapes on the GPU").
+//  2. the tile kernel over 128 (m) x 96 (n) dst tiles of every head x batch
+//     slice in one grid (src0 slice i2/dps2, i3/dps3 -- the broadcast map of
+//     "metal: OUT_PROD runs batched, broadcast and narrow shapes on the GPU");
+//  3. (stream-K schedule only) the fix-up that adds the k-partials of tiles
+//     shared by two or more CTAs.
 //
-// Tile kernel roles (448 threads):
-//  warp 0      TMA: raw src0 rows (32 k x one m-tile of f32 words or q8_0 /
-//              q4_0 blocks) into a ring, bhi/blo tiles (32 k x 128 n,
-//              128-byte swizzle) into the operand stages
-//  warp 1      TMEM allocation; one thread issues tcgen05.mma (M128 N128 K8)
-//  warps 2-5   src0 producer: raw ring -> dequantise -> split -> the K-major
-//              swizzled A images a_hi / a_lo of the operand stage
-//  warps 6-13  fold + epilogue: TMEM -> registers -> dst
+// Work is a list of (tile, k-block) iterations, tile-major.  Data-parallel
+// schedule: CTA c takes the num_kb iterations of tile c.  Stream-K schedule:
+// one CTA per SM, CTA c takes iterations [I*c/G, I*(c+1)/G) of the I in the
+// problem, so the last wave is not left a tenth full; a tile split between
+// CTAs is written as fp32 partials (at most two per CTA: its first and last
+// tile) and summed in k order by the fix-up.  Both are deterministic.
+//
+// Tile kernel roles (576 threads = 18 warps at 96 registers, which is what
+// one SM sub-partition's register file holds for the five warps it gets):
+//  warp 0      TMA: raw src0 rows (32 k x one m-tile of f32 / bf16 words or
+//              q8_0 / q4_0 blocks) into a ring, bhi/blo tiles (32 k x 96 n,
+//              128-byte swizzle) into the B stages
+//  warp 1      TMEM allocation; the MMA loop (M128 N96 K8, A from tensor
+//              memory, B from shared memory), one elected lane issuing
+//  warps 2-9   src0 producer, thread = row of the m-tile = TMEM lane, two
+//              warps per lane quarter each taking 16 of the block's 32 k:
+//              raw ring -> dequantise -> split -> a_hi / a_lo columns of an
+//              A stage in tensor memory (tcgen05.st)
+//  warps 10-17 fold + epilogue: TMEM -> registers -> dst
 // When src0's rows are not 16-byte aligned (TMA's rule), the producer loads
 // src0 from global memory itself instead of from the ring.
 //
 // Accumulation.  The tensor core adds each MMA's products into its fp32
 // accumulator with an error of up to about one ulp of the accumulator (it
 // does not round to nearest), so a long sum dominated by one 1e5-sized
-// gradient entry drifts past the 2e-6 * sum|a*b| bound.  Three measures keep
-// the error at a few ulps of the result:
+// gradient entry drifts past the 2e-6 * sum|a*b| bound.  So:
 //  * the two small cross terms a_lo*b_hi + a_hi*b_lo go to their own
 //    accumulator D2, whose magnitude is ~2^-11 of the result, so its
-//    accumulation error is negligible; it runs over the whole K;
-//  * the big term a_hi*b_hi goes to D1, restarted every `chunk_kb` k-blocks
-//    (so at most 4*chunk_kb MMAs accumulate into it);
+//    accumulation error is negligible; it runs over a CTA's whole segment
+//    of a tile (all of K in the data-parallel schedule);
+//  * the big term a_hi*b_hi goes to D1, restarted every CHUNK_KB k-blocks
+//    (so at most 8 MMAs accumulate into it);
 //  * the fold warps add each finished D1 chunk into a Kahan pair: the sum S
-//    lives in TMEM, the compensation C in registers (64 columns per thread).
-// TMEM columns: [0,128) D1 buffer 0, [128,256) D1 buffer 1, [256,384) D2,
-// [384,512) S; the MMA fills one D1 buffer while the fold drains the other.
+//    lives in TMEM, the compensation C in registers (48 columns per thread,
+//    kept as bfloat16 pairs).
+// TMEM columns: [0,96) D1 buffer 0, [96,192) D1 buffer 1, [192,288) D2,
+// [288,384) S, [384,448) and [448,512) the two A stages (a_hi in the first
+// 32 columns, a_lo in the next 32).  The MMA fills one D1 buffer while the
+// fold drains the other.
 //
 // Every wait is bounded (1 s of globaltimer); running out records
 // OOP_ERR_DEVICE_TIMEOUT, sets a CTA-wide abort flag, drains the copies and
 // MMAs already issued, frees TMEM and returns.  Nothing traps.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "oop_internal.cuh"
@@ -56,16 +73,26 @@ namespace oop {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 96;
 constexpr int BK = 32;                      // tf32 per 128-byte swizzle row
-constexpr int STAGES = 3;
-constexpr int THREADS = 448;
+constexpr int CHUNK_KB = 2;                 // k-blocks per D1 chunk
+constexpr int B_STAGES = 6;                 // bhi + blo stages in shared memory
+constexpr int A_STAGES = 2;                 // a_hi + a_lo stages in tensor memory
+constexpr int THREADS = 576;                // 18 warps, 96 registers each
+constexpr int MAX_REGS = 96;                // 5 warps x 32 lanes x 96 fill one SMSP
+constexpr int PRODUCER_THREADS = 256;
+constexpr int KH = BK / 2;                  // k per producer thread and block
 constexpr int FOLD_THREADS = 256;
-constexpr int A_IMG = BM * BK * 4;          // 16 KB
-constexpr int B_IMG = BN * BK * 4;          // 16 KB
-constexpr int STAGE_BYTES = 2 * A_IMG + 2 * B_IMG;
+constexpr int FOLD_COLS = BN / 2;           // columns per fold thread
+constexpr int B_IMG = BN * BK * 4;          // 12 KB
+constexpr int STAGE_BYTES = 2 * B_IMG;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_D2 = 2 * BN, COL_S = 3 * BN;
+constexpr uint32_t COL_D2 = 2 * BN;
+constexpr uint32_t COL_S = 3 * BN;
+constexpr uint32_t COL_A = 384;
+constexpr uint32_t A_COLS = 2 * BK;         // a_hi then a_lo, one column per k
+static_assert(4 * BN <= COL_A && COL_A + A_STAGES * A_COLS == TMEM_COLS, "tensor memory map");
+static_assert(BN % 16 == 0 && FOLD_COLS % 16 == 0, "MMA N and fold pieces");
 constexpr uint64_t WAIT_NS = 1000000000ull;
 constexpr int MAX_RSTAGES = 4;
 
@@ -80,7 +107,7 @@ struct RawA<OOP_TYPE_F32> {
     static constexpr int BOX_X = BM;                 // f32 elements
     static constexpr int ROW_BYTES = BM * 4;         // bytes per staged k row
     static constexpr int SLOT = ROW_BYTES * BK;      // 16 KB
-    static constexpr int RSTAGES = 2;
+    static constexpr int RSTAGES = 3;
 };
 template <>
 struct RawA<OOP_TYPE_BF16> {
@@ -108,13 +135,16 @@ struct RawA<OOP_TYPE_Q4_0> {
 };
 
 struct Bars {
-    uint64_t bfull[STAGES];       // TMA bytes of operand stage s landed
-    uint64_t afull[STAGES];       // the 128 src0-producer threads wrote stage s
-    uint64_t empty[STAGES];       // MMAs reading stage s completed
-    uint64_t rfull[MAX_RSTAGES];  // raw src0 slot r landed
-    uint64_t rempty[MAX_RSTAGES]; // raw src0 slot r consumed by the producer
+    // Iteration g (one k-block of one tile) uses ring slot g % RSTAGES, B
+    // stage g % B_STAGES and A stage g % A_STAGES.
+    uint64_t rfull[MAX_RSTAGES];  // every TMA copy of the iteration landed (raw src0, B)
+    uint64_t rempty[MAX_RSTAGES]; // the producers are done with ring slot r
+    uint64_t afull[A_STAGES];     // the producers wrote A stage s (and saw its B land)
+    uint64_t bempty[B_STAGES];    // the iteration's MMAs completed: its B stage and
+                                  // its A stage are free
     uint64_t accf[2];             // D1 buffer b holds a finished chunk
     uint64_t acce[2];             // D1 buffer b was drained by the fold
+    uint64_t d2free;              // the fold read D2 at the end of a segment
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
@@ -125,7 +155,7 @@ constexpr bool elementwise_type() { return TYPE == OOP_TYPE_F32 || TYPE == OOP_T
 
 template <int TYPE>
 constexpr size_t smem_bytes() {
-    return STAGES * STAGE_BYTES + RawA<TYPE>::RSTAGES * RawA<TYPE>::SLOT + sizeof(Bars) + 1024;
+    return B_STAGES * STAGE_BYTES + RawA<TYPE>::RSTAGES * RawA<TYPE>::SLOT + sizeof(Bars) + 1024;
 }
 
 struct TcParams {
@@ -133,7 +163,13 @@ struct TcParams {
     float *dst;
     int *status;
     int64_t M, K, N, ne02, ne12, dps2, dps3, a_row_bytes;
-    int num_kb, chunk_kb, mtiles, ntiles, inject;
+    int num_kb, mtiles, ntiles, inject;
+    // stream-K: `ctas` CTAs share `iters` = tiles * num_kb iterations and
+    // write the k-partials of shared tiles to `partial` ([ctas][2][BN][BM]);
+    // ctas == 0 selects the data-parallel schedule
+    int64_t iters;
+    int ctas;
+    float *partial;
     // grouped mode (MUL_MAT_ID_BACK): slices are experts, src1 rows are the
     // routed slots sorted by expert, dst rows are scattered back to slots
     const int *grp_count;         // [E] slots routed to each expert
@@ -141,6 +177,63 @@ struct TcParams {
     const int *grp_rows;          // [slots] sorted slot -> dst row
     const int *grp_tiles;         // work list: (expert << 16) | n-tile
     const int *grp_ntiles;        // valid entries in grp_tiles
+};
+
+// First iteration of stream-K CTA c, and the CTA that owns iteration x.
+__host__ __device__ __forceinline__ int64_t sk_begin(int64_t iters, int ctas, int64_t c) {
+    return iters * c / ctas;
+}
+__host__ __device__ __forceinline__ int64_t sk_owner(int64_t iters, int ctas, int64_t x) {
+    return ((x + 1) * ctas - 1) / iters;
+}
+
+// Where tile t sits: m-tile, n-tile, dst slice, its valid src1 rows, and the
+// first src0 row (k = 0) of the src0 slice it reads.
+struct Tile {
+    int mt, nt;
+    int64_t slice, ncols, brow0, a_row0;
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
+    Tile d;
+    d.mt = static_cast<int>(t % p.mtiles);
+    const int64_t rest = t / p.mtiles;
+    if constexpr (GROUPED) {
+        const int packed = p.grp_tiles[rest];
+        d.slice = packed >> 16;
+        d.nt = packed & 0xFFFF;
+        d.ncols = p.grp_count[d.slice];
+        d.brow0 = p.grp_offset[d.slice] + static_cast<int64_t>(d.nt) * BN;
+    } else {
+        d.nt = static_cast<int>(rest % p.ntiles);
+        d.slice = rest / p.ntiles;
+        d.ncols = p.N;
+        d.brow0 = 0;
+    }
+    const int64_t i2 = d.slice % p.ne12, i3 = d.slice / p.ne12;
+    d.a_row0 = (i3 / p.dps3 * p.ne02 + i2 / p.dps2) * p.K;
+    return d;
+}
+
+// Walks a CTA's iterations in order; every role keeps its own copy.
+template <bool GROUPED>
+struct Walk {
+    int64_t it, end, tile;
+    int kb;
+    Tile t;
+    __device__ __forceinline__ Walk(const TcParams &p, int64_t it0, int64_t it1)
+        : it(it0), end(it1), tile(it0 / p.num_kb), kb(static_cast<int>(it0 % p.num_kb)) {
+        if (it < end) t = decode_tile<GROUPED>(p, tile);
+    }
+    __device__ __forceinline__ void next(const TcParams &p) {
+        ++it;
+        if (++kb == p.num_kb) {
+            kb = 0;
+            ++tile;
+            if (it < end) t = decode_tile<GROUPED>(p, tile);
+        }
+    }
 };
 
 template <int TYPE>
@@ -164,89 +257,94 @@ __device__ __forceinline__ float load_a(const uint8_t *row, int64_t m) {
     }
 }
 
-// Element r (row of the m-tile) of a staged raw k row.  `off0` is where the
-// tile's first block starts inside the staged row.
+// The 16 src0 values (k rows 16*kh .. 16*kh+15 of a staged k-block) of row
+// r of the m-tile.  Lane l of the warp owns row r = 32 * (warp % 4) + l, so a
+// warp covers one quantisation block: its 16 scales are read once (lane j
+// reads k row j) and passed around with shuffles.
 template <int TYPE>
-__device__ __forceinline__ float staged_a(const uint8_t *srow, int r, int off0) {
+__device__ __forceinline__ void staged_half(const uint8_t *slot, int r, int off0, int lane,
+                                            int kh, float (&x)[KH]) {
+    using Raw = RawA<TYPE>;
+    const uint8_t *rows = slot + kh * KH * Raw::ROW_BYTES;
     if constexpr (TYPE == OOP_TYPE_F32) {
-        return reinterpret_cast<const float *>(srow)[r];
+#pragma unroll
+        for (int j = 0; j < KH; ++j)
+            x[j] = reinterpret_cast<const float *>(rows + j * Raw::ROW_BYTES)[r];
     } else if constexpr (TYPE == OOP_TYPE_BF16) {
-        return bf16_bits_to_float(reinterpret_cast<const uint16_t *>(srow)[r]);
-    } else if constexpr (TYPE == OOP_TYPE_Q8_0) {
-        const uint8_t *blk = srow + off0 + (r >> 5) * kQ8Bytes;
-        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
-        const int q = static_cast<int8_t>(blk[2 + (r & 31)]);
-        return ptx::scaled_small_int(d, q);
+#pragma unroll
+        for (int j = 0; j < KH; ++j)
+            x[j] = bf16_bits_to_float(reinterpret_cast<const uint16_t *>(rows + j * Raw::ROW_BYTES)[r]);
     } else {
-        const uint8_t *blk = srow + off0 + (r >> 5) * kQ4Bytes;
-        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
-        const int j = r & 31;
-        const uint8_t byte = blk[2 + (j & 15)];
-        const int v = j < 16 ? (byte & 0x0f) : (byte >> 4);
-        return ptx::scaled_small_int(d, v - 8);
+        const uint8_t *blk = rows + off0 + (r >> 5) * Raw::BLOCK;
+        const float dl = half_bits_to_float(
+            *reinterpret_cast<const uint16_t *>(blk + (lane & (KH - 1)) * Raw::ROW_BYTES));
+#pragma unroll
+        for (int j = 0; j < KH; ++j) {
+            const float d = __shfl_sync(0xffffffffu, dl, j);
+            int v;
+            if constexpr (TYPE == OOP_TYPE_Q8_0) {
+                v = static_cast<int8_t>(blk[j * Raw::ROW_BYTES + 2 + lane]);
+            } else {
+                const uint8_t byte = blk[j * Raw::ROW_BYTES + 2 + (lane & 15)];
+                v = (lane < 16 ? (byte & 0x0f) : (byte >> 4)) - 8;
+            }
+            x[j] = ptx::scaled_small_int(d, v);
+        }
     }
 }
 
+// A bounded wait whose outcome the whole warp shares, so that the lanes stay
+// converged for the warp-collective tcgen05.ld/st and shuffles after it.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          bool *timed_out) {
+    const bool ok = ptx::mbar_wait_bounded(bar, parity, abort, true, WAIT_NS, timed_out);
+    return __all_sync(0xffffffffu, ok);
+}
+
 template <int TYPE, bool TMA_A, bool GROUPED>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __maxnreg__(MAX_REGS)
     tc_out_prod_kernel(const __grid_constant__ CUtensorMap map_bhi,
                        const __grid_constant__ CUtensorMap map_blo,
                        const __grid_constant__ CUtensorMap map_a, const TcParams p) {
     using Raw = RawA<TYPE>;
+    constexpr bool HAS_ALO = TYPE != OOP_TYPE_BF16;   // bf16 values are TF32 values
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *ring = smem + STAGES * STAGE_BYTES;
+    uint8_t *ring = smem + B_STAGES * STAGE_BYTES;
     Bars *bars = reinterpret_cast<Bars *>(ring + Raw::RSTAGES * Raw::SLOT);
     volatile int *abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int mt = blockIdx.x % p.mtiles;
-    int nt;
-    int64_t slice;
-    int64_t ncols = p.N;          // valid columns of this tile's slice
-    int64_t brow0 = 0;            // grouped: first src1 row of this tile
-    if constexpr (GROUPED) {
-        const int t = blockIdx.x / p.mtiles;
-        if (t >= *p.grp_ntiles) return;              // whole CTA: no work left
-        const int packed = p.grp_tiles[t];
-        slice = packed >> 16;
-        nt = packed & 0xFFFF;
-        ncols = p.grp_count[slice];
-        brow0 = p.grp_offset[slice] + static_cast<int64_t>(nt) * BN;
+
+    // this CTA's iterations [it0, it1)
+    int64_t it0, it1;
+    if (p.ctas > 0) {
+        it0 = sk_begin(p.iters, p.ctas, blockIdx.x);
+        it1 = sk_begin(p.iters, p.ctas, blockIdx.x + 1);
     } else {
-        nt = blockIdx.x / p.mtiles;
-        slice = blockIdx.y;
+        const int64_t t = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+        if constexpr (GROUPED) {
+            if (t / p.mtiles >= *p.grp_ntiles) return;   // whole CTA: no work left
+        }
+        it0 = t * p.num_kb;
+        it1 = it0 + p.num_kb;
     }
-    const int64_t i2 = slice % p.ne12, i3 = slice / p.ne12;
-    const int64_t j2 = i2 / p.dps2, j3 = i3 / p.dps3;
-    const int64_t a_row0 = (j3 * p.ne02 + j2) * p.K;     // first src0 row of the slice
-    const int nchunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
-    // where this m-tile starts inside a raw row
-    int box_x = 0, off0 = 0;
-    if constexpr (elementwise_type<TYPE>()) {
-        box_x = mt * BM;
-    } else {
-        const int byte0 = mt * 4 * Raw::BLOCK;
-        box_x = byte0 & ~15;
-        off0 = byte0 - box_x;
-    }
+    if (it0 >= it1) return;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&bars->bfull[s], 1);
-            ptx::mbar_init(&bars->afull[s], 128);
-            ptx::mbar_init(&bars->empty[s], 1);
-        }
+        for (int s = 0; s < B_STAGES; ++s) ptx::mbar_init(&bars->bempty[s], 1);
+        for (int s = 0; s < A_STAGES; ++s) ptx::mbar_init(&bars->afull[s], PRODUCER_THREADS);
         for (int r = 0; r < Raw::RSTAGES; ++r) {
             ptx::mbar_init(&bars->rfull[r], 1);
-            ptx::mbar_init(&bars->rempty[r], 128);
+            ptx::mbar_init(&bars->rempty[r], PRODUCER_THREADS);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&bars->accf[b], 1);
             ptx::mbar_init(&bars->acce[b], FOLD_THREADS);
         }
+        ptx::mbar_init(&bars->d2free, FOLD_THREADS);
         ptx::mbar_init(&bars->mma_done, 1);
         bars->abort = 0;
         ptx::fence_mbar_init();
@@ -269,199 +367,256 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            int last_b[STAGES], last_r[MAX_RSTAGES];
-            for (int s = 0; s < STAGES; ++s) last_b[s] = -1;
+            int64_t last_r[MAX_RSTAGES];
             for (int r = 0; r < MAX_RSTAGES; ++r) last_r[r] = -1;
-            for (int kb = 0; kb < p.num_kb; ++kb) {
-                if constexpr (TMA_A) {
-                    const int r = kb % Raw::RSTAGES;
-                    const uint32_t rph = (kb / Raw::RSTAGES) & 1;
-                    if (!ptx::mbar_wait_bounded(&bars->rempty[r], rph ^ 1, abort, true, WAIT_NS,
-                                                &timed_out))
-                        break;
-                    ptx::mbar_arrive_expect_tx(&bars->rfull[r],
-                                               static_cast<uint32_t>(Raw::ROW_BYTES * BK));
-                    ptx::tma_load_2d(ring + r * Raw::SLOT, &map_a, &bars->rfull[r], box_x,
-                                     static_cast<int>(a_row0 + static_cast<int64_t>(kb) * BK));
-                    last_r[r] = kb;
-                }
-                const int s = kb % STAGES;
-                const uint32_t ph = (kb / STAGES) & 1;
-                if (!ptx::mbar_wait_bounded(&bars->empty[s], ph ^ 1, abort, true, WAIT_NS,
-                                            &timed_out))
+            int64_t g = 0;
+            for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), ++g) {
+                const Tile &t = w.t;
+                // ring slot free (producers done with g - RSTAGES), B stage
+                // free (MMAs of g - B_STAGES completed)
+                const int r = static_cast<int>(g % Raw::RSTAGES);
+                const int s = static_cast<int>(g % B_STAGES);
+                if (!ptx::mbar_wait_bounded(&bars->rempty[r],
+                                            (static_cast<uint32_t>(g / Raw::RSTAGES) & 1) ^ 1,
+                                            abort, true, WAIT_NS, &timed_out) ||
+                    !ptx::mbar_wait_bounded(&bars->bempty[s],
+                                            (static_cast<uint32_t>(g / B_STAGES) & 1) ^ 1, abort,
+                                            true, WAIT_NS, &timed_out))
                     break;
-                if (p.inject == 1 && kb == 0) continue;   // test hook: drop one stage
+                if (p.inject == 1 && g == 0) continue;   // test hook: drop one iteration
                 uint8_t *st = smem + s * STAGE_BYTES;
-                ptx::mbar_arrive_expect_tx(&bars->bfull[s], 2 * B_IMG);
-                if constexpr (GROUPED) {
-                    ptx::tma_load_2d(st + 2 * A_IMG, &map_bhi, &bars->bfull[s], kb * BK,
-                                     static_cast<int>(brow0));
-                    ptx::tma_load_2d(st + 2 * A_IMG + B_IMG, &map_blo, &bars->bfull[s], kb * BK,
-                                     static_cast<int>(brow0));
-                } else {
-                    ptx::tma_load_3d(st + 2 * A_IMG, &map_bhi, &bars->bfull[s], kb * BK,
-                                     nt * BN, static_cast<int>(slice));
-                    ptx::tma_load_3d(st + 2 * A_IMG + B_IMG, &map_blo, &bars->bfull[s], kb * BK,
-                                     nt * BN, static_cast<int>(slice));
+                ptx::mbar_arrive_expect_tx(
+                    &bars->rfull[r],
+                    static_cast<uint32_t>(2 * B_IMG + (TMA_A ? Raw::ROW_BYTES * BK : 0)));
+                if constexpr (TMA_A) {
+                    const int box_x = elementwise_type<TYPE>()
+                                          ? t.mt * BM
+                                          : ((t.mt * 4 * Raw::BLOCK) & ~15);
+                    ptx::tma_load_2d(ring + r * Raw::SLOT, &map_a, &bars->rfull[r], box_x,
+                                     static_cast<int>(t.a_row0 + static_cast<int64_t>(w.kb) * BK));
                 }
-                last_b[s] = kb;
+                if constexpr (GROUPED) {
+                    ptx::tma_load_2d(st, &map_bhi, &bars->rfull[r], w.kb * BK,
+                                     static_cast<int>(t.brow0));
+                    ptx::tma_load_2d(st + B_IMG, &map_blo, &bars->rfull[r], w.kb * BK,
+                                     static_cast<int>(t.brow0));
+                } else {
+                    ptx::tma_load_3d(st, &map_bhi, &bars->rfull[r], w.kb * BK, t.nt * BN,
+                                     static_cast<int>(t.slice));
+                    ptx::tma_load_3d(st + B_IMG, &map_blo, &bars->rfull[r], w.kb * BK,
+                                     t.nt * BN, static_cast<int>(t.slice));
+                }
+                last_r[r] = g;
             }
             // copies in flight must land before the CTA's smem is released
-            for (int s = 0; s < STAGES; ++s)
-                if (last_b[s] >= 0)
-                    ptx::mbar_wait_bounded(&bars->bfull[s], (last_b[s] / STAGES) & 1, abort,
-                                           false, WAIT_NS, &timed_out);
             for (int r = 0; r < Raw::RSTAGES; ++r)
                 if (last_r[r] >= 0)
-                    ptx::mbar_wait_bounded(&bars->rfull[r], (last_r[r] / Raw::RSTAGES) & 1,
+                    ptx::mbar_wait_bounded(&bars->rfull[r],
+                                           static_cast<uint32_t>(last_r[r] / Raw::RSTAGES) & 1,
                                            abort, false, WAIT_NS, &timed_out);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
-            int kb = 0;
-            bool ok = true;
-            for (int q = 0; q < nchunks && ok; ++q) {
-                const int buf = q & 1;
-                const uint32_t use = static_cast<uint32_t>(q >> 1);
-                if (!ptx::mbar_wait_bounded(&bars->acce[buf], (use & 1) ^ 1, abort, true,
-                                            WAIT_NS, &timed_out)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t d1 = tmem + static_cast<uint32_t>(buf * BN);
-                const uint32_t d2 = tmem + COL_D2;
-                const int kb_first = q * p.chunk_kb;
-                const int kb_end = min(p.num_kb, kb_first + p.chunk_kb);
-                for (; kb < kb_end; ++kb) {
-                    const int s = kb % STAGES;
-                    const uint32_t ph = (kb / STAGES) & 1;
-                    if (!ptx::mbar_wait_bounded(&bars->bfull[s], ph, abort, true, WAIT_NS,
-                                                &timed_out) ||
-                        !ptx::mbar_wait_bounded(&bars->afull[s], ph, abort, true, WAIT_NS,
-                                                &timed_out)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint32_t st = ptx::smem_u32(smem + s * STAGE_BYTES);
-                    const uint32_t ahi = st, alo = st + A_IMG;
-                    const uint32_t bhi = st + 2 * A_IMG, blo = st + 2 * A_IMG + B_IMG;
+        // The whole warp runs the loop, so its control flow and operands are
+        // warp-uniform (kept in uniform registers); one elected lane issues.
+        constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
+        const uint32_t d2 = tmem + COL_D2;
+        const uint64_t desc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(smem));
+        int64_t g = 0, q = -1, seg = -1;     // iteration, chunk, segment counters
+        int seg_kb0 = 0;
+        // A test of a barrier costs ~100 cycles even when its phase is long
+        // complete, so the barriers of iteration g+1 are tested early, while
+        // the MMAs of g are being issued; the full wait runs only when such
+        // an early test came back negative.
+        bool early_a = false, early_e = false;
+        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), ++g) {
+            const bool seg_first = g == 0 || w.kb == 0;
+            if (seg_first) {
+                ++seg;
+                seg_kb0 = w.kb;
+            }
+            const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
+            const bool chunk_last = in_chunk == CHUNK_KB - 1 || w.kb + 1 == p.num_kb ||
+                                    w.it + 1 == w.end;
+            if (in_chunk == 0) ++q;
+            const int buf = static_cast<int>(q & 1);
+            const int s = static_cast<int>(g % B_STAGES);
+            const int sa = static_cast<int>(g % A_STAGES);
+            // D1 buffer drained by the fold; D2 read at the previous segment's
+            // end; this block's A stage written (its producers also saw its B
+            // stage land)
+            if ((in_chunk == 0 && !__all_sync(0xffffffffu, early_e) &&
+                 !warp_wait(&bars->acce[buf], (static_cast<uint32_t>(q >> 1) & 1) ^ 1, abort,
+                            &timed_out)) ||
+                (seg_first && seg > 0 &&
+                 !warp_wait(&bars->d2free, static_cast<uint32_t>(seg - 1) & 1, abort,
+                            &timed_out)) ||
+                (!__all_sync(0xffffffffu, early_a) &&
+                 !warp_wait(&bars->afull[sa], static_cast<uint32_t>(g / A_STAGES) & 1, abort,
+                            &timed_out)))
+                break;
+            // early tests for g+1 (its A stage; its D1 buffer if it starts a chunk)
+            early_a = ptx::mbar_test_wait(&bars->afull[(g + 1) % A_STAGES],
+                                          static_cast<uint32_t>((g + 1) / A_STAGES) & 1);
+            early_e = chunk_last &&
+                      ptx::mbar_test_wait(&bars->acce[(q + 1) & 1],
+                                          (static_cast<uint32_t>((q + 1) >> 1) & 1) ^ 1);
+            ptx::tc_fence_after();
+            const uint32_t d1 = tmem + static_cast<uint32_t>(buf * BN);
+            const uint32_t ahi = tmem + COL_A + static_cast<uint32_t>(sa) * A_COLS;
+            const uint32_t alo = ahi + BK;
+            // descriptor start addresses count 16-byte units
+            const uint64_t dhi = desc0 + static_cast<uint64_t>((s * STAGE_BYTES) >> 4);
+            const uint64_t dlo = dhi + (B_IMG >> 4);
+            if (ptx::elect_one()) {
+                if constexpr (HAS_ALO) {
+                    // cross terms a_lo*b_hi + a_hi*b_lo into D2 (over the whole
+                    // segment), the big term a_hi*b_hi into D1 (per chunk)
+                    ptx::mma_block_3xtf32(d1, d2, ahi, alo, dhi, dlo, idesc, in_chunk == 0,
+                                          seg_first);
+                } else {
+                    // bf16 src0: a_lo is zero, one cross term
 #pragma unroll
                     for (int kk = 0; kk < BK / 8; ++kk) {
-                        const uint32_t off = kk * 32;   // 8 tf32 along k
-                        const uint32_t acc2 = (kb == 0 && kk == 0) ? 0u : 1u;
-                        const uint32_t acc1 = (kb == kb_first && kk == 0) ? 0u : 1u;
-                        ptx::mma_tf32(d2, ptx::sw128_kmajor_desc(alo + off),
-                                      ptx::sw128_kmajor_desc(bhi + off), idesc, acc2);
-                        ptx::mma_tf32(d2, ptx::sw128_kmajor_desc(ahi + off),
-                                      ptx::sw128_kmajor_desc(blo + off), idesc, 1u);
-                        ptx::mma_tf32(d1, ptx::sw128_kmajor_desc(ahi + off),
-                                      ptx::sw128_kmajor_desc(bhi + off), idesc, acc1);
+                        const uint64_t off = kk * 2;    // 8 tf32 = 32 bytes along k
+                        ptx::mma_tf32_ta(d2, ahi + kk * 8, dlo + off, idesc,
+                                         (seg_first && kk == 0) ? 0u : 1u);
+                        ptx::mma_tf32_ta(d1, ahi + kk * 8, dhi + off, idesc,
+                                         (in_chunk == 0 && kk == 0) ? 0u : 1u);
                     }
-                    ptx::mma_commit(&bars->empty[s]);
                 }
-                if (!ok) break;
-                ptx::mma_commit(&bars->accf[buf]);
+                ptx::mma_commit(&bars->bempty[s]);
+                if (chunk_last) ptx::mma_commit(&bars->accf[buf]);
             }
-            // every MMA issued must finish before TMEM is released
+            __syncwarp();
+        }
+        // every MMA issued must finish before TMEM is released
+        if (ptx::elect_one()) {
             ptx::mma_commit(&bars->mma_done);
             ptx::mbar_wait_bounded(&bars->mma_done, 0, abort, false, WAIT_NS, &timed_out);
         }
-    } else if (warp < 6) {
+        __syncwarp();
+    } else if (warp < 10) {
         // ---------------- src0 producer ----------------
-        const int r = (warp - 2) * 32 + lane;              // row of the A image
-        const int64_t m = static_cast<int64_t>(mt) * BM + r;
-        const bool mok = m < p.M;
-        const uint8_t *a_slice = p.a + a_row0 * p.a_row_bytes;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t ph = (kb / STAGES) & 1;
-            float x[BK];
-            const bool kfull = (kb + 1) * BK <= p.K;
+        const int quad = warp & 3;                       // TMEM lanes 32*quad ..
+        const int kh = (warp - 2) >> 2;                  // k rows KH*kh .. of each block
+        const int r = 32 * quad + lane;                  // row of the m-tile
+        const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+        int64_t g = 0;
+        bool early_r = false;
+        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), ++g) {
+            const Tile &t = w.t;
+            const int64_t m = static_cast<int64_t>(t.mt) * BM + r;
+            const bool mok = m < p.M;
+            const int64_t k0 = static_cast<int64_t>(w.kb) * BK + kh * KH;
+            const bool kfull = k0 + KH <= p.K;
+            float x[KH];
+            // every copy of this iteration landed: its raw src0 rows and, for
+            // the MMA that waits on this warp, its B stage
+            const int rs = static_cast<int>(g % Raw::RSTAGES);
+            if (!__all_sync(0xffffffffu, early_r) &&
+                !warp_wait(&bars->rfull[rs], static_cast<uint32_t>(g / Raw::RSTAGES) & 1, abort,
+                           &timed_out))
+                break;
+            // early test for g+1 (see the MMA issuer): its latency hides
+            // behind this iteration's work
+            early_r = ptx::mbar_test_wait(&bars->rfull[(g + 1) % Raw::RSTAGES],
+                                          static_cast<uint32_t>((g + 1) / Raw::RSTAGES) & 1);
             if constexpr (TMA_A) {
-                const int rs = kb % Raw::RSTAGES;
-                const uint32_t rph = (kb / Raw::RSTAGES) & 1;
-                if (!ptx::mbar_wait_bounded(&bars->rfull[rs], rph, abort, true, WAIT_NS,
-                                            &timed_out))
-                    break;
-                const uint8_t *slot = ring + rs * Raw::SLOT;
-                // one path per warp: the producer warps never diverge
-                if (__all_sync(0xffffffffu, mok) && kfull) {
-#pragma unroll
-                    for (int j = 0; j < BK; ++j)
-                        x[j] = staged_a<TYPE>(slot + j * Raw::ROW_BYTES, r, off0);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < BK; ++j) {
-                        const int64_t k = static_cast<int64_t>(kb) * BK + j;
-                        const float v = staged_a<TYPE>(slot + j * Raw::ROW_BYTES, r, off0);
-                        x[j] = (mok && k < p.K) ? v : 0.f;
-                    }
+                int off0 = 0;
+                if constexpr (!elementwise_type<TYPE>()) {
+                    const int byte0 = t.mt * 4 * Raw::BLOCK;
+                    off0 = byte0 - (byte0 & ~15);
                 }
                 __syncwarp();
-                ptx::mbar_arrive(&bars->rempty[rs]);
-            } else {
+                staged_half<TYPE>(ring + rs * Raw::SLOT, r, off0, lane, kh, x);
+                // rows past M and k past K read whatever the box holds there
+                if (!(__all_sync(0xffffffffu, mok) && kfull)) {
 #pragma unroll
-                for (int j = 0; j < BK; ++j) {
-                    const int64_t k = static_cast<int64_t>(kb) * BK + j;
+                    for (int j = 0; j < KH; ++j)
+                        if (!mok || k0 + j >= p.K) x[j] = 0.f;
+                }
+            } else {
+                const uint8_t *a_slice = p.a + t.a_row0 * p.a_row_bytes;
+#pragma unroll
+                for (int j = 0; j < KH; ++j) {
+                    const int64_t k = k0 + j;
                     x[j] = (mok && k < p.K) ? load_a<TYPE>(a_slice + k * p.a_row_bytes, m) : 0.f;
                 }
             }
             __syncwarp();
-            if (!ptx::mbar_wait_bounded(&bars->empty[s], ph ^ 1, abort, true, WAIT_NS,
-                                        &timed_out))
-                break;
-            __syncwarp();
-            uint8_t *ahi = smem + s * STAGE_BYTES;
-            uint8_t *alo = ahi + A_IMG;
+            ptx::mbar_arrive(&bars->rempty[rs]);
+            uint32_t hi[KH], lo[KH];
 #pragma unroll
-            for (int c = 0; c < BK / 4; ++c) {
-                uint32_t h[4], l[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if constexpr (TYPE == OOP_TYPE_F32) {
-                        ptx::split_tf32(x[4 * c + e], h[e], l[e]);
-                    } else {
-                        // d*q has at most 18 significant bits and a bf16 value
-                        // 8: x - hi is already a TF32 value (zero for bf16),
-                        // no second rounding needed
-                        h[e] = ptx::tf32_round_bits(__float_as_uint(x[4 * c + e]));
-                        l[e] = __float_as_uint(x[4 * c + e] - __uint_as_float(h[e]));
-                    }
+            for (int e = 0; e < KH; ++e) {
+                if constexpr (TYPE == OOP_TYPE_F32) {
+                    ptx::split_tf32(x[e], hi[e], lo[e]);
+                } else {
+                    // d*q has at most 18 significant bits: x - hi is already
+                    // a TF32 value, no second rounding needed
+                    hi[e] = ptx::tf32_round_bits(__float_as_uint(x[e]));
+                    lo[e] = __float_as_uint(x[e] - __uint_as_float(hi[e]));
                 }
-                const int off = r * 128 + ((c ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(ahi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4 *>(alo + off) = make_uint4(l[0], l[1], l[2], l[3]);
             }
-            __syncwarp();
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(&bars->afull[s]);
+            // A stage g % A_STAGES is free once the MMAs of g - A_STAGES completed
+            const int sa = static_cast<int>(g % A_STAGES);
+            if (g >= A_STAGES) {
+                const int64_t gp = g - A_STAGES;
+                if (!warp_wait(&bars->bempty[gp % B_STAGES],
+                               static_cast<uint32_t>(gp / B_STAGES) & 1, abort, &timed_out))
+                    break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a_st = tmem + lane_off + COL_A + static_cast<uint32_t>(sa) * A_COLS;
+            ptx::tmem_st16(a_st + KH * kh, hi);
+            if constexpr (HAS_ALO) ptx::tmem_st16(a_st + BK + KH * kh, lo);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bars->afull[sa]);
         }
     } else {
         // ---------------- fold + epilogue ----------------
         const int quad = warp & 3;                          // TMEM lanes 32*quad ..
-        const int half = (warp - 6) >> 2;                   // columns 64*half ..
+        const int half = (warp - 10) >> 2;                  // columns FOLD_COLS*half ..
         const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
-        const uint32_t col0 = static_cast<uint32_t>(64 * half);
-        const int64_t m = static_cast<int64_t>(mt) * BM + 32 * quad + lane;
-        float *dst = GROUPED ? p.dst : p.dst + slice * p.N * p.M;
-        const int64_t tile_cols = ncols - static_cast<int64_t>(nt) * BN;   // valid columns here
-        uint64_t cmp[32];                                   // Kahan compensations, in pairs
-#pragma unroll
-        for (int j = 0; j < 32; ++j) cmp[j] = 0;
-        for (int q = 0; q < nchunks; ++q) {
-            const int buf = q & 1;
-            const uint32_t use = static_cast<uint32_t>(q >> 1);
-            if (!ptx::mbar_wait_bounded(&bars->accf[buf], use & 1, abort, true, WAIT_NS,
-                                        &timed_out))
+        const uint32_t col0 = static_cast<uint32_t>(FOLD_COLS * half);
+        const int row = 32 * quad + lane;
+        // Kahan compensations, two columns per register as bfloat16: C is at
+        // most about half an ulp of S, so rounding it to 8 bits costs ~2^-9
+        // ulp of S per fold
+        uint32_t cmp[FOLD_COLS / 2];
+        int seg_kb0 = 0;
+        int64_t g = 0, q = -1;
+        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), ++g) {
+            if (g == 0 || w.kb == 0) seg_kb0 = w.kb;
+            const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
+            const bool last = w.kb + 1 == p.num_kb || w.it + 1 == w.end;   // segment ends
+            if (in_chunk == 0) ++q;
+            if (in_chunk != CHUNK_KB - 1 && !last) continue;   // once per chunk
+            const Tile &t = w.t;
+            const int buf = static_cast<int>(q & 1);
+            if (!warp_wait(&bars->accf[buf], static_cast<uint32_t>(q >> 1) & 1, abort,
+                           &timed_out))
                 break;
             ptx::tc_fence_after();
-            const bool first = q == 0, last = q == nchunks - 1;
+            const bool first = w.kb - seg_kb0 < CHUNK_KB;       // segment's first chunk
+            if (first) {
 #pragma unroll
-            for (int pc = 0; pc < 4; ++pc) {
+                for (int j = 0; j < FOLD_COLS / 2; ++j) cmp[j] = 0;
+            }
+            // where a finished segment goes: dst, or a stream-K partial slot
+            // (slot 0 for the CTA's first segment, 1 for its last)
+            const bool whole = seg_kb0 == 0 && w.kb + 1 == p.num_kb;
+            const int64_t m = static_cast<int64_t>(t.mt) * BM + row;
+            float *dst = GROUPED ? p.dst : p.dst + t.slice * p.N * p.M;
+            float *part = nullptr;
+            if (last && !whole)
+                part = p.partial + (static_cast<int64_t>(blockIdx.x) * 2 +
+                                    (w.it - w.kb + seg_kb0 == it0 ? 0 : 1)) *
+                                       (BM * BN);
+            const int64_t tile_cols = t.ncols - static_cast<int64_t>(t.nt) * BN;
+#pragma unroll
+            for (int pc = 0; pc < FOLD_COLS / 16; ++pc) {
                 const uint32_t col = col0 + pc * 16;
                 // tcgen05.ld/st are warp-collective (.sync.aligned): the lanes
                 // must be converged after the divergent stores of the last piece
@@ -476,13 +631,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 16; j += 2) {
                         // Kahan on two columns at once: the running sum is S - C
-                        uint64_t &c2 = cmp[pc * 8 + j / 2];
+                        uint32_t &cb = cmp[pc * 8 + j / 2];
+                        const uint64_t c2 = ptx::unpack_bf16x2(cb);
                         const uint64_t s2 = ptx::pack2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1]));
                         const uint64_t x2 = ptx::pack2(__uint_as_float(xv[j]), __uint_as_float(xv[j + 1]));
                         const uint64_t y2 = ptx::sub2(x2, c2);
                         const uint64_t t2 = ptx::add2(s2, y2);
-                        c2 = ptx::sub2(ptx::sub2(t2, s2), y2);
-                        float t0, t1;
+                        float t0, t1, n0, n1;
+                        ptx::unpack2(ptx::sub2(ptx::sub2(t2, s2), y2), n0, n1);
+                        cb = ptx::pack_bf16x2(n0, n1);
                         ptx::unpack2(t2, t0, t1);
                         xv[j] = __float_as_uint(t0);
                         xv[j + 1] = __float_as_uint(t1);
@@ -497,21 +654,26 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 16; j += 2) {
                             float c0, c1;
-                            ptx::unpack2(cmp[pc * 8 + j / 2], c0, c1);
+                            ptx::unpack2(ptx::unpack_bf16x2(cmp[pc * 8 + j / 2]), c0, c1);
+                            const float v0 = __uint_as_float(xv[j]) + (__uint_as_float(dv[j]) - c0);
+                            const float v1 =
+                                __uint_as_float(xv[j + 1]) + (__uint_as_float(dv[j + 1]) - c1);
                             const int64_t jc = static_cast<int64_t>(col) + j;   // column in tile
+                            if (part) {
+                                part[jc * BM + row] = v0;
+                                part[(jc + 1) * BM + row] = v1;
+                                continue;
+                            }
                             int64_t r0 = -1, r1 = -1;                            // dst rows
                             if constexpr (GROUPED) {
-                                if (jc < tile_cols) r0 = p.grp_rows[brow0 + jc];
-                                if (jc + 1 < tile_cols) r1 = p.grp_rows[brow0 + jc + 1];
+                                if (jc < tile_cols) r0 = p.grp_rows[t.brow0 + jc];
+                                if (jc + 1 < tile_cols) r1 = p.grp_rows[t.brow0 + jc + 1];
                             } else {
-                                if (jc < tile_cols) r0 = static_cast<int64_t>(nt) * BN + jc;
-                                if (jc + 1 < tile_cols) r1 = static_cast<int64_t>(nt) * BN + jc + 1;
+                                if (jc < tile_cols) r0 = static_cast<int64_t>(t.nt) * BN + jc;
+                                if (jc + 1 < tile_cols) r1 = static_cast<int64_t>(t.nt) * BN + jc + 1;
                             }
-                            if (r0 >= 0)
-                                dst[r0 * p.M + m] = __uint_as_float(xv[j]) + (__uint_as_float(dv[j]) - c0);
-                            if (r1 >= 0)
-                                dst[r1 * p.M + m] =
-                                    __uint_as_float(xv[j + 1]) + (__uint_as_float(dv[j + 1]) - c1);
+                            if (r0 >= 0) dst[r0 * p.M + m] = v0;
+                            if (r1 >= 0) dst[r1 * p.M + m] = v1;
                         }
                     }
                 } else {
@@ -521,6 +683,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
+            if (last) ptx::mbar_arrive(&bars->d2free);
             ptx::mbar_arrive(&bars->acce[buf]);
         }
     }
@@ -531,6 +694,52 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// Stream-K fix-up, one CTA per tile: a tile whose iterations belong to two or
+// more CTAs gets the sum of their partials, in CTA (= k) order, with a Kahan
+// compensation, rounded once.  Tiles owned by one CTA were written by it and
+// are skipped.
+constexpr int FIX_THREADS = 256;
+constexpr int FIX_PER = BM * BN / FIX_THREADS;
+static_assert(BM * BN % FIX_THREADS == 0, "fix-up tiling");
+
+__global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__restrict__ partial,
+                                                               float *__restrict__ dst, int64_t M,
+                                                               int64_t N, int mtiles, int ntiles,
+                                                               int num_kb, int64_t iters,
+                                                               int ctas) {
+    const int64_t t = blockIdx.x;
+    const int64_t x0 = t * num_kb, x1 = x0 + num_kb - 1;
+    const int64_t c0 = sk_owner(iters, ctas, x0), c1 = sk_owner(iters, ctas, x1);
+    if (c0 == c1) return;
+    float sum[FIX_PER], cmp[FIX_PER];
+#pragma unroll
+    for (int j = 0; j < FIX_PER; ++j) sum[j] = cmp[j] = 0.f;
+    for (int64_t c = c0; c <= c1; ++c) {
+        // CTA c's segment of this tile is its first (slot 0) if it starts in it
+        const int slot = sk_begin(iters, ctas, c) >= x0 ? 0 : 1;
+        const float *src = partial + (c * 2 + slot) * (BM * BN);
+#pragma unroll
+        for (int j = 0; j < FIX_PER; ++j) {
+            const float y = __ldg(src + threadIdx.x + j * FIX_THREADS) - cmp[j];
+            const float s2 = sum[j] + y;
+            cmp[j] = (s2 - sum[j]) - y;
+            sum[j] = s2;
+        }
+    }
+    const int mt = static_cast<int>(t % mtiles);
+    const int64_t rest = t / mtiles;
+    const int nt = static_cast<int>(rest % ntiles);
+    const int64_t slice = rest / ntiles;
+    float *d = dst + slice * N * M;
+#pragma unroll
+    for (int j = 0; j < FIX_PER; ++j) {
+        const int e = threadIdx.x + j * FIX_THREADS;
+        const int64_t m = static_cast<int64_t>(mt) * BM + e % BM;
+        const int64_t n = static_cast<int64_t>(nt) * BN + e / BM;
+        if (m < M && n < N) d[n * M + m] = sum[j] - cmp[j];
     }
 }
 
@@ -712,16 +921,47 @@ int64_t padded_k(int64_t K) { return (K + 3) / 4 * 4; }
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int g_inject = 0;
+int g_schedule = 0;     // test hook: 0 automatic, 1 data-parallel, 2 stream-K
 thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
-#ifndef OOP_TC_CHUNK_KB
-#define OOP_TC_CHUNK_KB 2
-#endif
-int g_chunk_kb = OOP_TC_CHUNK_KB;      // k-blocks (of 32) per D1 accumulation
+
+// Stream-K uses at most this many CTAs (one per SM); its partial slots are
+// part of the workspace.
+constexpr int kSkMaxCtas = 160;
+constexpr size_t kSlotBytes = size_t(BM) * BN * 4;
+
+int device_sms() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Stream-K or data-parallel for `tiles` tiles of `num_kb` k-blocks on `sms`
+// SMs.  Returns the stream-K CTA count, 0 for data-parallel.  Stream-K pays
+// when the last data-parallel wave would run mostly empty; each CTA then
+// costs about eight k-blocks more (partial stores and the fix-up).
+int plan_ctas(int64_t tiles, int num_kb, int sms, size_t partial_room) {
+    const int64_t iters = tiles * num_kb;
+    const int G = static_cast<int>(std::min<int64_t>(std::min(sms, kSkMaxCtas), iters));
+    if (G <= 0 || g_schedule == 1 || partial_room < static_cast<size_t>(G) * 2 * kSlotBytes)
+        return 0;
+    if (g_schedule == 2) return G;
+    if (iters < 16LL * G) return 0;
+    const int64_t dp = (tiles + G - 1) / G * num_kb;
+    const int64_t sk = (iters + G - 1) / G + 8;
+    return 10 * sk < 9 * dp ? G : 0;
+}
 
 template <int TYPE, bool GROUPED>
 cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap &mhi,
-                         const CUtensorMap &mlo, const TcParams &p, int64_t grid_x,
-                         int64_t slices, cudaStream_t stream) {
+                         const CUtensorMap &mlo, const TcParams &p, dim3 grid,
+                         cudaStream_t stream) {
     // TMA needs a 16-byte aligned base and row stride, and rows that fit int32.
     const bool tma_a = reinterpret_cast<uintptr_t>(a) % 16 == 0 && s.a_row_bytes % 16 == 0 &&
                        s.K * s.ne02 * s.ne03 < (1LL << 31);
@@ -740,10 +980,10 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
         cudaEvent_t before = g_ev_before, after = g_ev_after;
         g_ev_before = g_ev_after = nullptr;
         if (before && (e = cudaEventRecord(before, stream)) != cudaSuccess) return e;
-        kern<<<dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(slices)), THREADS, smem,
-               stream>>>(mhi, mlo, ma, p);
+        kern<<<grid, THREADS, smem, stream>>>(mhi, mlo, ma, p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+        ++g_kernel_launches;
         if (after && (e = cudaEventRecord(after, stream)) != cudaSuccess) return e;
         return cudaSuccess;
     };
@@ -751,27 +991,41 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
                  : run(tc_out_prod_kernel<TYPE, false, GROUPED>);
 }
 
+size_t split_bytes(const OutProdShape &s) {
+    return align256(static_cast<size_t>(s.ne12 * s.ne13) * static_cast<size_t>(s.N) *
+                    static_cast<size_t>(padded_k(s.K)) * 4);
+}
+
+int64_t tile_count(const OutProdShape &s) {
+    return ((s.M + BM - 1) / BM) * ((s.N + BN - 1) / BN) * s.ne12 * s.ne13;
+}
+
 }  // namespace
 
 void tc_set_inject(int v) { g_inject = v; }
+void tc_set_schedule(int v) { g_schedule = v; }
 void tc_set_profile_events(cudaEvent_t before, cudaEvent_t after) {
     g_ev_before = before;
     g_ev_after = after;
 }
 
+size_t tc_workspace_min_bytes(const OutProdShape &s) { return 2 * split_bytes(s); }
+
 size_t tc_workspace_bytes(const OutProdShape &s) {
-    const size_t one = align256(static_cast<size_t>(s.ne12 * s.ne13) *
-                                static_cast<size_t>(s.N) * static_cast<size_t>(padded_k(s.K)) * 4);
-    return 2 * one;
+    const int64_t iters = tile_count(s) * ((s.K + BK - 1) / BK);
+    const int64_t ctas = std::min<int64_t>(kSkMaxCtas, iters);
+    return tc_workspace_min_bytes(s) + static_cast<size_t>(std::max<int64_t>(ctas, 0)) * 2 * kSlotBytes;
 }
 
 cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const OutProdShape &s,
-                            void *workspace, int *status, cudaStream_t stream) {
+                            void *workspace, size_t workspace_bytes, int *status,
+                            cudaStream_t stream) {
     const int64_t slices = s.ne12 * s.ne13;
     const int64_t Kp = padded_k(s.K);
-    const size_t one = tc_workspace_bytes(s) / 2;
+    const size_t one = split_bytes(s);
     uint32_t *bhi = static_cast<uint32_t *>(workspace);
     uint32_t *blo = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + one);
+    float *partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + 2 * one);
 
     const int64_t gk = (Kp + 31) / 32, gn = (s.N + 31) / 32;
     if (gk > 0x7fffffffLL || gn > 65535 || slices > 65535) return cudaErrorInvalidConfiguration;
@@ -780,6 +1034,7 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
                     dim3(32, 8), 0, stream>>>(b, bhi, blo, s.K, s.N, Kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    ++g_kernel_launches;
 
     CUtensorMap mhi, mlo;
     if (!make_b_map(&mhi, bhi, Kp, s.N, slices) || !make_b_map(&mlo, blo, Kp, s.N, slices))
@@ -801,22 +1056,39 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     if (mtiles * ntiles > 0x7fffffffLL || (s.K + BK - 1) / BK > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     p.num_kb = static_cast<int>((s.K + BK - 1) / BK);
-    p.chunk_kb = g_chunk_kb;
     p.mtiles = static_cast<int>(mtiles);
     p.ntiles = static_cast<int>(ntiles);
     p.inject = g_inject;
     g_inject = 0;
+    const int64_t tiles = mtiles * ntiles * slices;
+    const size_t room = workspace_bytes > 2 * one ? workspace_bytes - 2 * one : 0;
+    p.ctas = plan_ctas(tiles, p.num_kb, device_sms(), room);
+    p.iters = tiles * p.num_kb;
+    p.partial = partial;
+    const dim3 grid = p.ctas > 0 ? dim3(static_cast<unsigned>(p.ctas))
+                                 : dim3(static_cast<unsigned>(mtiles * ntiles),
+                                        static_cast<unsigned>(slices));
 
     switch (s.a_type) {
     case OOP_TYPE_F32:
-        return launch_typed<OOP_TYPE_F32, false>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
+        e = launch_typed<OOP_TYPE_F32, false>(a, s, mhi, mlo, p, grid, stream);
+        break;
     case OOP_TYPE_Q8_0:
-        return launch_typed<OOP_TYPE_Q8_0, false>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
+        e = launch_typed<OOP_TYPE_Q8_0, false>(a, s, mhi, mlo, p, grid, stream);
+        break;
     case OOP_TYPE_Q4_0:
-        return launch_typed<OOP_TYPE_Q4_0, false>(a, s, mhi, mlo, p, mtiles * ntiles, slices, stream);
+        e = launch_typed<OOP_TYPE_Q4_0, false>(a, s, mhi, mlo, p, grid, stream);
+        break;
     default:
         return cudaErrorInvalidValue;
     }
+    if (e != cudaSuccess || p.ctas == 0) return e;
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    sk_fixup_kernel<<<static_cast<unsigned>(tiles), FIX_THREADS, 0, stream>>>(
+        partial, dst, s.M, s.N, p.mtiles, p.ntiles, p.num_kb, p.iters, p.ctas);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) ++g_kernel_launches;
+    return e;
 }
 
 // ---- MUL_MAT_ID_BACK launcher ------------------------------------------------
@@ -878,10 +1150,12 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
                                                         dx, rw, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    ++g_kernel_launches;
     mmid_gsplit_kernel<<<static_cast<unsigned>(t.nslot), 256, 0, stream>>>(
         g, rw.rows, rw.count, static_cast<int>(s.E), ghi, glo, s.N, t.Kp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    ++g_kernel_launches;
 
     CUtensorMap mhi, mlo;
     if (!make_b_map_2d(&mhi, ghi, t.Kp, t.nslot) || !make_b_map_2d(&mlo, glo, t.Kp, t.nslot))
@@ -914,7 +1188,6 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     p.dps3 = 1;
     p.a_row_bytes = os.a_row_bytes;
     p.num_kb = static_cast<int>((os.K + BK - 1) / BK);
-    p.chunk_kb = g_chunk_kb;
     p.mtiles = static_cast<int>(t.mtiles);
     p.ntiles = 0;
     p.inject = 0;
@@ -923,11 +1196,11 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     p.grp_rows = rw.rows;
     p.grp_tiles = rw.tiles;
     p.grp_ntiles = rw.ntiles;
-    const int64_t grid_x = t.mtiles * t.max_tiles;
+    const dim3 grid(static_cast<unsigned>(t.mtiles * t.max_tiles));
     if (s.w_type == OOP_TYPE_F32)
-        return launch_typed<OOP_TYPE_F32, true>(W, os, mhi, mlo, p, grid_x, 1, stream);
+        return launch_typed<OOP_TYPE_F32, true>(W, os, mhi, mlo, p, grid, stream);
     if (s.w_type == OOP_TYPE_BF16)
-        return launch_typed<OOP_TYPE_BF16, true>(W, os, mhi, mlo, p, grid_x, 1, stream);
+        return launch_typed<OOP_TYPE_BF16, true>(W, os, mhi, mlo, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -55,15 +55,19 @@ size_t oop_out_prod_noalloc_scratch_bytes(void) { return oop::kScratchBytes; }
 int oop_out_prod_noalloc(const void *a, int a_type, const float *b, float *dst,
                          const int64_t ne_a[4], const int64_t ne_b[4], const int64_t ne_dst[4],
                          void *stream) {
-    // Shape errors are reported exactly as oop_out_prod reports them.
-    const size_t need = oop_out_prod_workspace_size(a_type, ne_a, ne_b);
+    // Shape errors are reported exactly as oop_out_prod reports them.  The
+    // call needs at least the minimum workspace; whatever of the array is
+    // beyond that lets the tensor-core path pick its stream-K schedule.
+    const size_t need = oop_out_prod_workspace_min_size(a_type, ne_a, ne_b);
     if (need > oop::kScratchBytes) return OOP_ERR_SCRATCH_LIMIT;
+    size_t give = oop_out_prod_workspace_size(a_type, ne_a, ne_b);
+    if (give > oop::kScratchBytes) give = oop::kScratchBytes;
     void *scratch = nullptr;
-    if (need > 0) {
+    if (give > 0) {
         const int rc = oop::scratch_for_current_device(&scratch);
         if (rc != OOP_OK) return rc;
     }
-    return oop_out_prod(a, a_type, b, dst, ne_a, ne_b, ne_dst, scratch, need, stream);
+    return oop_out_prod(a, a_type, b, dst, ne_a, ne_b, ne_dst, scratch, give, stream);
 }
 
 }  // extern "C"

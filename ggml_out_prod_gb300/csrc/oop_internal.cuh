@@ -57,12 +57,20 @@ cudaError_t launch_skinny(const float *a, const float *b, float *dst,
 cudaError_t launch_dense_simt(const void *a, const float *b, float *dst,
                               const OutProdShape &s, cudaStream_t stream);
 
-// Tensor-core OUT_PROD (tcgen05, 3xTF32).
+// Kernels enqueued by the current API call on this thread (each launcher
+// adds its own).
+extern thread_local int g_kernel_launches;
+
+// Tensor-core OUT_PROD (tcgen05, 3xTF32).  The workspace holds the TF32 split
+// of src1 (the minimum) and, after it, the stream-K partial slots; with less
+// than tc_workspace_bytes the data-parallel schedule is used.
 size_t tc_workspace_bytes(const OutProdShape &s);
+size_t tc_workspace_min_bytes(const OutProdShape &s);
 void tc_set_inject(int v);   // test hook: the next tensor-core launch drops one TMA stage
+void tc_set_schedule(int v); // test hook: 0 automatic, 1 data-parallel, 2 stream-K
 void tc_set_profile_events(cudaEvent_t before, cudaEvent_t after);
 cudaError_t launch_dense_tc(const void *a, const float *b, float *dst,
-                            const OutProdShape &s, void *workspace,
+                            const OutProdShape &s, void *workspace, size_t workspace_bytes,
                             int *status, cudaStream_t stream);
 
 // MUL_MAT_ID_BACK as a grouped tensor-core product (slots sorted by expert).

@@ -54,13 +54,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same condition (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete, for at most
 // `limit_ns` nanoseconds.  Gives up early when *abort is set (and
 // honor_abort).  On running out it sets *abort and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   volatile int *abort, bool honor_abort,
                                                   uint64_t limit_ns, bool *timed_out) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -73,6 +86,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
             }
         }
     }
+}
+
+// True in exactly one active lane of the warp (all lanes must call it).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 // ---- TMA ------------------------------------------------------------------
@@ -97,10 +121,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---- tcgen05 ----------------------------------------------------------------
@@ -129,14 +149,52 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::tf32, one CTA.
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::tf32, one CTA.  A occupies
+// lanes 0..M-1 (row i in lane i) and 8 consecutive 32-bit columns (k).
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// One 32-k block of the 3xTF32 product, A from tensor memory, in one
+// statement (the accumulate predicates are set once, not per MMA):
+//   for kk = 0..3 (8 k each; A columns +8*kk, B descriptors +2*kk, i.e. 32
+//   bytes along the swizzled k row):
+//     d2 (+)= a_lo * b_hi ; d2 += a_hi * b_lo ; d1 (+)= a_hi * b_hi
+// d2 starts fresh at kk = 0 when `fresh2`, d1 when `fresh1`.
+__device__ __forceinline__ void mma_block_3xtf32(uint32_t d1, uint32_t d2, uint32_t ahi,
+                                                 uint32_t alo, uint64_t bhi, uint64_t blo,
+                                                 uint32_t idesc, uint32_t fresh1,
+                                                 uint32_t fresh2) {
+    asm volatile(
+        "{\n\t.reg .pred p1, p2, pt;\n\t"
+        "setp.eq.b32 p1, %7, 0;\n\t"
+        "setp.eq.b32 p2, %8, 0;\n\t"
+        "setp.eq.b32 pt, 0, 0;\n\t"
+        ".reg .b32 a0, a1, a2, a3, l0, l1, l2, l3;\n\t"
+        ".reg .b64 h0, h1, h2, h3, o0, o1, o2, o3;\n\t"
+        "mov.b32 a0, %2;\n\tadd.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
+        "mov.b32 l0, %3;\n\tadd.u32 l1, %3, 8;\n\tadd.u32 l2, %3, 16;\n\tadd.u32 l3, %3, 24;\n\t"
+        "mov.b64 h0, %4;\n\tadd.u64 h1, %4, 2;\n\tadd.u64 h2, %4, 4;\n\tadd.u64 h3, %4, 6;\n\t"
+        "mov.b64 o0, %5;\n\tadd.u64 o1, %5, 2;\n\tadd.u64 o2, %5, 4;\n\tadd.u64 o3, %5, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [l0], h0, %6, p2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [a0], o0, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a0], h0, %6, p1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [l1], h1, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [a1], o1, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a1], h1, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [l2], h2, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [a2], o2, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a2], h2, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [l3], h3, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [a3], o3, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a3], h3, %6, pt;\n\t}" ::"r"(d1),
+        "r"(d2), "r"(ahi), "r"(alo), "l"(bhi), "l"(blo), "r"(idesc), "r"(fresh1), "r"(fresh2)
         : "memory");
 }
 
@@ -148,53 +206,7 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
         : "memory");
 }
 
-#define OOP_R32(X)                                                                            \
-    X[0], X[1], X[2], X[3], X[4], X[5], X[6], X[7], X[8], X[9], X[10], X[11], X[12], X[13], \
-        X[14], X[15], X[16], X[17], X[18], X[19], X[20], X[21], X[22], X[23], X[24], X[25],   \
-        X[26], X[27], X[28], X[29], X[30], X[31]
-
-// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base lane + i).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-            taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-// 32 lanes x 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
-
+// 32 lanes x 16 consecutive 32-bit columns: thread i writes lane (base + i).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -311,10 +323,16 @@ __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
     return r;
 }
 
-// A small integer (|v| < 2^22) as float: place it in the mantissa of
-// 1.5 * 2^23 (whose ulp is 1) and subtract that constant.  Exact.
-__device__ __forceinline__ float small_int_to_float(int v) {
-    return __int_as_float(0x4B400000 + v) - 12582912.0f;
+// Two floats rounded to bfloat16 (nearest even) in one 32-bit register, the
+// first in the low half; and back.  bfloat16 keeps fp32's exponent range.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t unpack_bf16x2(uint32_t v) {
+    return pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
 // d * v for a small integer v, exactly: with f = 1.5 * 2^23 + v (exact),

@@ -89,13 +89,20 @@ typedef enum {
  * fp16.  Precision: every finite input gives a finite result within
  * 2e-6 * sum_k |a*b| of the exact sum.
  *
- * workspace: device scratch of at least oop_out_prod_workspace_size(...)
- * bytes, 256-byte aligned (NULL allowed when that size is 0).  Its contents on
- * entry do not matter; the call may overwrite all of it.  Two calls in flight
- * at once must not share one workspace.
+ * workspace: device scratch, 256-byte aligned, of
+ * oop_out_prod_workspace_size(...) bytes (NULL allowed when that size is 0).
+ * The tensor-core path holds the TF32 split of src1 there and, after it, the
+ * k-partials of its stream-K schedule; it runs with as little as
+ * oop_out_prod_workspace_min_size(...) bytes, then on its data-parallel
+ * schedule only (same results up to rounding order, maybe slower).  Less
+ * than the minimum returns OOP_ERR_WORKSPACE.  Its contents on entry do not
+ * matter; the call may overwrite all of it.  Two calls in flight at once must
+ * not share one workspace.  Both sizes are 0 for an invalid shape.
  */
 size_t oop_out_prod_workspace_size(int a_type, const int64_t ne_a[4],
                                    const int64_t ne_b[4]);
+size_t oop_out_prod_workspace_min_size(int a_type, const int64_t ne_a[4],
+                                       const int64_t ne_b[4]);
 
 int oop_out_prod(const void *a, int a_type, const float *b, float *dst,
                  const int64_t ne_a[4], const int64_t ne_b[4],
@@ -121,9 +128,9 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst,
  * Same operation, arguments, errors and precision as oop_out_prod, minus the
  * workspace: the scratch is a 64 MiB device array inside this library
  * (oop_out_prod_noalloc_scratch_bytes()), present on every GPU that loads the
- * library until the process exits.  A call whose scratch need
- * (oop_out_prod_workspace_size) exceeds it returns OOP_ERR_SCRATCH_LIMIT and
- * enqueues nothing.  The call allocates nothing: no cudaMalloc, cudaFree or
+ * library until the process exits.  A call whose least scratch need
+ * (oop_out_prod_workspace_min_size) exceeds it returns OOP_ERR_SCRATCH_LIMIT
+ * and enqueues nothing.  The call allocates nothing: no cudaMalloc, cudaFree or
  * allocating library routine.
  *
  * The first call on a device looks up that array's device address (once per
@@ -203,6 +210,22 @@ int oop_profile_main_kernel(void *before, void *after);
  * trapping.  dst is left unspecified by that call.  The flag is consumed by
  * that one launch.  Returns OOP_OK. */
 int oop_debug_inject_timeout(int enable);
+
+/* Test hook (no counterpart on the pages): the schedule of the tensor-core
+ * OUT_PROD tile kernel for the calls that follow on this process.  mode 0 =
+ * automatic (the default: stream-K when the last data-parallel wave would
+ * run mostly empty and the workspace holds the partials), 1 = always
+ * data-parallel (one 128 x 96 dst tile per CTA), 2 = always stream-K (one
+ * CTA per SM sharing the tile x k-block iterations, then a fix-up kernel),
+ * when the workspace allows.  Results agree to rounding order either way.
+ * Returns OOP_OK, or OOP_ERR_PATH for another mode. */
+int oop_debug_set_tc_schedule(int mode);
+
+/* How many kernels the last OUT_PROD or MUL_MAT_ID_BACK call made on this
+ * host thread enqueued (0 after a rejected call or an empty one; memsets are
+ * not kernels).  No counterpart on the pages; for benchmarks that report
+ * their launch count. */
+int oop_last_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,126 @@
+"""GPU parity of the tensor-core OUT_PROD under both tile schedules.
+
+Data-parallel: one 128 (m) x 96 (n) dst tile per CTA.  Stream-K: one CTA per SM
+shares the (tile, k-block) iterations, tiles split between CTAs are summed by
+a fix-up kernel.  Both must meet |gpu - exact| <= 2e-6 * sum_k |a*b| against
+the oracle, stream-K must repeat bit for bit, and the call must enqueue the
+kernels it claims (split pass + tile kernel, + fix-up for stream-K).  The
+shapes are small enough that forced stream-K gives every CTA only a few
+k-blocks, so most tiles are shared by several CTAs (the fix-up's hard case).
+"""
+
+import numpy as np
+import pytest
+
+import synth
+from helpers import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+F32, Q8, Q4 = synth.TYPE_F32, synth.TYPE_Q8_0, synth.TYPE_Q4_0
+
+
+@pytest.fixture(scope="module")
+def op():
+    import torch
+    import ggml_out_prod_gb300 as g
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    g.build()
+    g.lib()
+    yield g
+    g.set_tc_schedule(g.SCHEDULE_AUTO)
+
+
+CASES = [
+    # (type, ne_a, ne_b): ragged m, n and k tails; slices with broadcast
+    (Q8, (640, 1000, 1, 1), (300, 1000, 1, 1)),
+    (Q4, (384, 4096, 1, 1), (256, 4096, 1, 1)),
+    (F32, (200, 300, 2, 1), (70, 300, 4, 3)),
+    (F32, (130, 33, 1, 1), (129, 33, 1, 1)),
+]
+
+
+def _run(op, ta, tb, a_type, ne_a, schedule, workspace=None):
+    import torch
+    op.set_tc_schedule(schedule)
+    try:
+        out = op.out_prod(ta, tb, a_type=a_type, ne_a=ne_a, path=op.PATH_TCGEN05,
+                          workspace=workspace)
+        n = op.last_launch_count()
+        torch.cuda.synchronize()
+    finally:
+        op.set_tc_schedule(op.SCHEDULE_AUTO)
+    assert op.device_status() == 0
+    return out.cpu().numpy(), n
+
+
+@pytest.mark.parametrize("a_type,ne_a,ne_b", CASES)
+def test_schedules_match_oracle(op, orc, a_type, ne_a, ne_b):
+    import torch
+    a = synth.make_a(a_type, ne_a, 60, std=0.02 if a_type != F32 else 1.0)
+    b = synth.make_b(ne_b, 61, std=1e3, outliers=True)
+    ref = orc.out_prod(a, a_type, b, ne_a, ne_b)
+    ta = torch.from_numpy(a).cuda()
+    tb = torch.from_numpy(b).cuda()
+    dp, n_dp = _run(op, ta, tb, a_type, ne_a, op.SCHEDULE_DATA_PARALLEL)
+    sk, n_sk = _run(op, ta, tb, a_type, ne_a, op.SCHEDULE_STREAM_K)
+    sk2, _ = _run(op, ta, tb, a_type, ne_a, op.SCHEDULE_STREAM_K)
+    assert n_dp == 2 and n_sk == 3
+    assert_parity(dp, ref["f64"], ref["abs"], f"data-parallel {a_type} {ne_a}")
+    assert_parity(sk, ref["f64"], ref["abs"], f"stream-K {a_type} {ne_a}")
+    assert np.array_equal(sk.view(np.uint32), sk2.view(np.uint32)), "stream-K not repeatable"
+
+
+def test_minimum_workspace_runs_data_parallel(op, orc):
+    """With only the minimum workspace, a forced stream-K call falls back to
+    the data-parallel schedule (two launches) and stays correct."""
+    import torch
+    a_type, ne_a, ne_b = Q8, (640, 1000, 1, 1), (300, 1000, 1, 1)
+    a = synth.make_a(a_type, ne_a, 62, std=0.02)
+    b = synth.make_b(ne_b, 63, std=1e3, outliers=True)
+    ref = orc.out_prod(a, a_type, b, ne_a, ne_b)
+    need = op.oop_out_prod_workspace_min_size(a_type, ne_a, ne_b)
+    full = op.oop_out_prod_workspace_size(a_type, ne_a, ne_b)
+    assert 0 < need < full
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    got, n = _run(op, torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), a_type, ne_a,
+                  op.SCHEDULE_STREAM_K, workspace=ws)
+    assert n == 2
+    assert_parity(got, ref["f64"], ref["abs"], "minimum workspace")
+
+
+def test_below_minimum_workspace_rejected(op):
+    import torch
+    ne_a, ne_b = (640, 1000, 1, 1), (300, 1000, 1, 1)
+    need = op.oop_out_prod_workspace_min_size(Q8, ne_a, ne_b)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    ta = torch.zeros(1000 * 640 // 32 * 34, dtype=torch.uint8, device="cuda")
+    tb = torch.zeros((1000, 300), dtype=torch.float32, device="cuda")
+    with pytest.raises(op.OopError) as e:
+        op.out_prod(ta, tb, a_type=Q8, ne_a=ne_a, path=op.PATH_TCGEN05, workspace=ws)
+    assert e.value.status == op.ERR_WORKSPACE
+    assert op.last_launch_count() == 0
+
+
+def test_auto_schedule_choice(op):
+    """The automatic schedule takes stream-K exactly when the data-parallel
+    waves (tiles / SMs, rounded up, times the k-blocks per tile) would cost
+    more than 10/9 of an even share of the iterations plus eight k-blocks;
+    shown here on q8_0 [5120, K] x [1024, K] for a short and a long K and a
+    small problem whose one wave is mostly empty."""
+    import torch
+    sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 160)
+    for m, k, n in ((5120, 5120, 1024), (5120, 17408, 1024), (1536, 1536, 1024),
+                    (256, 8192, 96)):
+        ta = torch.zeros(k * m // 32 * 34, dtype=torch.uint8, device="cuda")
+        tb = torch.zeros((k, n), dtype=torch.float32, device="cuda")
+        op.out_prod(ta, tb, a_type=Q8, ne_a=(m, k, 1, 1), path=op.PATH_TCGEN05)
+        got = op.last_launch_count()
+        torch.cuda.synchronize()
+        tiles = -(-m // 128) * -(-n // 96)
+        nkb = -(-k // 32)
+        g = min(sms, tiles * nkb)
+        dp = -(-tiles // g) * nkb
+        sk = -(-(tiles * nkb) // g) + 8
+        want_sk = tiles * nkb >= 16 * g and 10 * sk < 9 * dp
+        assert got == (3 if want_sk else 2), (m, k, n, got)
