@@ -236,6 +236,20 @@ struct Walk {
     }
 };
 
+// Position in a ring of N slots: the slot and the parity of its current use
+// (the parity a "full" wait expects; an "empty" wait expects its negation).
+template <int N>
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next() {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1;
+        }
+    }
+};
+
 template <int TYPE>
 __device__ __forceinline__ float load_a(const uint8_t *row, int64_t m) {
     if constexpr (TYPE == OOP_TYPE_F32) {
@@ -367,21 +381,20 @@ __global__ void __maxnreg__(MAX_REGS)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            int64_t last_r[MAX_RSTAGES];
-            for (int r = 0; r < MAX_RSTAGES; ++r) last_r[r] = -1;
-            int64_t g = 0;
-            for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), ++g) {
+            int last_ph[MAX_RSTAGES];           // parity of each slot's last copy, -1: none
+            for (int r = 0; r < MAX_RSTAGES; ++r) last_ph[r] = -1;
+            Ring<Raw::RSTAGES> rr;
+            Ring<B_STAGES> bb;
+            int g = 0;
+            for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), rr.next(), bb.next(), ++g) {
                 const Tile &t = w.t;
                 // ring slot free (producers done with g - RSTAGES), B stage
                 // free (MMAs of g - B_STAGES completed)
-                const int r = static_cast<int>(g % Raw::RSTAGES);
-                const int s = static_cast<int>(g % B_STAGES);
-                if (!ptx::mbar_wait_bounded(&bars->rempty[r],
-                                            (static_cast<uint32_t>(g / Raw::RSTAGES) & 1) ^ 1,
-                                            abort, true, WAIT_NS, &timed_out) ||
-                    !ptx::mbar_wait_bounded(&bars->bempty[s],
-                                            (static_cast<uint32_t>(g / B_STAGES) & 1) ^ 1, abort,
-                                            true, WAIT_NS, &timed_out))
+                const int r = rr.slot, s = bb.slot;
+                if (!ptx::mbar_wait_bounded(&bars->rempty[r], rr.phase ^ 1, abort, true, WAIT_NS,
+                                            &timed_out) ||
+                    !ptx::mbar_wait_bounded(&bars->bempty[s], bb.phase ^ 1, abort, true, WAIT_NS,
+                                            &timed_out))
                     break;
                 if (p.inject == 1 && g == 0) continue;   // test hook: drop one iteration
                 uint8_t *st = smem + s * STAGE_BYTES;
@@ -406,13 +419,12 @@ __global__ void __maxnreg__(MAX_REGS)
                     ptx::tma_load_3d(st + B_IMG, &map_blo, &bars->rfull[r], w.kb * BK,
                                      t.nt * BN, static_cast<int>(t.slice));
                 }
-                last_r[r] = g;
+                last_ph[r] = static_cast<int>(rr.phase);
             }
             // copies in flight must land before the CTA's smem is released
             for (int r = 0; r < Raw::RSTAGES; ++r)
-                if (last_r[r] >= 0)
-                    ptx::mbar_wait_bounded(&bars->rfull[r],
-                                           static_cast<uint32_t>(last_r[r] / Raw::RSTAGES) & 1,
+                if (last_ph[r] >= 0)
+                    ptx::mbar_wait_bounded(&bars->rfull[r], static_cast<uint32_t>(last_ph[r]),
                                            abort, false, WAIT_NS, &timed_out);
         }
     } else if (warp == 1) {
@@ -422,14 +434,16 @@ __global__ void __maxnreg__(MAX_REGS)
         constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
         const uint32_t d2 = tmem + COL_D2;
         const uint64_t desc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(smem));
-        int64_t g = 0, q = -1, seg = -1;     // iteration, chunk, segment counters
+        int g = 0, q = -1, seg = -1;         // iteration, chunk, segment counters
         int seg_kb0 = 0;
+        Ring<A_STAGES> aa;
+        Ring<B_STAGES> bb;
         // A test of a barrier costs ~100 cycles even when its phase is long
         // complete, so the barriers of iteration g+1 are tested early, while
         // the MMAs of g are being issued; the full wait runs only when such
         // an early test came back negative.
         bool early_a = false, early_e = false;
-        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), ++g) {
+        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), aa.next(), bb.next(), ++g) {
             const bool seg_first = g == 0 || w.kb == 0;
             if (seg_first) {
                 ++seg;
@@ -439,9 +453,8 @@ __global__ void __maxnreg__(MAX_REGS)
             const bool chunk_last = in_chunk == CHUNK_KB - 1 || w.kb + 1 == p.num_kb ||
                                     w.it + 1 == w.end;
             if (in_chunk == 0) ++q;
-            const int buf = static_cast<int>(q & 1);
-            const int s = static_cast<int>(g % B_STAGES);
-            const int sa = static_cast<int>(g % A_STAGES);
+            const int buf = q & 1;
+            const int s = bb.slot, sa = aa.slot;
             // D1 buffer drained by the fold; D2 read at the previous segment's
             // end; this block's A stage written (its producers also saw its B
             // stage land)
@@ -452,12 +465,14 @@ __global__ void __maxnreg__(MAX_REGS)
                  !warp_wait(&bars->d2free, static_cast<uint32_t>(seg - 1) & 1, abort,
                             &timed_out)) ||
                 (!__all_sync(0xffffffffu, early_a) &&
-                 !warp_wait(&bars->afull[sa], static_cast<uint32_t>(g / A_STAGES) & 1, abort,
-                            &timed_out)))
+                 !warp_wait(&bars->afull[sa], aa.phase, abort, &timed_out)))
                 break;
             // early tests for g+1 (its A stage; its D1 buffer if it starts a chunk)
-            early_a = ptx::mbar_test_wait(&bars->afull[(g + 1) % A_STAGES],
-                                          static_cast<uint32_t>((g + 1) / A_STAGES) & 1);
+            {
+                Ring<A_STAGES> an = aa;
+                an.next();
+                early_a = ptx::mbar_test_wait(&bars->afull[an.slot], an.phase);
+            }
             early_e = chunk_last &&
                       ptx::mbar_test_wait(&bars->acce[(q + 1) & 1],
                                           (static_cast<uint32_t>((q + 1) >> 1) & 1) ^ 1);
@@ -502,9 +517,12 @@ __global__ void __maxnreg__(MAX_REGS)
         const int kh = (warp - 2) >> 2;                  // k rows KH*kh .. of each block
         const int r = 32 * quad + lane;                  // row of the m-tile
         const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
-        int64_t g = 0;
+        int g = 0;
         bool early_r = false;
-        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), ++g) {
+        Ring<Raw::RSTAGES> rr;
+        Ring<A_STAGES> aa;
+        Ring<B_STAGES> eb;                               // bempty of iteration g - A_STAGES
+        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), rr.next(), aa.next(), ++g) {
             const Tile &t = w.t;
             const int64_t m = static_cast<int64_t>(t.mt) * BM + r;
             const bool mok = m < p.M;
@@ -513,15 +531,17 @@ __global__ void __maxnreg__(MAX_REGS)
             float x[KH];
             // every copy of this iteration landed: its raw src0 rows and, for
             // the MMA that waits on this warp, its B stage
-            const int rs = static_cast<int>(g % Raw::RSTAGES);
+            const int rs = rr.slot;
             if (!__all_sync(0xffffffffu, early_r) &&
-                !warp_wait(&bars->rfull[rs], static_cast<uint32_t>(g / Raw::RSTAGES) & 1, abort,
-                           &timed_out))
+                !warp_wait(&bars->rfull[rs], rr.phase, abort, &timed_out))
                 break;
             // early test for g+1 (see the MMA issuer): its latency hides
             // behind this iteration's work
-            early_r = ptx::mbar_test_wait(&bars->rfull[(g + 1) % Raw::RSTAGES],
-                                          static_cast<uint32_t>((g + 1) / Raw::RSTAGES) & 1);
+            {
+                Ring<Raw::RSTAGES> rn = rr;
+                rn.next();
+                early_r = ptx::mbar_test_wait(&bars->rfull[rn.slot], rn.phase);
+            }
             if constexpr (TMA_A) {
                 int off0 = 0;
                 if constexpr (!elementwise_type<TYPE>()) {
@@ -559,12 +579,10 @@ __global__ void __maxnreg__(MAX_REGS)
                 }
             }
             // A stage g % A_STAGES is free once the MMAs of g - A_STAGES completed
-            const int sa = static_cast<int>(g % A_STAGES);
+            const int sa = aa.slot;
             if (g >= A_STAGES) {
-                const int64_t gp = g - A_STAGES;
-                if (!warp_wait(&bars->bempty[gp % B_STAGES],
-                               static_cast<uint32_t>(gp / B_STAGES) & 1, abort, &timed_out))
-                    break;
+                if (!warp_wait(&bars->bempty[eb.slot], eb.phase, abort, &timed_out)) break;
+                eb.next();
             }
             ptx::tc_fence_after();
             const uint32_t a_st = tmem + lane_off + COL_A + static_cast<uint32_t>(sa) * A_COLS;
@@ -586,7 +604,7 @@ __global__ void __maxnreg__(MAX_REGS)
         // ulp of S per fold
         uint32_t cmp[FOLD_COLS / 2];
         int seg_kb0 = 0;
-        int64_t g = 0, q = -1;
+        int g = 0, q = -1;
         for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), ++g) {
             if (g == 0 || w.kb == 0) seg_kb0 = w.kb;
             const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
@@ -594,7 +612,7 @@ __global__ void __maxnreg__(MAX_REGS)
             if (in_chunk == 0) ++q;
             if (in_chunk != CHUNK_KB - 1 && !last) continue;   // once per chunk
             const Tile &t = w.t;
-            const int buf = static_cast<int>(q & 1);
+            const int buf = q & 1;
             if (!warp_wait(&bars->accf[buf], static_cast<uint32_t>(q >> 1) & 1, abort,
                            &timed_out))
                 break;
