@@ -335,8 +335,11 @@ __global__ void __maxnreg__(MAX_REGS)
     // this CTA's iterations [it0, it1)
     int64_t it0, it1;
     if (p.ctas > 0) {
-        it0 = sk_begin(p.iters, p.ctas, blockIdx.x);
-        it1 = sk_begin(p.iters, p.ctas, blockIdx.x + 1);
+        // grouped: the tile count is known on the device only
+        const int64_t iters =
+            GROUPED ? static_cast<int64_t>(p.mtiles) * *p.grp_ntiles * p.num_kb : p.iters;
+        it0 = sk_begin(iters, p.ctas, blockIdx.x);
+        it1 = sk_begin(iters, p.ctas, blockIdx.x + 1);
     } else {
         const int64_t t = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
         if constexpr (GROUPED) {
@@ -723,21 +726,25 @@ constexpr int FIX_THREADS = 256;
 constexpr int FIX_PER = BM * BN / FIX_THREADS;
 static_assert(BM * BN % FIX_THREADS == 0, "fix-up tiling");
 
+template <bool GROUPED>
 __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__restrict__ partial,
-                                                               float *__restrict__ dst, int64_t M,
-                                                               int64_t N, int mtiles, int ntiles,
-                                                               int num_kb, int64_t iters,
-                                                               int ctas) {
+                                                               const TcParams p) {
     const int64_t t = blockIdx.x;
-    const int64_t x0 = t * num_kb, x1 = x0 + num_kb - 1;
-    const int64_t c0 = sk_owner(iters, ctas, x0), c1 = sk_owner(iters, ctas, x1);
+    const int64_t tiles = GROUPED ? static_cast<int64_t>(p.mtiles) * *p.grp_ntiles
+                                  : p.iters / p.num_kb;
+    if (t >= tiles) return;
+    const int64_t iters = tiles * p.num_kb;
+    const int64_t x0 = t * p.num_kb, x1 = x0 + p.num_kb - 1;
+    const int64_t c0 = sk_owner(iters, p.ctas, x0), c1 = sk_owner(iters, p.ctas, x1);
     if (c0 == c1) return;
     float sum[FIX_PER], cmp[FIX_PER];
 #pragma unroll
     for (int j = 0; j < FIX_PER; ++j) sum[j] = cmp[j] = 0.f;
     for (int64_t c = c0; c <= c1; ++c) {
+        const int64_t b0 = sk_begin(iters, p.ctas, c);
+        if (b0 == sk_begin(iters, p.ctas, c + 1)) continue;    // a CTA with no iterations
         // CTA c's segment of this tile is its first (slot 0) if it starts in it
-        const int slot = sk_begin(iters, ctas, c) >= x0 ? 0 : 1;
+        const int slot = b0 >= x0 ? 0 : 1;
         const float *src = partial + (c * 2 + slot) * (BM * BN);
 #pragma unroll
         for (int j = 0; j < FIX_PER; ++j) {
@@ -747,17 +754,18 @@ __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__re
             sum[j] = s2;
         }
     }
-    const int mt = static_cast<int>(t % mtiles);
-    const int64_t rest = t / mtiles;
-    const int nt = static_cast<int>(rest % ntiles);
-    const int64_t slice = rest / ntiles;
-    float *d = dst + slice * N * M;
+    const Tile d = decode_tile<GROUPED>(p, t);
+    const int64_t tile_cols = d.ncols - static_cast<int64_t>(d.nt) * BN;
+    float *out = GROUPED ? p.dst : p.dst + d.slice * p.N * p.M;
 #pragma unroll
     for (int j = 0; j < FIX_PER; ++j) {
         const int e = threadIdx.x + j * FIX_THREADS;
-        const int64_t m = static_cast<int64_t>(mt) * BM + e % BM;
-        const int64_t n = static_cast<int64_t>(nt) * BN + e / BM;
-        if (m < M && n < N) d[n * M + m] = sum[j] - cmp[j];
+        const int64_t m = static_cast<int64_t>(d.mt) * BM + e % BM;
+        const int64_t col = e / BM;                               // column in the tile
+        if (m >= p.M || col >= tile_cols) continue;
+        const int64_t row = GROUPED ? p.grp_rows[d.brow0 + col]
+                                    : static_cast<int64_t>(d.nt) * BN + col;
+        out[row * p.M + m] = sum[j] - cmp[j];
     }
 }
 
@@ -1102,8 +1110,7 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     }
     if (e != cudaSuccess || p.ctas == 0) return e;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    sk_fixup_kernel<<<static_cast<unsigned>(tiles), FIX_THREADS, 0, stream>>>(
-        partial, dst, s.M, s.N, p.mtiles, p.ntiles, p.num_kb, p.iters, p.ctas);
+    sk_fixup_kernel<false><<<static_cast<unsigned>(tiles), FIX_THREADS, 0, stream>>>(partial, p);
     e = cudaGetLastError();
     if (e == cudaSuccess) ++g_kernel_launches;
     return e;
@@ -1115,7 +1122,8 @@ namespace {
 
 struct MmidPlan {
     int64_t nslot, Kp, max_tiles, mtiles;
-    size_t off_count, off_offset, off_ntiles, off_tiles, off_rows, off_ghi, off_glo, total;
+    size_t off_count, off_offset, off_ntiles, off_tiles, off_rows, off_ghi, off_glo, off_part,
+        total;
 };
 
 MmidPlan plan_mmid(const MmidShape &s) {
@@ -1137,6 +1145,7 @@ MmidPlan plan_mmid(const MmidShape &s) {
     t.off_rows = take(sizeof(int) * static_cast<size_t>(t.nslot));
     t.off_ghi = take(4 * static_cast<size_t>(t.nslot) * static_cast<size_t>(t.Kp));
     t.off_glo = take(4 * static_cast<size_t>(t.nslot) * static_cast<size_t>(t.Kp));
+    t.off_part = take(static_cast<size_t>(kSkMaxCtas) * 2 * kSlotBytes);   // stream-K partials
     t.total = o;
     return t;
 }
@@ -1214,12 +1223,28 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     p.grp_rows = rw.rows;
     p.grp_tiles = rw.tiles;
     p.grp_ntiles = rw.ntiles;
-    const dim3 grid(static_cast<unsigned>(t.mtiles * t.max_tiles));
+    // The work list is only known on the device, so the schedule is chosen
+    // here: stream-K (one CTA per SM walking the (tile, k-block) iterations
+    // the device computes from the list's length) unless data-parallel is
+    // forced by the test hook.  Experts' tiles are short in k (K = N of W),
+    // so a persistent CTA that flows from one tile into the next saves most
+    // of each tile's start-up.
+    const int G = std::min(device_sms(), kSkMaxCtas);
+    p.ctas = (g_schedule == 1 || G <= 0) ? 0 : G;
+    p.partial = reinterpret_cast<float *>(ws + t.off_part);
+    const int64_t max_grid = t.mtiles * t.max_tiles;
+    const dim3 grid(static_cast<unsigned>(p.ctas > 0 ? p.ctas : max_grid));
     if (s.w_type == OOP_TYPE_F32)
-        return launch_typed<OOP_TYPE_F32, true>(W, os, mhi, mlo, p, grid, stream);
-    if (s.w_type == OOP_TYPE_BF16)
-        return launch_typed<OOP_TYPE_BF16, true>(W, os, mhi, mlo, p, grid, stream);
-    return cudaErrorInvalidValue;
+        e = launch_typed<OOP_TYPE_F32, true>(W, os, mhi, mlo, p, grid, stream);
+    else if (s.w_type == OOP_TYPE_BF16)
+        e = launch_typed<OOP_TYPE_BF16, true>(W, os, mhi, mlo, p, grid, stream);
+    else
+        return cudaErrorInvalidValue;
+    if (e != cudaSuccess || p.ctas == 0) return e;
+    sk_fixup_kernel<true><<<static_cast<unsigned>(max_grid), FIX_THREADS, 0, stream>>>(p.partial, p);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) ++g_kernel_launches;
+    return e;
 }
 
 }  // namespace oop

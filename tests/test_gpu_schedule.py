@@ -124,3 +124,36 @@ def test_auto_schedule_choice(op):
         sk = -(-(tiles * nkb) // g) + 8
         want_sk = tiles * nkb >= 16 * g and 10 * sk < 9 * dp
         assert got == (3 if want_sk else 2), (m, k, n, got)
+
+
+@pytest.mark.parametrize("wt", [synth.TYPE_F32, synth.TYPE_BF16])
+def test_grouped_mul_mat_id_back_schedules(op, orc, wt):
+    """MUL_MAT_ID_BACK's grouped product: stream-K over the device-side work
+    list (the default: routing, split, tile kernel, fix-up) and data-parallel
+    (three launches) both match the oracle; stream-K repeats bit for bit."""
+    import torch
+    K, N, E, n_used, T = 300, 136, 7, 3, 110
+    W = synth.normal(70, K * N * E, std=0.02).reshape(E, N, K)
+    if wt == synth.TYPE_BF16:
+        W = synth.to_bf16_bits(W)
+    ids = synth.routing_ids(71, E, n_used, T)
+    g = synth.normal(72, N * n_used * T).reshape(T, n_used, N)
+    ref = orc.mul_mat_id_back(W, wt, ids, g, (K, N, E))
+    tW = torch.from_numpy(np.ascontiguousarray(W).view(np.int16) if wt == synth.TYPE_BF16
+                          else np.ascontiguousarray(W)).cuda()
+    tids, tg = torch.from_numpy(ids).cuda(), torch.from_numpy(g).cuda()
+    outs, counts = [], []
+    for sched in (op.SCHEDULE_AUTO, op.SCHEDULE_AUTO, op.SCHEDULE_DATA_PARALLEL):
+        op.set_tc_schedule(sched)
+        try:
+            out = op.mul_mat_id_back(tW, tids, tg, w_type=wt, path=op.PATH_TCGEN05)
+            counts.append(op.last_launch_count())
+            torch.cuda.synchronize()
+        finally:
+            op.set_tc_schedule(op.SCHEDULE_AUTO)
+        assert op.device_status() == 0
+        outs.append(out.cpu().numpy())
+    assert counts == [4, 4, 3]
+    for o, what in zip(outs, ("stream-K", "stream-K again", "data-parallel")):
+        assert_parity(o, ref["f64"], ref["abs"], f"grouped {wt} {what}")
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
