@@ -184,7 +184,10 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst, const
     cudaError_t e;
     switch (chosen) {
     case OOP_PATH_SKINNY:
-        e = launch_skinny(static_cast<const float *>(a), b, dst, s, st);
+        if (skinny_tma_ok(static_cast<const float *>(a), b, s))
+            e = launch_skinny_tma(static_cast<const float *>(a), b, dst, s, status, st);
+        else
+            e = launch_skinny(static_cast<const float *>(a), b, dst, s, st);
         if (e == cudaSuccess) g_kernel_launches = 1;
         break;
     case OOP_PATH_TCGEN05:

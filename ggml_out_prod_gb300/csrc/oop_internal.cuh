@@ -4,6 +4,7 @@
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdint>
 
@@ -49,9 +50,18 @@ __device__ __forceinline__ void record_status(int *status, int code) {
 
 // ---- kernels (each .cu file owns its launcher) ----------------------------
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point, looked up
+// once (nullptr when the driver does not offer it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 // Skinny-N OUT_PROD: f32 src0, N <= 32.
 cudaError_t launch_skinny(const float *a, const float *b, float *dst,
                           const OutProdShape &s, cudaStream_t stream);
+// Its persistent TMA-fed form for large problems (N % 4 == 0, M % 4 == 0,
+// 16-byte aligned a and b, at least two m-tile x slice items per SM).
+bool skinny_tma_ok(const float *a, const float *b, const OutProdShape &s);
+cudaError_t launch_skinny_tma(const float *a, const float *b, float *dst,
+                              const OutProdShape &s, int *status, cudaStream_t stream);
 
 // CUDA-core tiled OUT_PROD, any src0 type.
 cudaError_t launch_dense_simt(const void *a, const float *b, float *dst,

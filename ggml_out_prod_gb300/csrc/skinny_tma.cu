@@ -1,0 +1,292 @@
+// skinny_tma.cu -- OUT_PROD for narrow src1 (N <= 32) on large f32 problems:
+// a persistent, TMA-fed form of the skinny-N kernel.
+//
+// The cost of a rank-r gradient is reading src0 once from HBM.  With many
+// slices (a batch of LoRA gradients, long sequences) the register
+// double-buffered skinny kernel keeps too few bytes in flight to fill HBM
+// (it levels off near 3.6 TB/s).  Here:
+//  * one CTA per SM walks work items (dst slice, m-tile of 32*VW columns) in a
+//    fixed order: item = blockIdx.x + j * gridDim.x;
+//  * a TMA warp streams each item's src0 rows (boxes of 64 k x TM m, zero
+//    filled past M) and the matching rows of src1 (64 k x N words, one bulk
+//    copy) through a ring of shared-memory stages, independently of the
+//    consumers, so several stages (~34 KB each) stay in flight per SM and the
+//    next item's rows arrive while the current one is being reduced;
+//  * eight consumer warps split each stage's 64 k rows (8 each); lane = VW
+//    consecutive m, N*VW fp32 accumulators per thread, b read as broadcast
+//    float4s;
+//  * at the end of an item the warps' partials meet in shared memory in fixed
+//    warp order and one thread per output writes dst: deterministic, one
+//    writer per element, no atomics, no workspace.
+// Waits are bounded like the tensor-core kernel's: running out records
+// OOP_ERR_DEVICE_TIMEOUT, every role stops, the TMA warp drains its copies.
+#include <algorithm>
+
+#include "oop_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace oop {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreads = kConsumers + 32;        // + the TMA warp
+constexpr int kTK = 64;                          // k rows per stage
+constexpr int kRowsPerWarp = kTK / kConsumerWarps;
+constexpr int kMaxStages = 8;
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+struct TmaArgs {
+    const float *b;
+    float *dst;
+    int *status;
+    int64_t M, K, N, ne02, ne12, dps2, dps3;
+    int64_t mtiles, items;      // items = slices * mtiles
+    int kstages;                // ceil(K / kTK)
+};
+
+template <int NP, int VW>
+struct Layout {
+    static constexpr int TM = 32 * VW;
+    static constexpr int A_BYTES = kTK * TM * 4;
+    static constexpr int B_BYTES = kTK * NP * 4;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int RED = kConsumerWarps * NP * TM * 4;
+    // as many stages as fit in ~220 KB next to the reduction buffer
+    static constexpr int STAGES_FIT = (220 * 1024 - RED - 2048) / STAGE;
+    static constexpr int STAGES = STAGES_FIT < kMaxStages ? STAGES_FIT : kMaxStages;
+    static_assert(STAGES >= 2, "ring depth");
+    static constexpr size_t SMEM = size_t(STAGES) * STAGE + RED + 2 * STAGES * 8 + 16 + 1024;
+};
+
+// N == NP here (the launcher takes this kernel only for N % 4 == 0).
+template <int NP, int VW>
+__global__ void __launch_bounds__(kThreads, 1)
+    skinny_tma_kernel(const __grid_constant__ CUtensorMap map_a, const TmaArgs p) {
+    using L = Layout<NP, VW>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *red = reinterpret_cast<float *>(smem + L::STAGES * L::STAGE);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::STAGES * L::STAGE + L::RED);
+    uint64_t *empty = full + L::STAGES;
+    int *abort_flag = reinterpret_cast<int *>(empty + L::STAGES);
+    volatile int *abort = abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], kConsumers);
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    bool timed_out = false;
+
+    if (warp == kConsumerWarps) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            ptx::prefetch_tmap(&map_a);
+            int last_ph[L::STAGES];
+            for (int s = 0; s < L::STAGES; ++s) last_ph[s] = -1;
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int64_t item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
+                const int64_t slice = item / p.mtiles;
+                const int mt = static_cast<int>(item % p.mtiles);
+                const int64_t i2 = slice % p.ne12, i3 = slice / p.ne12;
+                const int64_t arow0 = (i3 / p.dps3 * p.ne02 + i2 / p.dps2) * p.K;
+                const float *bs = p.b + slice * p.K * p.N;
+                for (int ks = 0; ks < p.kstages; ++ks) {
+                    if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1, abort, true, kWaitNs,
+                                                &timed_out)) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t k0 = static_cast<int64_t>(ks) * kTK;
+                    const uint32_t bbytes =
+                        static_cast<uint32_t>(std::min<int64_t>(kTK, p.K - k0) * p.N * 4);
+                    uint8_t *st = smem + s * L::STAGE;
+                    ptx::mbar_arrive_expect_tx(&full[s], L::A_BYTES + bbytes);
+                    ptx::tma_load_2d(st, &map_a, &full[s], mt * L::TM,
+                                     static_cast<int>(arow0 + k0));
+                    ptx::bulk_load(st + L::A_BYTES, bs + k0 * p.N, bbytes, &full[s]);
+                    last_ph[s] = static_cast<int>(ph);
+                    if (++s == L::STAGES) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            // copies in flight must land before the CTA's shared memory is released
+            for (int i = 0; i < L::STAGES; ++i)
+                if (last_ph[i] >= 0)
+                    ptx::mbar_wait_bounded(&full[i], static_cast<uint32_t>(last_ph[i]), abort,
+                                           false, kWaitNs, &timed_out);
+        }
+    } else {
+        // ---------------- consumers ----------------
+        // After a wait runs out the warps keep walking the same items and
+        // stages, without waiting or computing, so that all eight still meet
+        // at every named barrier.
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < p.items; item += gridDim.x) {
+            const int64_t slice = item / p.mtiles;
+            const int mt = static_cast<int>(item % p.mtiles);
+            float acc[NP][VW];
+#pragma unroll
+            for (int n = 0; n < NP; ++n)
+#pragma unroll
+                for (int v = 0; v < VW; ++v) acc[n][v] = 0.f;
+            for (int ks = 0; ks < p.kstages; ++ks) {
+                if (ok) {
+                    const bool got = ptx::mbar_wait_bounded(&full[s], ph, abort, true, kWaitNs,
+                                                            &timed_out);
+                    ok = __all_sync(0xffffffffu, got);
+                }
+                if (ok) {
+                    const float *sa = reinterpret_cast<const float *>(smem + s * L::STAGE);
+                    const float *sb =
+                        reinterpret_cast<const float *>(smem + s * L::STAGE + L::A_BYTES);
+                    const int64_t k0 = static_cast<int64_t>(ks) * kTK;
+#pragma unroll
+                    for (int j = 0; j < kRowsPerWarp; ++j) {
+                        const int row = warp * kRowsPerWarp + j;
+                        if (k0 + row < p.K) {       // rows past K belong to the next slice
+                            float av[VW];
+                            if constexpr (VW == 4) {
+                                const float4 t =
+                                    reinterpret_cast<const float4 *>(sa + row * L::TM)[lane];
+                                av[0] = t.x; av[1] = t.y; av[2] = t.z; av[3] = t.w;
+                            } else {
+                                const float2 t =
+                                    reinterpret_cast<const float2 *>(sa + row * L::TM)[lane];
+                                av[0] = t.x; av[1] = t.y;
+                            }
+                            const float *brow = sb + row * NP;
+#pragma unroll
+                            for (int n4 = 0; n4 < NP; n4 += 4) {
+                                const float4 bv = *reinterpret_cast<const float4 *>(brow + n4);
+#pragma unroll
+                                for (int v = 0; v < VW; ++v) {
+                                    acc[n4 + 0][v] = fmaf(av[v], bv.x, acc[n4 + 0][v]);
+                                    acc[n4 + 1][v] = fmaf(av[v], bv.y, acc[n4 + 1][v]);
+                                    acc[n4 + 2][v] = fmaf(av[v], bv.z, acc[n4 + 2][v]);
+                                    acc[n4 + 3][v] = fmaf(av[v], bv.w, acc[n4 + 3][v]);
+                                }
+                            }
+                        }
+                    }
+                    ptx::mbar_arrive(&empty[s]);
+                }
+                if (++s == L::STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            // ---- the warps' partials meet in shared memory (fixed warp order) ----
+#pragma unroll
+            for (int n = 0; n < NP; ++n)
+#pragma unroll
+                for (int v = 0; v < VW; ++v)
+                    red[(warp * NP + n) * L::TM + lane * VW + v] = acc[n][v];
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+            if (ok) {
+                float *dst = p.dst + slice * p.N * p.M;
+                for (int o = threadIdx.x; o < NP * L::TM; o += kConsumers) {
+                    const int n = o / L::TM, mm = o % L::TM;
+                    float sum = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w)
+                        sum += red[(w * NP + n) * L::TM + mm];
+                    const int64_t m = static_cast<int64_t>(mt) * L::TM + mm;
+                    if (m < p.M) dst[static_cast<int64_t>(n) * p.M + m] = sum;
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+        }
+    }
+    if (timed_out) record_status(p.status, OOP_ERR_DEVICE_TIMEOUT);
+}
+
+int device_sm_count() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return v;
+}
+
+template <int NP, int VW>
+cudaError_t launch_tma(const float *a, const float *b, float *dst, const OutProdShape &s,
+                       int *status, int sms, cudaStream_t stream) {
+    using L = Layout<NP, VW>;
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const int64_t rows = s.K * s.ne02 * s.ne03;
+    CUtensorMap map;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.M), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.M * 4)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(L::TM), kTK};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(a), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    TmaArgs p = {};
+    p.b = b;
+    p.dst = dst;
+    p.status = status;
+    p.M = s.M;
+    p.K = s.K;
+    p.N = s.N;
+    p.ne02 = s.ne02;
+    p.ne12 = s.ne12;
+    p.dps2 = s.dps2;
+    p.dps3 = s.dps3;
+    p.mtiles = (s.M + L::TM - 1) / L::TM;
+    p.items = p.mtiles * s.ne12 * s.ne13;
+    p.kstages = static_cast<int>((s.K + kTK - 1) / kTK);
+    auto kern = skinny_tma_kernel<NP, VW>;
+    static_assert(L::SMEM <= 232448, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L::SMEM));
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::min<int64_t>(p.items, sms);
+    kern<<<static_cast<unsigned>(grid), kThreads, L::SMEM, stream>>>(map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool skinny_tma_ok(const float *a, const float *b, const OutProdShape &s) {
+    const int sms = device_sm_count();
+    const int64_t tm = s.N <= 16 ? 128 : 64;
+    const int64_t items = (s.M + tm - 1) / tm * s.ne12 * s.ne13;
+    return sms > 0 && s.N % 4 == 0 && s.M % 4 == 0 && reinterpret_cast<uintptr_t>(a) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(b) % 16 == 0 && s.K * s.ne02 * s.ne03 < (1LL << 31) &&
+           s.K < (1LL << 31) && items >= 2LL * sms;
+}
+
+cudaError_t launch_skinny_tma(const float *a, const float *b, float *dst, const OutProdShape &s,
+                              int *status, cudaStream_t stream) {
+    const int sms = device_sm_count();
+    switch (s.N) {
+    case 4: return launch_tma<4, 4>(a, b, dst, s, status, sms, stream);
+    case 8: return launch_tma<8, 4>(a, b, dst, s, status, sms, stream);
+    case 12: return launch_tma<12, 4>(a, b, dst, s, status, sms, stream);
+    case 16: return launch_tma<16, 4>(a, b, dst, s, status, sms, stream);
+    case 20: return launch_tma<20, 2>(a, b, dst, s, status, sms, stream);
+    case 24: return launch_tma<24, 2>(a, b, dst, s, status, sms, stream);
+    case 28: return launch_tma<28, 2>(a, b, dst, s, status, sms, stream);
+    case 32: return launch_tma<32, 2>(a, b, dst, s, status, sms, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace oop
