@@ -292,17 +292,27 @@ __device__ __forceinline__ void staged_half(const uint8_t *slot, int r, int off0
         const uint8_t *blk = rows + off0 + (r >> 5) * Raw::BLOCK;
         const float dl = half_bits_to_float(
             *reinterpret_cast<const uint16_t *>(blk + (lane & (KH - 1)) * Raw::ROW_BYTES));
+        // d*v two k rows at a time in packed f32x2 arithmetic, exactly: with
+        // f = 1.5*2^23 + v (exact), d*f - d*1.5*2^23 is one fused multiply-add
+        // whose single rounding is exact because d*v fits in fp32
+        const uint64_t big2 = ptx::pack2(-12582912.0f, -12582912.0f);
 #pragma unroll
-        for (int j = 0; j < KH; ++j) {
-            const float d = __shfl_sync(0xffffffffu, dl, j);
-            int v;
-            if constexpr (TYPE == OOP_TYPE_Q8_0) {
-                v = static_cast<int8_t>(blk[j * Raw::ROW_BYTES + 2 + lane]);
-            } else {
-                const uint8_t byte = blk[j * Raw::ROW_BYTES + 2 + (lane & 15)];
-                v = (lane < 16 ? (byte & 0x0f) : (byte >> 4)) - 8;
+        for (int j = 0; j < KH; j += 2) {
+            int v[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if constexpr (TYPE == OOP_TYPE_Q8_0) {
+                    v[e] = static_cast<int8_t>(blk[(j + e) * Raw::ROW_BYTES + 2 + lane]);
+                } else {
+                    const uint8_t byte = blk[(j + e) * Raw::ROW_BYTES + 2 + (lane & 15)];
+                    v[e] = (lane < 16 ? (byte & 0x0f) : (byte >> 4)) - 8;
+                }
             }
-            x[j] = ptx::scaled_small_int(d, v);
+            const uint64_t d2 = ptx::pack2(__shfl_sync(0xffffffffu, dl, j),
+                                           __shfl_sync(0xffffffffu, dl, j + 1));
+            const uint64_t f2 = ptx::pack2(__int_as_float(0x4B400000 + v[0]),
+                                           __int_as_float(0x4B400000 + v[1]));
+            ptx::unpack2(ptx::fma2(d2, f2, ptx::mul2(d2, big2)), x[j], x[j + 1]);
         }
     }
 }
@@ -571,14 +581,22 @@ __global__ void __maxnreg__(MAX_REGS)
             ptx::mbar_arrive(&bars->rempty[rs]);
             uint32_t hi[KH], lo[KH];
 #pragma unroll
-            for (int e = 0; e < KH; ++e) {
+            for (int e = 0; e < KH; e += 2) {
+                hi[e] = ptx::tf32_round_bits(__float_as_uint(x[e]));
+                hi[e + 1] = ptx::tf32_round_bits(__float_as_uint(x[e + 1]));
+                // x - hi is exact in fp32 (two elements per instruction)
+                float r0, r1;
+                ptx::unpack2(ptx::sub2(ptx::pack2(x[e], x[e + 1]),
+                                       ptx::pack2(__uint_as_float(hi[e]), __uint_as_float(hi[e + 1]))),
+                             r0, r1);
                 if constexpr (TYPE == OOP_TYPE_F32) {
-                    ptx::split_tf32(x[e], hi[e], lo[e]);
+                    lo[e] = ptx::tf32_round_bits(__float_as_uint(r0));
+                    lo[e + 1] = ptx::tf32_round_bits(__float_as_uint(r1));
                 } else {
                     // d*q has at most 18 significant bits: x - hi is already
                     // a TF32 value, no second rounding needed
-                    hi[e] = ptx::tf32_round_bits(__float_as_uint(x[e]));
-                    lo[e] = __float_as_uint(x[e] - __uint_as_float(hi[e]));
+                    lo[e] = __float_as_uint(r0);
+                    lo[e + 1] = __float_as_uint(r1);
                 }
             }
             // A stage g % A_STAGES is free once the MMAs of g - A_STAGES completed

@@ -334,6 +334,18 @@ __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
     return r;
 }
 
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // Two floats rounded to bfloat16 (nearest even) in one 32-bit register, the
 // first in the low half; and back.  bfloat16 keeps fp32's exponent range.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -344,13 +356,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ uint64_t unpack_bf16x2(uint32_t v) {
     return pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-}
-
-// d * v for a small integer v, exactly: with f = 1.5 * 2^23 + v (exact),
-// d * f - d * 1.5 * 2^23 is formed in one fused multiply-add, whose single
-// rounding is exact because d * v fits in fp32 (d has 11 significant bits).
-__device__ __forceinline__ float scaled_small_int(float d, int v) {
-    return fmaf(d, __int_as_float(0x4B400000 + v), d * -12582912.0f);
 }
 
 }  // namespace ptx
