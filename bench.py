@@ -47,7 +47,7 @@ NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # headline workload, from the ncu capture summarised in
 # profiles/tc_out_prod_q8_m5120_k5120_n1024.md; None while that capture does
 # not match the kernel in this tree.
-TC_TRAFFIC_BYTES = None
+TC_TRAFFIC_BYTES = 87_931_648
 
 
 def _peaks():
