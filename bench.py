@@ -266,18 +266,28 @@ def gpu_arm(args):
     ms_step_max = _barrier_max(torch, ms_step, ws)
     value = ws * flops / (ms_step_max * 1e-3) / 1e12
 
-    # ---- e2e: host buffers through the public API -------------------------
+    # ---- e2e: host buffers through the C ABI's host entry ------------------
+    # (oop_out_prod_host: copies in, product, copy of dst out, one call; the
+    # timed region ends when dst is back in host memory)
     a_host = torch.from_numpy(a_np).pin_memory()
     b_host = torch.from_numpy(b_np).pin_memory()
+    dst_host = torch.empty((1, 1, DENSE_N, DENSE_M), dtype=torch.float32, pin_memory=True)
+    nbuf = op.oop_out_prod_host_buffer_size(op.TYPE_Q8_0, ne_a, (DENSE_N, DENSE_K, 1, 1))
+    dev_buf = torch.empty(nbuf, dtype=torch.uint8, device=device)
+
+    def e2e_call():
+        op.out_prod_host(a_host, b_host, a_type=op.TYPE_Q8_0, ne_a=ne_a, out=dst_host,
+                         device_buffer=dev_buf)
+
     for _ in range(max(1, args.warmup)):
-        op.out_prod_host(a_host, b_host, a_type=op.TYPE_Q8_0, device=device)
+        e2e_call()
     torch.cuda.synchronize()
     e2e_t = []
     for _ in range(args.steps):
         timer.flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        op.out_prod_host(a_host, b_host, a_type=op.TYPE_Q8_0, device=device)
+        e2e_call()
         e2e_t.append(time.perf_counter() - t0)
     e2e_s = _barrier_max(torch, statistics.mean(e2e_t), ws)
 

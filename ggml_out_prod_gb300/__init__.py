@@ -64,7 +64,7 @@ EXPORTS = (
     "oop_device_status", "oop_status_string", "oop_version", "oop_debug_inject_timeout",
     "oop_last_cuda_error", "oop_out_prod_noalloc", "oop_out_prod_noalloc_scratch_bytes",
     "oop_profile_main_kernel", "oop_out_prod_workspace_min_size", "oop_debug_set_tc_schedule",
-    "oop_last_launch_count",
+    "oop_last_launch_count", "oop_out_prod_host", "oop_out_prod_host_buffer_size",
 )
 
 
@@ -135,6 +135,11 @@ def lib():
             L.oop_debug_set_tc_schedule.argtypes = [ctypes.c_int]
             L.oop_last_launch_count.restype = ctypes.c_int
             L.oop_last_launch_count.argtypes = []
+            L.oop_out_prod_host_buffer_size.restype = ctypes.c_size_t
+            L.oop_out_prod_host_buffer_size.argtypes = [ctypes.c_int, _i64p, _i64p]
+            L.oop_out_prod_host.restype = ctypes.c_int
+            L.oop_out_prod_host.argtypes = [_vp, ctypes.c_int, _vp, _vp, _i64p, _i64p, _i64p,
+                                            _vp, ctypes.c_size_t, _vp]
             _lib = L
     return _lib
 
@@ -166,6 +171,16 @@ def oop_debug_set_tc_schedule(mode) -> int:
 
 def oop_last_launch_count() -> int:
     return int(lib().oop_last_launch_count())
+
+
+def oop_out_prod_host_buffer_size(a_type, ne_a, ne_b) -> int:
+    return int(lib().oop_out_prod_host_buffer_size(int(a_type), _ne(ne_a), _ne(ne_b)))
+
+
+def oop_out_prod_host(a, a_type, b, dst, ne_a, ne_b, ne_dst, device_buffer, device_bytes,
+                      stream) -> int:
+    return int(lib().oop_out_prod_host(a, int(a_type), b, dst, _ne(ne_a), _ne(ne_b), _ne(ne_dst),
+                                       device_buffer, int(device_bytes), stream))
 
 
 def oop_out_prod(a, a_type, b, dst, ne_a, ne_b, ne_dst, workspace, workspace_bytes, stream,
@@ -331,14 +346,37 @@ def last_launch_count() -> int:
     return oop_last_launch_count()
 
 
-def out_prod_host(a_host, b_host, a_type=None, device="cuda", path=PATH_AUTO):
-    """OUT_PROD from host tensors: copies in (pinned memory, non-blocking),
-    runs on the device, copies the result back; returns a host tensor."""
+def out_prod_host(a_host, b_host, a_type=None, ne_a=None, out=None, device_buffer=None,
+                  stream=None):
+    """OUT_PROD from host tensors through the C ABI's host entry: the copies
+    in, the product and the copy of dst out are enqueued by one call (two
+    column chunks pipelined when the shape allows), then the stream is
+    synchronised.  a_host / b_host: CPU tensors (pinned memory makes the
+    copies asynchronous); ``out``: a CPU float32 tensor of dst's shape
+    (allocated pinned when None); ``device_buffer``: a CUDA uint8 tensor of at
+    least oop_out_prod_host_buffer_size bytes (allocated when None)."""
     torch = _torch()
-    a = a_host.to(device, non_blocking=True)
-    b = b_host.to(device, non_blocking=True)
-    d = out_prod(a, b, a_type=a_type, path=path)
-    out = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
-    out.copy_(d, non_blocking=True)
-    torch.cuda.current_stream().synchronize()
+    if a_type is None:
+        a_type = TYPE_F32
+    for t, n in ((a_host, "a_host"), (b_host, "b_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    if b_host.dtype != torch.float32:
+        raise ValueError("b_host must be float32")
+    if ne_a is None:
+        ne_a = ne_of(a_host, a_type)
+    ne_b = ne_of(b_host)
+    ne_dst = (ne_a[0], ne_b[0], ne_b[2], ne_b[3])
+    if out is None:
+        out = torch.empty((ne_dst[3], ne_dst[2], ne_dst[1], ne_dst[0]), dtype=torch.float32,
+                          pin_memory=True)
+    nbuf = oop_out_prod_host_buffer_size(a_type, ne_a, ne_b)
+    if device_buffer is None:
+        device_buffer = torch.empty(max(nbuf, 1), dtype=torch.uint8, device="cuda")
+    st = _stream_ptr(stream)
+    rc = oop_out_prod_host(_ptr(a_host), a_type, _ptr(b_host), _ptr(out), ne_a, ne_b, ne_dst,
+                           _ptr(device_buffer), device_buffer.numel(), st)
+    if rc != OK:
+        raise OopError(rc, "oop_out_prod_host")
+    (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return out

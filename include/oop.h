@@ -118,6 +118,34 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst,
                     size_t workspace_bytes, void *stream, int path);
 
 /*
+ * OUT_PROD from HOST buffers (no counterpart on the pages; the benchmark's
+ * end-to-end figure goes through it): enqueues on `stream` the copies of a
+ * and b into `device_buffer`, the product, and the copy of dst back into
+ * dst_host; returns once everything is enqueued.  Synchronise `stream`
+ * before reading dst_host.  Pinned (page-locked) host memory makes the copies
+ * asynchronous; pageable memory works but blocks the host in the copies.
+ *
+ * device_buffer: device memory of at least
+ * oop_out_prod_host_buffer_size(...) bytes (0 for an invalid shape),
+ * 256-byte aligned, holding the device copies of a, b and dst and the
+ * workspace.  For a single slice wide enough, the call pipelines two column
+ * chunks of dst: the second chunk's b columns are copied in while the first
+ * chunk is computed, the first chunk of dst is copied out while the second is
+ * computed; those copies run on a copy stream the library creates once per
+ * device and are ordered against `stream` by events, so the call returns with
+ * `stream` waiting for its last copy.  Calls on one device are enqueued one
+ * at a time (a library lock).  Errors: as oop_out_prod; OOP_ERR_WORKSPACE for
+ * a missing, small or misaligned device_buffer.
+ */
+size_t oop_out_prod_host_buffer_size(int a_type, const int64_t ne_a[4],
+                                     const int64_t ne_b[4]);
+
+int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float *dst_host,
+                      const int64_t ne_a[4], const int64_t ne_b[4],
+                      const int64_t ne_dst[4], void *device_buffer,
+                      size_t device_bytes, void *stream);
+
+/*
  * OUT_PROD without any device allocation (no counterpart on the pages: the
  * Metal op takes its scratch from the ggml graph).  For callers that cannot
  * allocate device memory or hand the library a scratch buffer -- code inside

@@ -249,3 +249,40 @@ def test_host_checks_reject(op):
     with pytest.raises(op.OopError) as e:
         op.out_prod(a, torch.ones((1, 3, 8, 40), device="cuda"), path=op.PATH_SKINNY)
     assert e.value.status == op.ERR_PATH
+
+
+# ---------------------------------------------------------------------------
+# the host entry (host buffers in and out, one call)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("a_type,ne_a,ne_b", [
+    (Q8, (640, 1000, 1, 1), (300, 1000, 1, 1)),     # pipelined: two column chunks
+    (F32, (200, 300, 2, 1), (70, 300, 4, 3)),       # several slices: one pass
+    (F32, (256, 512, 1, 1), (8, 512, 1, 1)),        # skinny-N
+    (Q4, (384, 700, 1, 1), (200, 700, 1, 1)),       # pipelined, ragged chunk
+])
+def test_host_entry_matches_oracle(op, orc, a_type, ne_a, ne_b):
+    import torch
+    a = synth.make_a(a_type, ne_a, 90, std=0.02 if a_type != F32 else 1.0)
+    b = synth.make_b(ne_b, 91, std=1e3, outliers=True)
+    ref = orc.out_prod(a, a_type, b, ne_a, ne_b)
+    out = op.out_prod_host(torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory(),
+                           a_type=a_type, ne_a=ne_a)
+    assert op.device_status() == 0
+    assert_parity(out.numpy(), ref["f64"], ref["abs"], f"host entry {a_type} {ne_a}")
+
+
+def test_host_entry_rejects(op):
+    import torch
+    ne_a, ne_b = (640, 1000, 1, 1), (300, 1000, 1, 1)
+    need = op.oop_out_prod_host_buffer_size(Q8, ne_a, ne_b)
+    assert need > 0
+    a = torch.zeros(1000 * 640 // 32 * 34, dtype=torch.uint8)
+    b = torch.zeros((1000, 300), dtype=torch.float32)
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(op.OopError) as e:
+        op.out_prod_host(a, b, a_type=Q8, ne_a=ne_a, device_buffer=small)
+    assert e.value.status == op.ERR_WORKSPACE
+    with pytest.raises(op.OopError) as e:                # K mismatch
+        op.out_prod_host(a, torch.zeros((999, 300), dtype=torch.float32), a_type=Q8, ne_a=ne_a)
+    assert e.value.status == op.ERR_SHAPE
