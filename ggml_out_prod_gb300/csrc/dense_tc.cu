@@ -170,6 +170,9 @@ struct TcParams {
     int64_t iters;
     int ctas;
     float *partial;
+    // persistent != 0 (with ctas == 0): CTA c takes whole tiles c, c + G, ...
+    // (G = grid size) of the tile count, which grouped mode reads on the device
+    int persistent;
     // grouped mode (MUL_MAT_ID_BACK): slices are experts, src1 rows are the
     // routed slots sorted by expert, dst rows are scattered back to slots
     const int *grp_count;         // [E] slots routed to each expert
@@ -197,15 +200,19 @@ struct Tile {
 template <bool GROUPED>
 __device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
     Tile d;
-    d.mt = static_cast<int>(t % p.mtiles);
-    const int64_t rest = t / p.mtiles;
     if constexpr (GROUPED) {
-        const int packed = p.grp_tiles[rest];
+        // work-list entries innermost: an expert's n-tiles of one m-tile are
+        // neighbours, so the second one finds that m-tile of W in L2
+        const int64_t entries = *p.grp_ntiles;
+        d.mt = static_cast<int>(t / entries);
+        const int packed = p.grp_tiles[t % entries];
         d.slice = packed >> 16;
         d.nt = packed & 0xFFFF;
         d.ncols = p.grp_count[d.slice];
         d.brow0 = p.grp_offset[d.slice] + static_cast<int64_t>(d.nt) * BN;
     } else {
+        d.mt = static_cast<int>(t % p.mtiles);
+        const int64_t rest = t / p.mtiles;
         d.nt = static_cast<int>(rest % p.ntiles);
         d.slice = rest / p.ntiles;
         d.ncols = p.N;
@@ -216,21 +223,29 @@ __device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
     return d;
 }
 
+// A CTA's share of the iterations: it0 .. it1 - 1, starting at k-block kb0
+// of tile tile0; after a tile's last k-block the walk moves `stride` tiles on
+// (1 for a contiguous range, the grid size for whole tiles taken round-robin).
+struct Span {
+    int64_t it0, it1, tile0, stride;
+    int kb0;
+};
+
 // Walks a CTA's iterations in order; every role keeps its own copy.
 template <bool GROUPED>
 struct Walk {
-    int64_t it, end, tile;
+    int64_t it, end, tile, stride;
     int kb;
     Tile t;
-    __device__ __forceinline__ Walk(const TcParams &p, int64_t it0, int64_t it1)
-        : it(it0), end(it1), tile(it0 / p.num_kb), kb(static_cast<int>(it0 % p.num_kb)) {
+    __device__ __forceinline__ Walk(const TcParams &p, const Span &sp)
+        : it(sp.it0), end(sp.it1), tile(sp.tile0), stride(sp.stride), kb(sp.kb0) {
         if (it < end) t = decode_tile<GROUPED>(p, tile);
     }
     __device__ __forceinline__ void next(const TcParams &p) {
         ++it;
         if (++kb == p.num_kb) {
             kb = 0;
-            ++tile;
+            tile += stride;
             if (it < end) t = decode_tile<GROUPED>(p, tile);
         }
     }
@@ -344,19 +359,29 @@ __global__ void __maxnreg__(MAX_REGS)
 
     // this CTA's iterations [it0, it1)
     int64_t it0, it1;
+    Span span = {};
     if (p.ctas > 0) {
         // grouped: the tile count is known on the device only
         const int64_t iters =
             GROUPED ? static_cast<int64_t>(p.mtiles) * *p.grp_ntiles * p.num_kb : p.iters;
         it0 = sk_begin(iters, p.ctas, blockIdx.x);
         it1 = sk_begin(iters, p.ctas, blockIdx.x + 1);
+        span = {it0, it1, it0 / p.num_kb, 1, static_cast<int>(it0 % p.num_kb)};
+    } else if (p.persistent) {
+        const int64_t tiles =
+            GROUPED ? static_cast<int64_t>(p.mtiles) * *p.grp_ntiles : p.iters / p.num_kb;
+        const int64_t mine = tiles > blockIdx.x ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+        it0 = 0;
+        it1 = mine * p.num_kb;
+        span = {it0, it1, static_cast<int64_t>(blockIdx.x), static_cast<int64_t>(gridDim.x), 0};
     } else {
         const int64_t t = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
         if constexpr (GROUPED) {
-            if (t / p.mtiles >= *p.grp_ntiles) return;   // whole CTA: no work left
+            if (t >= static_cast<int64_t>(p.mtiles) * *p.grp_ntiles) return;   // no work left
         }
         it0 = t * p.num_kb;
         it1 = it0 + p.num_kb;
+        span = {it0, it1, t, 1, 0};
     }
     if (it0 >= it1) return;
 
@@ -399,7 +424,7 @@ __global__ void __maxnreg__(MAX_REGS)
             Ring<Raw::RSTAGES> rr;
             Ring<B_STAGES> bb;
             int g = 0;
-            for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), rr.next(), bb.next(), ++g) {
+            for (Walk<GROUPED> w(p, span); w.it < w.end; w.next(p), rr.next(), bb.next(), ++g) {
                 const Tile &t = w.t;
                 // ring slot free (producers done with g - RSTAGES), B stage
                 // free (MMAs of g - B_STAGES completed)
@@ -456,7 +481,7 @@ __global__ void __maxnreg__(MAX_REGS)
         // the MMAs of g are being issued; the full wait runs only when such
         // an early test came back negative.
         bool early_a = false, early_e = false;
-        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), aa.next(), bb.next(), ++g) {
+        for (Walk<GROUPED> w(p, span); w.it < w.end; w.next(p), aa.next(), bb.next(), ++g) {
             const bool seg_first = g == 0 || w.kb == 0;
             if (seg_first) {
                 ++seg;
@@ -471,10 +496,14 @@ __global__ void __maxnreg__(MAX_REGS)
             // D1 buffer drained by the fold; D2 read at the previous segment's
             // end; this block's A stage written (its producers also saw its B
             // stage land)
+            // D2 is first written at a segment's second block (its first
+            // block keeps every product in the fresh D1 chunk), so the wait for
+            // the fold to have read the previous segment's D2 sits there
+            const int seg_pos = w.kb - seg_kb0;
             if ((in_chunk == 0 && !__all_sync(0xffffffffu, early_e) &&
                  !warp_wait(&bars->acce[buf], (static_cast<uint32_t>(q >> 1) & 1) ^ 1, abort,
                             &timed_out)) ||
-                (seg_first && seg > 0 &&
+                (seg_pos == 1 && seg > 0 &&
                  !warp_wait(&bars->d2free, static_cast<uint32_t>(seg - 1) & 1, abort,
                             &timed_out)) ||
                 (!__all_sync(0xffffffffu, early_a) &&
@@ -498,20 +527,23 @@ __global__ void __maxnreg__(MAX_REGS)
             const uint64_t dlo = dhi + (B_IMG >> 4);
             if (ptx::elect_one()) {
                 if constexpr (HAS_ALO) {
-                    // cross terms a_lo*b_hi + a_hi*b_lo into D2 (over the whole
-                    // segment), the big term a_hi*b_hi into D1 (per chunk)
-                    ptx::mma_block_3xtf32(d1, d2, ahi, alo, dhi, dlo, idesc, in_chunk == 0,
-                                          seg_first);
+                    if (seg_pos == 0)   // every product into the fresh D1, small ones first
+                        ptx::mma_block_3xtf32_one(d1, ahi, alo, dhi, dlo, idesc);
+                    else                // cross terms into D2, the big term into D1
+                        ptx::mma_block_3xtf32(d1, d2, ahi, alo, dhi, dlo, idesc, in_chunk == 0,
+                                              seg_pos == 1);
                 } else {
                     // bf16 src0: a_lo is zero, one cross term
 #pragma unroll
                     for (int kk = 0; kk < BK / 8; ++kk) {
                         const uint64_t off = kk * 2;    // 8 tf32 = 32 bytes along k
-                        ptx::mma_tf32_ta(d2, ahi + kk * 8, dlo + off, idesc,
-                                         (seg_first && kk == 0) ? 0u : 1u);
-                        ptx::mma_tf32_ta(d1, ahi + kk * 8, dhi + off, idesc,
-                                         (in_chunk == 0 && kk == 0) ? 0u : 1u);
+                        ptx::mma_tf32_ta(seg_pos == 0 ? d1 : d2, ahi + kk * 8, dlo + off, idesc,
+                                         (seg_pos <= 1 && kk == 0) ? 0u : 1u);
                     }
+#pragma unroll
+                    for (int kk = 0; kk < BK / 8; ++kk)
+                        ptx::mma_tf32_ta(d1, ahi + kk * 8, dhi + kk * 2, idesc,
+                                         (in_chunk == 0 && kk == 0 && seg_pos != 0) ? 0u : 1u);
                 }
                 ptx::mma_commit(&bars->bempty[s]);
                 if (chunk_last) ptx::mma_commit(&bars->accf[buf]);
@@ -535,7 +567,7 @@ __global__ void __maxnreg__(MAX_REGS)
         Ring<Raw::RSTAGES> rr;
         Ring<A_STAGES> aa;
         Ring<B_STAGES> eb;                               // bempty of iteration g - A_STAGES
-        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), rr.next(), aa.next(), ++g) {
+        for (Walk<GROUPED> w(p, span); w.it < w.end; w.next(p), rr.next(), aa.next(), ++g) {
             const Tile &t = w.t;
             const int64_t m = static_cast<int64_t>(t.mt) * BM + r;
             const bool mok = m < p.M;
@@ -626,7 +658,7 @@ __global__ void __maxnreg__(MAX_REGS)
         uint32_t cmp[FOLD_COLS / 2];
         int seg_kb0 = 0;
         int g = 0, q = -1;
-        for (Walk<GROUPED> w(p, it0, it1); w.it < w.end; w.next(p), ++g) {
+        for (Walk<GROUPED> w(p, span); w.it < w.end; w.next(p), ++g) {
             if (g == 0 || w.kb == 0) seg_kb0 = w.kb;
             const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
             const bool last = w.kb + 1 == p.num_kb || w.it + 1 == w.end;   // segment ends
@@ -688,7 +720,12 @@ __global__ void __maxnreg__(MAX_REGS)
                 if (last) {
                     uint32_t (&dv)[16] = sv;                // D2, the cross terms
                     __syncwarp();
-                    ptx::tmem_ld16_wait(tmem + lane_off + COL_D2 + col, dv);
+                    if (w.kb > seg_kb0) {
+                        ptx::tmem_ld16_wait(tmem + lane_off + COL_D2 + col, dv);
+                    } else {                                // a one-block segment: none
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) dv[j] = 0;
+                    }
                     if (m < p.M) {
 #pragma unroll
                         for (int j = 0; j < 16; j += 2) {
@@ -862,16 +899,17 @@ __global__ void __launch_bounds__(1024) mmid_route_kernel(const int32_t *__restr
     }
 }
 
-// Sorted slot j: g[rows[j]][0..R) -> ghi, glo [j][Kp], TF32 split, zero
-// padding for r in [R, Kp).  Rows past the routed total are left alone: the
-// tile kernel never stores the columns they feed.
+// Sorted slots j (kSplitSlots per CTA): g[rows[j]][0..R) -> ghi, glo [j][Kp],
+// TF32 split, zero padding for r in [R, Kp).  Rows past the routed total are
+// left alone: the tile kernel never stores the columns they feed.
+constexpr int kSplitSlots = 8;
+
 __global__ void __launch_bounds__(256) mmid_gsplit_kernel(const float *__restrict__ g,
                                                           const int *__restrict__ rows,
                                                           const int *__restrict__ count, int E,
                                                           uint32_t *__restrict__ ghi,
                                                           uint32_t *__restrict__ glo, int64_t R,
                                                           int64_t Kp) {
-    const int64_t j = blockIdx.x;
     __shared__ int total;
     if (threadIdx.x == 0) {
         int t = 0;
@@ -879,13 +917,16 @@ __global__ void __launch_bounds__(256) mmid_gsplit_kernel(const float *__restric
         total = t;
     }
     __syncthreads();
-    if (j >= total) return;
-    const float *src = g + static_cast<int64_t>(rows[j]) * R;
-    for (int64_t r = threadIdx.x; r < Kp; r += blockDim.x) {
-        uint32_t h = 0, l = 0;
-        if (r < R) ptx::split_tf32(__ldg(src + r), h, l);
-        ghi[j * Kp + r] = h;
-        glo[j * Kp + r] = l;
+    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kSplitSlots;
+    const int64_t j1 = min(static_cast<int64_t>(total), j0 + kSplitSlots);
+    for (int64_t j = j0; j < j1; ++j) {
+        const float *src = g + static_cast<int64_t>(rows[j]) * R;
+        for (int64_t r = threadIdx.x; r < Kp; r += blockDim.x) {
+            uint32_t h = 0, l = 0;
+            if (r < R) ptx::split_tf32(__ldg(src + r), h, l);
+            ghi[j * Kp + r] = h;
+            glo[j * Kp + r] = l;
+        }
     }
 }
 
@@ -1198,7 +1239,8 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++g_kernel_launches;
-    mmid_gsplit_kernel<<<static_cast<unsigned>(t.nslot), 256, 0, stream>>>(
+    mmid_gsplit_kernel<<<static_cast<unsigned>((t.nslot + kSplitSlots - 1) / kSplitSlots), 256, 0,
+                         stream>>>(
         g, rw.rows, rw.count, static_cast<int>(s.E), ghi, glo, s.N, t.Kp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1250,10 +1292,11 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     // so a persistent CTA that flows from one tile into the next saves most
     // of each tile's start-up.
     const int G = std::min(device_sms(), kSkMaxCtas);
-    p.ctas = (g_schedule == 1 || G <= 0) ? 0 : G;
+    p.ctas = (g_schedule == 2 && G > 0) ? G : 0;
+    p.persistent = (g_schedule == 0 && G > 0) ? 1 : 0;
     p.partial = reinterpret_cast<float *>(ws + t.off_part);
     const int64_t max_grid = t.mtiles * t.max_tiles;
-    const dim3 grid(static_cast<unsigned>(p.ctas > 0 ? p.ctas : max_grid));
+    const dim3 grid(static_cast<unsigned>(p.ctas > 0 || p.persistent ? G : max_grid));
     if (s.w_type == OOP_TYPE_F32)
         e = launch_typed<OOP_TYPE_F32, true>(W, os, mhi, mlo, p, grid, stream);
     else if (s.w_type == OOP_TYPE_BF16)

@@ -209,6 +209,37 @@ __device__ __forceinline__ void mma_block_3xtf32(uint32_t d1, uint32_t d2, uint3
         : "memory");
 }
 
+// The same 32-k block with every product in d (restarted): the eight small
+// cross terms first, while d is still ~2^-11 of its final size, then the four
+// big terms.
+__device__ __forceinline__ void mma_block_3xtf32_one(uint32_t d, uint32_t ahi, uint32_t alo,
+                                                     uint64_t bhi, uint64_t blo, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t"
+        "setp.ne.b32 pf, 0, 0;\n\t"
+        "setp.eq.b32 pt, 0, 0;\n\t"
+        ".reg .b32 a0, a1, a2, a3, l0, l1, l2, l3;\n\t"
+        ".reg .b64 h0, h1, h2, h3, o0, o1, o2, o3;\n\t"
+        "mov.b32 a0, %1;\n\tadd.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+        "mov.b32 l0, %2;\n\tadd.u32 l1, %2, 8;\n\tadd.u32 l2, %2, 16;\n\tadd.u32 l3, %2, 24;\n\t"
+        "mov.b64 h0, %3;\n\tadd.u64 h1, %3, 2;\n\tadd.u64 h2, %3, 4;\n\tadd.u64 h3, %3, 6;\n\t"
+        "mov.b64 o0, %4;\n\tadd.u64 o1, %4, 2;\n\tadd.u64 o2, %4, 4;\n\tadd.u64 o3, %4, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [l0], h0, %5, pf;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a0], o0, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [l1], h1, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a1], o1, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [l2], h2, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a2], o2, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [l3], h3, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a3], o3, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a0], h0, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a1], h1, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a2], h2, %5, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a3], h3, %5, pt;\n\t}" ::"r"(d),
+        "r"(ahi), "r"(alo), "l"(bhi), "l"(blo), "r"(idesc)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 op this thread issued completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(

@@ -245,9 +245,10 @@ int oop_debug_inject_timeout(int enable);
  * run mostly empty and the workspace holds the partials), 1 = always
  * data-parallel (one 128 x 96 dst tile per CTA), 2 = always stream-K (one
  * CTA per SM sharing the tile x k-block iterations, then a fix-up kernel),
- * when the workspace allows.  MUL_MAT_ID_BACK's grouped product uses
- * stream-K for modes 0 and 2 (its tile count is known on the device only)
- * and data-parallel for mode 1.  Results agree to rounding order either way.
+ * when the workspace allows.  MUL_MAT_ID_BACK's grouped product (its tile
+ * count is known on the device only) runs one CTA per SM taking whole tiles
+ * round-robin in mode 0, stream-K in mode 2 and data-parallel in mode 1.
+ * Results agree to rounding order either way.
  * Returns OOP_OK, or OOP_ERR_PATH for another mode. */
 int oop_debug_set_tc_schedule(int mode);
 

@@ -128,9 +128,10 @@ def test_auto_schedule_choice(op):
 
 @pytest.mark.parametrize("wt", [synth.TYPE_F32, synth.TYPE_BF16])
 def test_grouped_mul_mat_id_back_schedules(op, orc, wt):
-    """MUL_MAT_ID_BACK's grouped product: stream-K over the device-side work
-    list (the default: routing, split, tile kernel, fix-up) and data-parallel
-    (three launches) both match the oracle; stream-K repeats bit for bit."""
+    """MUL_MAT_ID_BACK's grouped product under its three schedules: persistent
+    whole tiles round-robin (the default: routing, split, tile kernel), stream-K
+    over the device-side work list (+ the fix-up) and data-parallel; all match
+    the oracle and the default repeats bit for bit."""
     import torch
     K, N, E, n_used, T = 300, 136, 7, 3, 110
     W = synth.normal(70, K * N * E, std=0.02).reshape(E, N, K)
@@ -143,7 +144,9 @@ def test_grouped_mul_mat_id_back_schedules(op, orc, wt):
                           else np.ascontiguousarray(W)).cuda()
     tids, tg = torch.from_numpy(ids).cuda(), torch.from_numpy(g).cuda()
     outs, counts = [], []
-    for sched in (op.SCHEDULE_AUTO, op.SCHEDULE_AUTO, op.SCHEDULE_DATA_PARALLEL):
+    scheds = (op.SCHEDULE_AUTO, op.SCHEDULE_AUTO, op.SCHEDULE_STREAM_K,
+              op.SCHEDULE_DATA_PARALLEL)
+    for sched in scheds:
         op.set_tc_schedule(sched)
         try:
             out = op.mul_mat_id_back(tW, tids, tg, w_type=wt, path=op.PATH_TCGEN05)
@@ -153,7 +156,7 @@ def test_grouped_mul_mat_id_back_schedules(op, orc, wt):
             op.set_tc_schedule(op.SCHEDULE_AUTO)
         assert op.device_status() == 0
         outs.append(out.cpu().numpy())
-    assert counts == [4, 4, 3]
-    for o, what in zip(outs, ("stream-K", "stream-K again", "data-parallel")):
+    assert counts == [3, 3, 4, 3]
+    for o, what in zip(outs, ("persistent", "persistent again", "stream-K", "data-parallel")):
         assert_parity(o, ref["f64"], ref["abs"], f"grouped {wt} {what}")
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
