@@ -160,3 +160,42 @@ def test_grouped_mul_mat_id_back_schedules(op, orc, wt):
     for o, what in zip(outs, ("persistent", "persistent again", "stream-K", "data-parallel")):
         assert_parity(o, ref["f64"], ref["abs"], f"grouped {wt} {what}")
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+def test_long_k_stream_k_many_ctas_per_tile(op, orc):
+    """K = 262144 (8192 k-blocks) on two tiles: the automatic choice is
+    stream-K, each tile is shared by ~76 CTAs and the fix-up adds ~76
+    partials per element; checked on sampled elements against the oracle."""
+    import torch
+    m, k, n = 256, 262144, 64
+    a = synth.make_a(Q8, (m, k, 1, 1), 64, std=0.02)
+    b = synth.make_b((n, k, 1, 1), 65, std=1e3, outliers=True)
+    out = op.out_prod(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), a_type=Q8,
+                      ne_a=(m, k, 1, 1), path=op.PATH_TCGEN05)
+    launches = op.last_launch_count()
+    torch.cuda.synchronize()
+    assert op.device_status() == 0
+    assert launches == 3                                  # split, tile kernel, fix-up
+    assert bool(torch.isfinite(out).all())
+    rng = np.random.default_rng(11)
+    coords = np.stack([rng.integers(0, m, 300), rng.integers(0, n, 300),
+                       np.zeros(300, np.int64), np.zeros(300, np.int64)], 1).astype(np.int64)
+    val, ab = orc.out_prod_at(a, Q8, b, (m, k, 1, 1), (n, k, 1, 1), coords)
+    got = out[0, 0, coords[:, 1], coords[:, 0]].cpu().numpy()
+    assert_parity(got, val, ab, "long K stream-K")
+
+
+@pytest.mark.parametrize("a_type,ne_a,ne_b", [
+    (Q8, (32, 200, 1, 1), (40, 200, 1, 1)),      # one ragged m-tile, one ragged n-tile
+    (F32, (500, 96, 1, 1), (33, 96, 1, 1)),      # the narrowest tensor-core width
+    (Q4, (96, 33, 1, 1), (97, 33, 1, 1)),        # one k-block of 33: ragged k, n = 96 + 1
+])
+def test_small_edges_both_schedules(op, orc, a_type, ne_a, ne_b):
+    import torch
+    a = synth.make_a(a_type, ne_a, 66, std=0.02 if a_type != F32 else 1.0)
+    b = synth.make_b(ne_b, 67, std=1e3, outliers=True)
+    ref = orc.out_prod(a, a_type, b, ne_a, ne_b)
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    for sched in (op.SCHEDULE_DATA_PARALLEL, op.SCHEDULE_STREAM_K):
+        got, _ = _run(op, ta, tb, a_type, ne_a, sched)
+        assert_parity(got, ref["f64"], ref["abs"], f"edge {a_type} {ne_a} {ne_b} sched {sched}")
