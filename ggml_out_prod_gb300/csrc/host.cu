@@ -1,16 +1,17 @@
 // host.cu -- OUT_PROD from host buffers: the copies in, the product, the copy
 // of dst out, enqueued as one call.
 //
-// For a single slice with N wide enough for two column chunks, the work is
-// pipelined over two chunks of dst columns n: src0 and the first chunk's
-// src1 columns go in, the first product runs while the second chunk's src1
-// columns are copied, the second product runs while the first chunk of dst
-// is copied out.  The copies run on a library-owned copy stream (one per
+// For a single slice with N wide enough, the work is pipelined over up to four
+// chunks of dst columns n (boundaries on 96-column tile edges): src0 and the
+// first chunk's src1 columns go in, then each product runs while the next
+// chunk's src1 columns are copied in and the previous chunk of dst is copied
+// out.  The copies run on a library-owned copy stream (one per
 // device, created on first use) ordered against the caller's stream by
 // events; everything is enqueued before the call returns and the caller's
 // stream is made to wait for the last copy, so synchronising that stream is
 // enough.  Otherwise the copies and the product run in order on the caller's
 // stream.
+#include <algorithm>
 #include <mutex>
 
 #include "oop_internal.cuh"
@@ -19,7 +20,8 @@ namespace oop {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kEvents = 6;
+constexpr int kMaxChunks = 4;
+constexpr int kEvents = 2 * kMaxChunks + 2;
 
 struct HostPipe {
     cudaStream_t copy = nullptr;
@@ -126,9 +128,10 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
 
     const int64_t M = ne_a[0], K = ne_a[1], N = ne_b[0];
     const bool single = ne_b[2] * ne_b[3] == 1 && ne_a[2] * ne_a[3] == 1;
-    const int64_t n0 = (N / 2 + 95) / 96 * 96;                 // chunk boundary on a tile edge
-    const bool pipelined = single && K > 0 && n0 >= 96 && n0 < N;
-    if (!pipelined) {
+    // chunks of at least two 96-column tiles, boundaries on tile edges
+    const int64_t tiles_n = (N + 95) / 96;
+    const int chunks = single && K > 0 ? static_cast<int>(std::min<int64_t>(kMaxChunks, tiles_n / 2)) : 1;
+    if (chunks < 2) {
         rc = rc_of(cudaMemcpyAsync(a_dev, a_host, L.a_bytes, cudaMemcpyHostToDevice, st));
         if (rc == OOP_OK)
             rc = rc_of(cudaMemcpyAsync(b_dev, b_host, L.b_bytes, cudaMemcpyHostToDevice, st));
@@ -146,35 +149,40 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
     if (rc != OOP_OK) return rc;
     cudaStream_t cs = pp->copy;
     cudaEvent_t *ev = pp->ev;
-    const int64_t nc[2] = {n0, N - n0};
-    const int64_t nb[2] = {0, n0};
-    float *bc[2] = {b_dev, b_dev + K * n0};                    // chunk c: [K][nc] contiguous
+    int64_t nb[kMaxChunks + 1];                                // chunk c: columns [nb[c], nb[c+1])
+    for (int c = 0; c <= chunks; ++c)
+        nb[c] = std::min<int64_t>(N, (tiles_n * c + chunks - 1) / chunks * 96);
     cudaError_t e = cudaEventRecord(ev[0], st);                // after the caller's prior work
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[0], 0);
     if (e == cudaSuccess) e = cudaMemcpyAsync(a_dev, a_host, L.a_bytes, cudaMemcpyHostToDevice, cs);
-    for (int c = 0; c < 2 && e == cudaSuccess; ++c) {
-        e = cudaMemcpy2DAsync(bc[c], nc[c] * 4, b_host + nb[c], N * 4, nc[c] * 4, K,
+    // copy stream: src1 chunk c in, then (once product c is done) dst chunk c out
+    // compute (caller's) stream: product c once its src1 chunk is in
+    int launches = 0;
+    for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+        const int64_t nc = nb[c + 1] - nb[c];
+        float *bc = b_dev + K * nb[c];                          // [K][nc] contiguous
+        e = cudaMemcpy2DAsync(bc, nc * 4, b_host + nb[c], N * 4, nc * 4, K,
                               cudaMemcpyHostToDevice, cs);
         if (e == cudaSuccess) e = cudaEventRecord(ev[1 + c], cs);
-    }
-    int launches = 0;
-    for (int c = 0; c < 2 && e == cudaSuccess; ++c) {
-        e = cudaStreamWaitEvent(st, ev[1 + c], 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[1 + c], 0);
         if (e != cudaSuccess) break;
-        const int64_t ne_bc[4] = {nc[c], K, 1, 1};
-        const int64_t ne_dc[4] = {M, nc[c], 1, 1};
-        rc = oop_out_prod(a_dev, a_type, bc[c], dst_dev + nb[c] * M, ne_a, ne_bc, ne_dc, ws,
+        const int64_t ne_bc[4] = {nc, K, 1, 1};
+        const int64_t ne_dc[4] = {M, nc, 1, 1};
+        rc = oop_out_prod(a_dev, a_type, bc, dst_dev + nb[c] * M, ne_a, ne_bc, ne_dc, ws,
                           L.ws_bytes, stream);
         if (rc != OOP_OK) return rc;
         launches += g_kernel_launches;
-        e = cudaEventRecord(ev[3 + c], st);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[3 + c], 0);
+        e = cudaEventRecord(ev[1 + kMaxChunks + c], st);
+    }
+    for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+        e = cudaStreamWaitEvent(cs, ev[1 + kMaxChunks + c], 0);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(dst_host + nb[c] * M, dst_dev + nb[c] * M,
-                                static_cast<size_t>(nc[c] * M) * 4, cudaMemcpyDeviceToHost, cs);
+                                static_cast<size_t>((nb[c + 1] - nb[c]) * M) * 4,
+                                cudaMemcpyDeviceToHost, cs);
     }
-    if (e == cudaSuccess) e = cudaEventRecord(ev[5], cs);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[5], 0);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[2 * kMaxChunks + 1], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[2 * kMaxChunks + 1], 0);
     g_kernel_launches = launches;
     return rc_of(e);
 }

@@ -128,9 +128,9 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst,
  * device_buffer: device memory of at least
  * oop_out_prod_host_buffer_size(...) bytes (0 for an invalid shape),
  * 256-byte aligned, holding the device copies of a, b and dst and the
- * workspace.  For a single slice wide enough, the call pipelines two column
- * chunks of dst: the second chunk's b columns are copied in while the first
- * chunk is computed, the first chunk of dst is copied out while the second is
+ * workspace.  For a single slice wide enough, the call pipelines up to four
+ * column chunks of dst: a chunk's b columns are copied in while the previous
+ * chunk is computed, and a chunk of dst is copied out while the next one is
  * computed; those copies run on a copy stream the library creates once per
  * device and are ordered against `stream` by events, so the call returns with
  * `stream` waiting for its last copy.  Calls on one device are enqueued one
