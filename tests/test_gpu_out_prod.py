@@ -260,7 +260,7 @@ def test_host_checks_reject(op):
     (Q8, (256, 4096, 1, 1), (100, 4096, 1, 1)),     # long K, narrow: one pass
     (F32, (200, 300, 2, 1), (70, 300, 4, 3)),       # several slices: one pass
     (F32, (256, 512, 1, 1), (8, 512, 1, 1)),        # skinny-N: one pass
-    (Q4, (384, 700, 1, 1), (200, 700, 1, 1)),       # one tile wide pair: one pass
+    (Q4, (384, 700, 1, 1), (200, 700, 1, 1)),       # three n-tiles, too few to chunk: one pass
 ])
 def test_host_entry_matches_oracle(op, orc, a_type, ne_a, ne_b):
     import torch
