@@ -825,32 +825,50 @@ __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__re
 }
 
 // b[slice][k][n] (n fastest) -> bhi, blo [slice][n][Kp] (k fastest), TF32
-// split, zero padding for k in [K, Kp).
+// split, zero padding for k in [K, Kp).  64 k x 64 n per CTA through shared
+// memory; two consecutive n per thread on the way in (when N is even), two
+// consecutive k per thread (8-byte stores) on the way out.
+constexpr int kSplitTile = 64;
+
 __global__ void __launch_bounds__(256) bsplit_kernel(const float *__restrict__ b,
                                                      uint32_t *__restrict__ bhi,
                                                      uint32_t *__restrict__ blo, int64_t K,
                                                      int64_t N, int64_t Kp) {
-    __shared__ float tile[32][33];
+    __shared__ float tile[kSplitTile][kSplitTile + 1];      // [k][n]
     const int64_t slice = blockIdx.z;
-    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 32;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.y) * 32;
+    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * kSplitTile;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kSplitTile;
     const float *bs = b + slice * K * N;
-    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int tx = threadIdx.x, ty = threadIdx.y;           // 32 x 8
+    const bool pairs = (N % 2 == 0) && (reinterpret_cast<uintptr_t>(b) % 8 == 0);
 #pragma unroll
-    for (int i = ty; i < 32; i += 8) {
-        const int64_t k = k0 + i, n = n0 + tx;
-        tile[i][tx] = (k < K && n < N) ? __ldg(bs + k * N + n) : 0.f;
+    for (int i = ty; i < kSplitTile; i += 8) {
+        const int64_t k = k0 + i, n = n0 + 2 * tx;
+        float v0 = 0.f, v1 = 0.f;
+        if (k < K) {
+            if (pairs && n + 1 < N) {
+                const float2 t = __ldg(reinterpret_cast<const float2 *>(bs + k * N + n));
+                v0 = t.x;
+                v1 = t.y;
+            } else {
+                if (n < N) v0 = __ldg(bs + k * N + n);
+                if (n + 1 < N) v1 = __ldg(bs + k * N + n + 1);
+            }
+        }
+        tile[i][2 * tx] = v0;
+        tile[i][2 * tx + 1] = v1;
     }
     __syncthreads();
 #pragma unroll
-    for (int i = ty; i < 32; i += 8) {
-        const int64_t n = n0 + i, k = k0 + tx;
+    for (int i = ty; i < kSplitTile; i += 8) {
+        const int64_t n = n0 + i, k = k0 + 2 * tx;          // Kp is a multiple of 4
         if (n < N && k < Kp) {
-            uint32_t h, l;
-            ptx::split_tf32(tile[tx][i], h, l);
+            uint32_t h0, l0, h1, l1;
+            ptx::split_tf32(tile[2 * tx][i], h0, l0);
+            ptx::split_tf32(tile[2 * tx + 1][i], h1, l1);
             const int64_t o = (slice * N + n) * Kp + k;
-            bhi[o] = h;
-            blo[o] = l;
+            *reinterpret_cast<uint2 *>(bhi + o) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(blo + o) = make_uint2(l0, l1);
         }
     }
 }
@@ -1114,7 +1132,7 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     uint32_t *blo = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + one);
     float *partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + 2 * one);
 
-    const int64_t gk = (Kp + 31) / 32, gn = (s.N + 31) / 32;
+    const int64_t gk = (Kp + kSplitTile - 1) / kSplitTile, gn = (s.N + kSplitTile - 1) / kSplitTile;
     if (gk > 0x7fffffffLL || gn > 65535 || slices > 65535) return cudaErrorInvalidConfiguration;
     bsplit_kernel<<<dim3(static_cast<unsigned>(gk), static_cast<unsigned>(gn),
                          static_cast<unsigned>(slices)),
