@@ -1043,7 +1043,7 @@ int plan_ctas(int64_t tiles, int num_kb, int sms, size_t partial_room) {
     if (G <= 0 || g_schedule == 1 || partial_room < static_cast<size_t>(G) * 2 * kSlotBytes)
         return 0;
     if (g_schedule == 2) return G;
-    if (iters < 16LL * G) return 0;
+    if (iters < 4LL * G) return 0;
     const int64_t dp = (tiles + G - 1) / G * num_kb;
     const int64_t sk = (iters + G - 1) / G + 8;
     return 10 * sk < 9 * dp ? G : 0;
