@@ -173,6 +173,12 @@ def _barrier_max(torch, value, ws):
     return float(t.item())
 
 
+def whole_job_value(ws, flops_per_rank, ms_step_max):
+    """TFLOP/s of the whole job: every rank's work over the slowest rank's
+    step time (replicas: each rank runs the full workload)."""
+    return ws * flops_per_rank / (ms_step_max * 1e-3) / 1e12
+
+
 def _cublas_tf32(torch, device):
     """cuBLAS TF32 GEMM throughput (context for the TF32 roofline)."""
     prev = torch.backends.cuda.matmul.allow_tf32
@@ -264,7 +270,7 @@ def gpu_arm(args):
     ms_step = statistics.mean(step_ms)
     ms_main = statistics.mean(main_ms)
     ms_step_max = _barrier_max(torch, ms_step, ws)
-    value = ws * flops / (ms_step_max * 1e-3) / 1e12
+    value = whole_job_value(ws, flops, ms_step_max)
 
     # ---- e2e: host buffers through the C ABI's host entry ------------------
     # (oop_out_prod_host: copies in, product, copy of dst out, one call; the
