@@ -13,8 +13,11 @@
 //    consumers, so several stages (~34 KB each) stay in flight per SM and the
 //    next item's rows arrive while the current one is being reduced;
 //  * eight consumer warps split each stage's 64 k rows (8 each); lane = VW
-//    consecutive m, N*VW fp32 accumulators per thread, b read as broadcast
-//    float4s;
+//    consecutive m, N*VW fp32 accumulators per thread held as (n, n+1)
+//    pairs and updated with packed f32x2 FMAs (half the issue slots of
+//    scalar FMAs; the same round-to-nearest products and sums), b read as
+//    broadcast float4s; in a full stage each row's loads are issued before
+//    the previous row's FMAs;
 //  * at the end of an item the warps' partials meet in shared memory in fixed
 //    warp order and one thread per output writes dst: deterministic, one
 //    writer per element, no atomics, no workspace.
@@ -59,6 +62,48 @@ struct Layout {
     static constexpr size_t SMEM = size_t(STAGES) * STAGE + RED + 2 * STAGES * 8 + 16 + 1024;
 };
 
+// One k row of a consumer warp: this lane's VW values of src0 and the row of
+// src1 (all N values, the same for every lane).
+template <int NP, int VW>
+struct Row {
+    float a[VW];
+    float4 b[NP / 4];
+};
+
+template <int NP, int VW>
+__device__ __forceinline__ void load_row(const float *sa, const float *sb, int row, int lane,
+                                         Row<NP, VW> &r) {
+    if constexpr (VW == 4) {
+        const float4 t = reinterpret_cast<const float4 *>(sa + row * 32 * VW)[lane];
+        r.a[0] = t.x;
+        r.a[1] = t.y;
+        r.a[2] = t.z;
+        r.a[3] = t.w;
+    } else {
+        const float2 t = reinterpret_cast<const float2 *>(sa + row * 32 * VW)[lane];
+        r.a[0] = t.x;
+        r.a[1] = t.y;
+    }
+    const float4 *brow = reinterpret_cast<const float4 *>(sb + row * NP);
+#pragma unroll
+    for (int q = 0; q < NP / 4; ++q) r.b[q] = brow[q];
+}
+
+// acc[j][v] holds the sums of n = 2j (low half) and n = 2j + 1 (high half)
+// for this lane's m = VW * lane + v.
+template <int NP, int VW>
+__device__ __forceinline__ void fma_row(const Row<NP, VW> &r, uint64_t (&acc)[NP / 2][VW]) {
+#pragma unroll
+    for (int v = 0; v < VW; ++v) {
+        const uint64_t a2 = ptx::pack2(r.a[v], r.a[v]);
+#pragma unroll
+        for (int q = 0; q < NP / 4; ++q) {
+            acc[2 * q][v] = ptx::fma2(a2, ptx::pack2(r.b[q].x, r.b[q].y), acc[2 * q][v]);
+            acc[2 * q + 1][v] = ptx::fma2(a2, ptx::pack2(r.b[q].z, r.b[q].w), acc[2 * q + 1][v]);
+        }
+    }
+}
+
 // N == NP here (the launcher takes this kernel only for N % 4 == 0).
 template <int NP, int VW>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -78,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], kConsumers);
+            ptx::mbar_init(&empty[s], kConsumerWarps);   // one arrival per warp
         }
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -139,11 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t item = blockIdx.x; item < p.items; item += gridDim.x) {
             const int64_t slice = item / p.mtiles;
             const int mt = static_cast<int>(item % p.mtiles);
-            float acc[NP][VW];
+            uint64_t acc[NP / 2][VW];
 #pragma unroll
-            for (int n = 0; n < NP; ++n)
+            for (int j = 0; j < NP / 2; ++j)
 #pragma unroll
-                for (int v = 0; v < VW; ++v) acc[n][v] = 0.f;
+                for (int v = 0; v < VW; ++v) acc[j][v] = 0;   // +0.0f in both halves
             for (int ks = 0; ks < p.kstages; ++ks) {
                 if (ok) {
                     const bool got = ptx::mbar_wait_bounded(&full[s], ph, abort, true, kWaitNs,
@@ -155,35 +200,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float *sb =
                         reinterpret_cast<const float *>(smem + s * L::STAGE + L::A_BYTES);
                     const int64_t k0 = static_cast<int64_t>(ks) * kTK;
+                    const int row0 = warp * kRowsPerWarp;
+                    if (k0 + kTK <= p.K) {
+                        // a full stage: row j + 1's loads go out before row j's FMAs
+                        Row<NP, VW> cur, nxt;
+                        load_row<NP, VW>(sa, sb, row0, lane, cur);
 #pragma unroll
-                    for (int j = 0; j < kRowsPerWarp; ++j) {
-                        const int row = warp * kRowsPerWarp + j;
-                        if (k0 + row < p.K) {       // rows past K belong to the next slice
-                            float av[VW];
-                            if constexpr (VW == 4) {
-                                const float4 t =
-                                    reinterpret_cast<const float4 *>(sa + row * L::TM)[lane];
-                                av[0] = t.x; av[1] = t.y; av[2] = t.z; av[3] = t.w;
-                            } else {
-                                const float2 t =
-                                    reinterpret_cast<const float2 *>(sa + row * L::TM)[lane];
-                                av[0] = t.x; av[1] = t.y;
-                            }
-                            const float *brow = sb + row * NP;
-#pragma unroll
-                            for (int n4 = 0; n4 < NP; n4 += 4) {
-                                const float4 bv = *reinterpret_cast<const float4 *>(brow + n4);
-#pragma unroll
-                                for (int v = 0; v < VW; ++v) {
-                                    acc[n4 + 0][v] = fmaf(av[v], bv.x, acc[n4 + 0][v]);
-                                    acc[n4 + 1][v] = fmaf(av[v], bv.y, acc[n4 + 1][v]);
-                                    acc[n4 + 2][v] = fmaf(av[v], bv.z, acc[n4 + 2][v]);
-                                    acc[n4 + 3][v] = fmaf(av[v], bv.w, acc[n4 + 3][v]);
-                                }
+                        for (int j = 0; j < kRowsPerWarp; ++j) {
+                            if (j + 1 < kRowsPerWarp)
+                                load_row<NP, VW>(sa, sb, row0 + j + 1, lane, nxt);
+                            fma_row<NP, VW>(cur, acc);
+                            if (j + 1 < kRowsPerWarp) cur = nxt;
+                        }
+                    } else {
+                        // the last stage of a slice: rows past K belong to the
+                        // next slice (src0) or were not copied (src1)
+                        for (int j = 0; j < kRowsPerWarp; ++j) {
+                            if (k0 + row0 + j < p.K) {
+                                Row<NP, VW> cur;
+                                load_row<NP, VW>(sa, sb, row0 + j, lane, cur);
+                                fma_row<NP, VW>(cur, acc);
                             }
                         }
                     }
-                    ptx::mbar_arrive(&empty[s]);
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&empty[s]);
                 }
                 if (++s == L::STAGES) {
                     s = 0;
@@ -192,10 +233,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // ---- the warps' partials meet in shared memory (fixed warp order) ----
 #pragma unroll
-            for (int n = 0; n < NP; ++n)
+            for (int j = 0; j < NP / 2; ++j) {
+                float lo[VW], hi[VW];
 #pragma unroll
-                for (int v = 0; v < VW; ++v)
-                    red[(warp * NP + n) * L::TM + lane * VW + v] = acc[n][v];
+                for (int v = 0; v < VW; ++v) ptx::unpack2(acc[j][v], lo[v], hi[v]);
+                float *r0 = red + (warp * NP + 2 * j) * L::TM + lane * VW;
+                float *r1 = r0 + L::TM;
+                if constexpr (VW == 4) {
+                    *reinterpret_cast<float4 *>(r0) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<float4 *>(r1) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                } else {
+                    *reinterpret_cast<float2 *>(r0) = make_float2(lo[0], lo[1]);
+                    *reinterpret_cast<float2 *>(r1) = make_float2(hi[0], hi[1]);
+                }
+            }
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
             if (ok) {
                 float *dst = p.dst + slice * p.N * p.M;
