@@ -47,7 +47,7 @@ NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # headline workload, from the ncu capture summarised in
 # profiles/tc_out_prod_q8_m5120_k5120_n1024.md; None while that capture does
 # not match the kernel in this tree.
-TC_TRAFFIC_BYTES = 87_931_648
+TC_TRAFFIC_BYTES = 83_122_688
 
 
 def _peaks():
@@ -136,16 +136,19 @@ class Timer:
     def flush(self):
         self.flush_buf.fill_(1.0)
 
-    def run(self, fn, steps, warmup):
+    def run(self, fn, steps, warmup, flush=True):
+        """flush=False only for inputs larger than L2, which evict themselves."""
         torch = self.torch
         for _ in range(warmup):
-            self.flush()
+            if flush:
+                self.flush()
             fn()
         torch.cuda.synchronize()
         stream = torch.cuda.current_stream()
         evs = []
         for _ in range(steps):
-            self.flush()
+            if flush:
+                self.flush()
             s = torch.cuda.Event(enable_timing=True)
             e = torch.cuda.Event(enable_timing=True)
             s.record(stream)
@@ -316,20 +319,32 @@ def gpu_arm(args):
     for r in synth.LORA_RANKS:
         parts[f"lora_r{r}"] = skinny_part(r, max(args.steps, 20))
 
-    # rank-8 gradients for many slices in one launch (steady-state streaming)
+    # rank-r gradients for many slices in one launch (steady-state streaming).
+    # src0 is 335 MB, larger than L2, so these steps need no flush; the
+    # figure after a flush is reported beside it (the flush leaves up to 129 MB
+    # of dirty lines that are written back during the call).
     nsl = 64
     an = synth.make_a(synth.TYPE_F32, (2560, 512, nsl, 1), 70)
-    bn = synth.make_b((8, 512, nsl, 1), 71, std=100.0, outliers=True)
-    ta, tb = torch.from_numpy(an).to(device), torch.from_numpy(bn).to(device)
-    o = torch.empty((1, nsl, 8, 2560), dtype=torch.float32, device=device)
-    t = timer.run(lambda: op.out_prod(ta, tb, out=o, path=op.PATH_SKINNY), max(args.steps, 10), 3)
-    byts = 4.0 * nsl * (2560 * 512 + 8 * 512 + 2560 * 8)
-    us = statistics.mean(t) * 1e3
-    parts["lora_r8_x64_slices"] = {
-        "workload": "64 rank-8 gradients in one launch: a [2560, 512, 64] f32, b [8, 512, 64]",
-        "us": round(us, 3), "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
-        "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / hbm, 4)}
-    del ta, tb, o
+    ta = torch.from_numpy(an).to(device)
+    del an
+    for r in synth.LORA_RANKS:
+        bn = synth.make_b((r, 512, nsl, 1), 71, std=100.0, outliers=True)
+        tb = torch.from_numpy(bn).to(device)
+        o = torch.empty((1, nsl, r, 2560), dtype=torch.float32, device=device)
+        call = (lambda tb=tb, o=o: op.out_prod(ta, tb, out=o, path=op.PATH_SKINNY))
+        t = timer.run(call, max(args.steps, 10), 3, flush=False)
+        tf = timer.run(call, max(args.steps, 10), 3)
+        byts = 4.0 * nsl * (2560 * 512 + r * 512 + 2560 * r)
+        us, usf = statistics.mean(t) * 1e3, statistics.mean(tf) * 1e3
+        parts[f"lora_r{r}_x64_slices"] = {
+            "workload": f"64 rank-{r} gradients in one launch: a [2560, 512, 64] f32, b [{r}, 512, 64]",
+            "us": round(us, 3), "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
+            "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / hbm, 4),
+            "l2": "inputs larger than L2, no flush",
+            "us_after_l2_flush": round(usf, 3),
+            "frac_of_measured_hbm_after_flush": round(byts / (usf * 1e-6) / 1e9 / hbm, 4)}
+        del tb, o
+    del ta
 
     for n_seq in (1, 2):
         an, bn = synth.grouped_heads(n_seq)

@@ -18,9 +18,15 @@
 //    scalar FMAs; the same round-to-nearest products and sums), b read as
 //    broadcast float4s; in a full stage each row's loads are issued before
 //    the previous row's FMAs;
-//  * at the end of an item the warps' partials meet in shared memory in fixed
-//    warp order and one thread per output writes dst: deterministic, one
+//  * at the end of an item warps 4-7 hand their partials to warps 0-3
+//    through shared memory, then warps 0-3 publish theirs and one thread per
+//    output adds the four in warp order and writes dst: deterministic, one
 //    writer per element, no atomics, no workspace.
+// Every lane needs every src1 value of a row, and a broadcast from shared
+// memory delivers 4 bytes per wavefront whatever the load width, so a row
+// costs N wavefronts for src1 against VW for src0: four m per lane (TM = 128)
+// halves that cost per byte against two; N = 28 and 32 keep two m per lane
+// (four would not fit in the registers).
 // Waits are bounded like the tensor-core kernel's: running out records
 // OOP_ERR_DEVICE_TIMEOUT, every role stops, the TMA warp drains its copies.
 #include <algorithm>
@@ -54,7 +60,10 @@ struct Layout {
     static constexpr int A_BYTES = kTK * TM * 4;
     static constexpr int B_BYTES = kTK * NP * 4;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int RED = kConsumerWarps * NP * TM * 4;
+    static constexpr int RED = kConsumerWarps / 2 * NP * TM * 4;   // four warps' partials
+    // the next row's loads ahead of the FMAs where the registers allow
+    // (nine warps put three on one sub-partition: at most 168 registers)
+    static constexpr bool PREFETCH = NP * VW + 2 * (NP + VW) <= 136;
     // as many stages as fit in ~220 KB next to the reduction buffer
     static constexpr int STAGES_FIT = (220 * 1024 - RED - 2048) / STAGE;
     static constexpr int STAGES = STAGES_FIT < kMaxStages ? STAGES_FIT : kMaxStages;
@@ -100,6 +109,47 @@ __device__ __forceinline__ void fma_row(const Row<NP, VW> &r, uint64_t (&acc)[NP
         for (int q = 0; q < NP / 4; ++q) {
             acc[2 * q][v] = ptx::fma2(a2, ptx::pack2(r.b[q].x, r.b[q].y), acc[2 * q][v]);
             acc[2 * q + 1][v] = ptx::fma2(a2, ptx::pack2(r.b[q].z, r.b[q].w), acc[2 * q + 1][v]);
+        }
+    }
+}
+
+// A warp's partial in the reduction buffer: rows n of TM floats, this lane's
+// VW consecutive m in each.
+template <int NP, int VW>
+__device__ __forceinline__ void store_partial(float *r, const uint64_t (&acc)[NP / 2][VW]) {
+#pragma unroll
+    for (int j = 0; j < NP / 2; ++j) {
+        float lo[VW], hi[VW];
+#pragma unroll
+        for (int v = 0; v < VW; ++v) ptx::unpack2(acc[j][v], lo[v], hi[v]);
+        float *r0 = r + 2 * j * 32 * VW, *r1 = r0 + 32 * VW;
+        if constexpr (VW == 4) {
+            *reinterpret_cast<float4 *>(r0) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<float4 *>(r1) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+        } else {
+            *reinterpret_cast<float2 *>(r0) = make_float2(lo[0], lo[1]);
+            *reinterpret_cast<float2 *>(r1) = make_float2(hi[0], hi[1]);
+        }
+    }
+}
+
+template <int NP, int VW>
+__device__ __forceinline__ void add_partial(const float *r, uint64_t (&acc)[NP / 2][VW]) {
+#pragma unroll
+    for (int j = 0; j < NP / 2; ++j) {
+        const float *r0 = r + 2 * j * 32 * VW, *r1 = r0 + 32 * VW;
+        if constexpr (VW == 4) {
+            const float4 lo = *reinterpret_cast<const float4 *>(r0);
+            const float4 hi = *reinterpret_cast<const float4 *>(r1);
+            acc[j][0] = ptx::add2(acc[j][0], ptx::pack2(lo.x, hi.x));
+            acc[j][1] = ptx::add2(acc[j][1], ptx::pack2(lo.y, hi.y));
+            acc[j][2] = ptx::add2(acc[j][2], ptx::pack2(lo.z, hi.z));
+            acc[j][3] = ptx::add2(acc[j][3], ptx::pack2(lo.w, hi.w));
+        } else {
+            const float2 lo = *reinterpret_cast<const float2 *>(r0);
+            const float2 hi = *reinterpret_cast<const float2 *>(r1);
+            acc[j][0] = ptx::add2(acc[j][0], ptx::pack2(lo.x, hi.x));
+            acc[j][1] = ptx::add2(acc[j][1], ptx::pack2(lo.y, hi.y));
         }
     }
 }
@@ -202,15 +252,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t k0 = static_cast<int64_t>(ks) * kTK;
                     const int row0 = warp * kRowsPerWarp;
                     if (k0 + kTK <= p.K) {
-                        // a full stage: row j + 1's loads go out before row j's FMAs
-                        Row<NP, VW> cur, nxt;
-                        load_row<NP, VW>(sa, sb, row0, lane, cur);
+                        if constexpr (L::PREFETCH) {
+                            // row j + 1's loads go out before row j's FMAs
+                            Row<NP, VW> cur, nxt;
+                            load_row<NP, VW>(sa, sb, row0, lane, cur);
 #pragma unroll
-                        for (int j = 0; j < kRowsPerWarp; ++j) {
-                            if (j + 1 < kRowsPerWarp)
-                                load_row<NP, VW>(sa, sb, row0 + j + 1, lane, nxt);
-                            fma_row<NP, VW>(cur, acc);
-                            if (j + 1 < kRowsPerWarp) cur = nxt;
+                            for (int j = 0; j < kRowsPerWarp; ++j) {
+                                if (j + 1 < kRowsPerWarp)
+                                    load_row<NP, VW>(sa, sb, row0 + j + 1, lane, nxt);
+                                fma_row<NP, VW>(cur, acc);
+                                if (j + 1 < kRowsPerWarp) cur = nxt;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < kRowsPerWarp; ++j) {
+                                Row<NP, VW> cur;
+                                load_row<NP, VW>(sa, sb, row0 + j, lane, cur);
+                                fma_row<NP, VW>(cur, acc);
+                            }
                         }
                     } else {
                         // the last stage of a slice: rows past K belong to the
@@ -231,21 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ph ^= 1;
                 }
             }
-            // ---- the warps' partials meet in shared memory (fixed warp order) ----
-#pragma unroll
-            for (int j = 0; j < NP / 2; ++j) {
-                float lo[VW], hi[VW];
-#pragma unroll
-                for (int v = 0; v < VW; ++v) ptx::unpack2(acc[j][v], lo[v], hi[v]);
-                float *r0 = red + (warp * NP + 2 * j) * L::TM + lane * VW;
-                float *r1 = r0 + L::TM;
-                if constexpr (VW == 4) {
-                    *reinterpret_cast<float4 *>(r0) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-                    *reinterpret_cast<float4 *>(r1) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                } else {
-                    *reinterpret_cast<float2 *>(r0) = make_float2(lo[0], lo[1]);
-                    *reinterpret_cast<float2 *>(r1) = make_float2(hi[0], hi[1]);
-                }
+            // ---- the warps' partials meet in shared memory (fixed order) ----
+            // round 1: warp w + 4 hands its partial to warp w (w < 4)
+            const int slot = warp & 3;
+            float *mine = red + slot * NP * L::TM + lane * VW;
+            if (warp >= 4) store_partial<NP, VW>(mine, acc);
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+            // round 2: warps 0-3 add it and publish the sum in the same slot
+            // (each lane rereads and rewrites only its own words), then one
+            // thread per output adds the four slots
+            if (warp < 4) {
+                add_partial<NP, VW>(mine, acc);
+                store_partial<NP, VW>(mine, acc);
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
             if (ok) {
@@ -254,8 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int n = o / L::TM, mm = o % L::TM;
                     float sum = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w)
-                        sum += red[(w * NP + n) * L::TM + mm];
+                    for (int w = 0; w < 4; ++w) sum += red[(w * NP + n) * L::TM + mm];
                     const int64_t m = static_cast<int64_t>(mt) * L::TM + mm;
                     if (m < p.M) dst[static_cast<int64_t>(n) * p.M + m] = sum;
                 }
@@ -315,25 +370,39 @@ cudaError_t launch_tma(const float *a, const float *b, float *dst, const OutProd
 
 }  // namespace
 
+// Items of 128 m (four m per lane) up to N = 24, of 64 m above; N = 20 and
+// 24 fall back to 64 when 128-wide items would leave fewer than two per SM.
+// 0: the persistent form does not apply (fewer than two items per SM).
+static int64_t tma_tile_m(const OutProdShape &s, int sms) {
+    const int64_t slices = s.ne12 * s.ne13;
+    const int64_t need = 2LL * sms;
+    if (s.N <= 24 && (s.M + 127) / 128 * slices >= need) return 128;
+    if (s.N >= 20 && (s.M + 63) / 64 * slices >= need) return 64;
+    return 0;
+}
+
 bool skinny_tma_ok(const float *a, const float *b, const OutProdShape &s) {
     const int sms = device_sm_count();
-    const int64_t tm = s.N <= 16 ? 128 : 64;
-    const int64_t items = (s.M + tm - 1) / tm * s.ne12 * s.ne13;
     return sms > 0 && s.N % 4 == 0 && s.M % 4 == 0 && reinterpret_cast<uintptr_t>(a) % 16 == 0 &&
            reinterpret_cast<uintptr_t>(b) % 16 == 0 && s.K * s.ne02 * s.ne03 < (1LL << 31) &&
-           s.K < (1LL << 31) && items >= 2LL * sms;
+           s.K < (1LL << 31) && tma_tile_m(s, sms) > 0;
 }
 
 cudaError_t launch_skinny_tma(const float *a, const float *b, float *dst, const OutProdShape &s,
                               int *status, cudaStream_t stream) {
     const int sms = device_sm_count();
+    const bool wide = tma_tile_m(s, sms) == 128;
     switch (s.N) {
     case 4: return launch_tma<4, 4>(a, b, dst, s, status, sms, stream);
     case 8: return launch_tma<8, 4>(a, b, dst, s, status, sms, stream);
     case 12: return launch_tma<12, 4>(a, b, dst, s, status, sms, stream);
     case 16: return launch_tma<16, 4>(a, b, dst, s, status, sms, stream);
-    case 20: return launch_tma<20, 2>(a, b, dst, s, status, sms, stream);
-    case 24: return launch_tma<24, 2>(a, b, dst, s, status, sms, stream);
+    case 20:
+        return wide ? launch_tma<20, 4>(a, b, dst, s, status, sms, stream)
+                    : launch_tma<20, 2>(a, b, dst, s, status, sms, stream);
+    case 24:
+        return wide ? launch_tma<24, 4>(a, b, dst, s, status, sms, stream)
+                    : launch_tma<24, 2>(a, b, dst, s, status, sms, stream);
     case 28: return launch_tma<28, 2>(a, b, dst, s, status, sms, stream);
     case 32: return launch_tma<32, 2>(a, b, dst, s, status, sms, stream);
     default: return cudaErrorInvalidValue;

@@ -1,7 +1,8 @@
 """GPU parity of the skinny-N OUT_PROD on large problems, where the library
 takes its persistent TMA-fed form (at least two m-tile x slice items per SM,
-N % 4 == 0, M % 4 == 0): ragged m-tiles, K not a multiple of the 64-row
-stage, broadcast slices, every N the form supports, outliers in b."""
+N % 4 == 0, M % 4 == 0; items of 128 m up to N = 24, of 64 m above or when
+128 would be too few): ragged m-tiles, K not a multiple of the 64-row stage,
+broadcast slices, both item widths, outliers in b."""
 
 import numpy as np
 import pytest
@@ -27,7 +28,9 @@ def op():
 @pytest.mark.parametrize("ne_a,ne_b", [
     ((1000, 300, 40, 1), (8, 300, 40, 1)),       # 8 m-tiles (last ragged) x 40 slices
     ((1000, 300, 10, 1), (4, 300, 40, 1)),       # broadcast: 4 dst slices per src0 slice
-    ((1000, 130, 20, 1), (24, 130, 20, 1)),      # N = 24: 64-wide m-tiles; K = 2 stages + 2 rows
+    ((1000, 130, 20, 1), (24, 130, 20, 1)),      # N = 24, 160 items of 128 m: 64-wide; K = 2 stages + 2
+    ((1000, 200, 40, 1), (24, 200, 40, 1)),      # N = 24, 320 items of 128 m; K = 3 stages + 8 rows
+    ((640, 96, 64, 1), (20, 96, 64, 1)),         # N = 20, 128-wide, K = 1.5 stages
     ((512, 77, 5, 2), (32, 77, 20, 4)),          # N = 32, broadcast in both dims
     ((2000, 64, 30, 1), (12, 64, 30, 1)),        # K exactly one stage
 ])
