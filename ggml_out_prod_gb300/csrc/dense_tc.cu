@@ -777,8 +777,14 @@ __global__ void __maxnreg__(MAX_REGS)
 // more CTAs gets the sum of their partials, in CTA (= k) order, with a Kahan
 // compensation, rounded once.  Tiles owned by one CTA were written by it and
 // are skipped.
+// One thread per element of a shared tile: grid (tiles, BM * BN / FIX_THREADS).
+// The partials of the CTAs sharing the tile are read FIX_BATCH at a time
+// (independent loads in flight together) and added in CTA order with a Kahan
+// compensation, so a tile shared by many CTAs (long K on few tiles) is not a
+// chain of dependent loads.
 constexpr int FIX_THREADS = 256;
-constexpr int FIX_PER = BM * BN / FIX_THREADS;
+constexpr int FIX_CHUNKS = BM * BN / FIX_THREADS;
+constexpr int FIX_BATCH = 8;
 static_assert(BM * BN % FIX_THREADS == 0, "fix-up tiling");
 
 template <bool GROUPED>
@@ -792,36 +798,47 @@ __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__re
     const int64_t x0 = t * p.num_kb, x1 = x0 + p.num_kb - 1;
     const int64_t c0 = sk_owner(iters, p.ctas, x0), c1 = sk_owner(iters, p.ctas, x1);
     if (c0 == c1) return;
-    float sum[FIX_PER], cmp[FIX_PER];
+    const int e = static_cast<int>(blockIdx.y) * FIX_THREADS + threadIdx.x;   // in [0, BM*BN)
+    float sum = 0.f, cmp = 0.f;
+    int64_t b_next = sk_begin(iters, p.ctas, c0);
+    for (int64_t cb = c0; cb <= c1; cb += FIX_BATCH) {
+        float v[FIX_BATCH];
+        bool use[FIX_BATCH];
 #pragma unroll
-    for (int j = 0; j < FIX_PER; ++j) sum[j] = cmp[j] = 0.f;
-    for (int64_t c = c0; c <= c1; ++c) {
-        const int64_t b0 = sk_begin(iters, p.ctas, c);
-        if (b0 == sk_begin(iters, p.ctas, c + 1)) continue;    // a CTA with no iterations
-        // CTA c's segment of this tile is its first (slot 0) if it starts in it
-        const int slot = b0 >= x0 ? 0 : 1;
-        const float *src = partial + (c * 2 + slot) * (BM * BN);
+        for (int i = 0; i < FIX_BATCH; ++i) {
+            const int64_t c = cb + i;
+            use[i] = false;
+            v[i] = 0.f;
+            if (c <= c1) {
+                const int64_t b0 = b_next;
+                b_next = sk_begin(iters, p.ctas, c + 1);
+                if (b0 != b_next) {                    // a CTA with iterations
+                    // CTA c's segment of this tile is its first (slot 0) if it
+                    // starts in it
+                    const int slot = b0 >= x0 ? 0 : 1;
+                    v[i] = __ldg(partial + (c * 2 + slot) * (BM * BN) + e);
+                    use[i] = true;
+                }
+            }
+        }
 #pragma unroll
-        for (int j = 0; j < FIX_PER; ++j) {
-            const float y = __ldg(src + threadIdx.x + j * FIX_THREADS) - cmp[j];
-            const float s2 = sum[j] + y;
-            cmp[j] = (s2 - sum[j]) - y;
-            sum[j] = s2;
+        for (int i = 0; i < FIX_BATCH; ++i) {
+            if (use[i]) {
+                const float y = v[i] - cmp;
+                const float s2 = sum + y;
+                cmp = (s2 - sum) - y;
+                sum = s2;
+            }
         }
     }
     const Tile d = decode_tile<GROUPED>(p, t);
     const int64_t tile_cols = d.ncols - static_cast<int64_t>(d.nt) * BN;
     float *out = GROUPED ? p.dst : p.dst + d.slice * p.N * p.M;
-#pragma unroll
-    for (int j = 0; j < FIX_PER; ++j) {
-        const int e = threadIdx.x + j * FIX_THREADS;
-        const int64_t m = static_cast<int64_t>(d.mt) * BM + e % BM;
-        const int64_t col = e / BM;                               // column in the tile
-        if (m >= p.M || col >= tile_cols) continue;
-        const int64_t row = GROUPED ? p.grp_rows[d.brow0 + col]
-                                    : static_cast<int64_t>(d.nt) * BN + col;
-        out[row * p.M + m] = sum[j] - cmp[j];
-    }
+    const int64_t m = static_cast<int64_t>(d.mt) * BM + e % BM;
+    const int64_t col = e / BM;                                   // column in the tile
+    if (m >= p.M || col >= tile_cols) return;
+    const int64_t row = GROUPED ? p.grp_rows[d.brow0 + col] : static_cast<int64_t>(d.nt) * BN + col;
+    out[row * p.M + m] = sum - cmp;
 }
 
 // b[slice][k][n] (n fastest) -> bhi, blo [slice][n][Kp] (k fastest), TF32
@@ -1189,7 +1206,8 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     }
     if (e != cudaSuccess || p.ctas == 0) return e;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    sk_fixup_kernel<false><<<static_cast<unsigned>(tiles), FIX_THREADS, 0, stream>>>(partial, p);
+    sk_fixup_kernel<false><<<dim3(static_cast<unsigned>(tiles), FIX_CHUNKS), FIX_THREADS, 0, stream>>>(
+        partial, p);
     e = cudaGetLastError();
     if (e == cudaSuccess) ++g_kernel_launches;
     return e;
@@ -1322,7 +1340,8 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     else
         return cudaErrorInvalidValue;
     if (e != cudaSuccess || p.ctas == 0) return e;
-    sk_fixup_kernel<true><<<static_cast<unsigned>(max_grid), FIX_THREADS, 0, stream>>>(p.partial, p);
+    sk_fixup_kernel<true><<<dim3(static_cast<unsigned>(max_grid), FIX_CHUNKS), FIX_THREADS, 0, stream>>>(
+        p.partial, p);
     e = cudaGetLastError();
     if (e == cudaSuccess) ++g_kernel_launches;
     return e;
