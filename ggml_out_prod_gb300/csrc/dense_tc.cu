@@ -777,17 +777,21 @@ __global__ void __maxnreg__(MAX_REGS)
 // more CTAs gets the sum of their partials, in CTA (= k) order, with a Kahan
 // compensation, rounded once.  Tiles owned by one CTA were written by it and
 // are skipped.
-// One thread per element of a shared tile: grid (tiles, BM * BN / FIX_THREADS).
-// The partials of the CTAs sharing the tile are read FIX_BATCH at a time
-// (independent loads in flight together) and added in CTA order with a Kahan
-// compensation, so a tile shared by many CTAs (long K on few tiles) is not a
-// chain of dependent loads.
+// Sums the partials of the tiles that several CTAs share, in CTA (= k) order
+// with a Kahan compensation, and writes them to dst.  Two forms:
+//  * EPT = FIX_CHUNKS, BATCH = 1: one CTA per tile, EPT elements per thread,
+//    for tiles shared by a few CTAs (each partial read once, coalesced);
+//  * EPT = 1, BATCH = FIX_BATCH: grid (tiles, FIX_CHUNKS), one element per
+//    thread, the partials read BATCH at a time (independent loads in flight
+//    together), for tiles shared by many CTAs (long K on few tiles), where
+//    the first form is a long chain of dependent loads on a few SMs.
+// Both add the same partials in the same order: the results are identical.
 constexpr int FIX_THREADS = 256;
 constexpr int FIX_CHUNKS = BM * BN / FIX_THREADS;
 constexpr int FIX_BATCH = 8;
 static_assert(BM * BN % FIX_THREADS == 0, "fix-up tiling");
 
-template <bool GROUPED>
+template <bool GROUPED, int EPT, int BATCH>
 __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__restrict__ partial,
                                                                const TcParams p) {
     const int64_t t = blockIdx.x;
@@ -798,17 +802,19 @@ __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__re
     const int64_t x0 = t * p.num_kb, x1 = x0 + p.num_kb - 1;
     const int64_t c0 = sk_owner(iters, p.ctas, x0), c1 = sk_owner(iters, p.ctas, x1);
     if (c0 == c1) return;
-    const int e = static_cast<int>(blockIdx.y) * FIX_THREADS + threadIdx.x;   // in [0, BM*BN)
-    float sum = 0.f, cmp = 0.f;
-    int64_t b_next = sk_begin(iters, p.ctas, c0);
-    for (int64_t cb = c0; cb <= c1; cb += FIX_BATCH) {
-        float v[FIX_BATCH];
-        bool use[FIX_BATCH];
+    // this thread's elements of the tile: e0 + j * FIX_THREADS, j < EPT
+    const int e0 = static_cast<int>(blockIdx.y) * EPT * FIX_THREADS + threadIdx.x;
+    float sum[EPT], cmp[EPT];
 #pragma unroll
-        for (int i = 0; i < FIX_BATCH; ++i) {
+    for (int j = 0; j < EPT; ++j) sum[j] = cmp[j] = 0.f;
+    int64_t b_next = sk_begin(iters, p.ctas, c0);
+    for (int64_t cb = c0; cb <= c1; cb += BATCH) {
+        float v[BATCH][EPT];
+        bool use[BATCH];
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
             const int64_t c = cb + i;
             use[i] = false;
-            v[i] = 0.f;
             if (c <= c1) {
                 const int64_t b0 = b_next;
                 b_next = sk_begin(iters, p.ctas, c + 1);
@@ -816,29 +822,51 @@ __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__re
                     // CTA c's segment of this tile is its first (slot 0) if it
                     // starts in it
                     const int slot = b0 >= x0 ? 0 : 1;
-                    v[i] = __ldg(partial + (c * 2 + slot) * (BM * BN) + e);
+                    const float *src = partial + (c * 2 + slot) * (BM * BN) + e0;
+#pragma unroll
+                    for (int j = 0; j < EPT; ++j) v[i][j] = __ldg(src + j * FIX_THREADS);
                     use[i] = true;
                 }
             }
         }
 #pragma unroll
-        for (int i = 0; i < FIX_BATCH; ++i) {
-            if (use[i]) {
-                const float y = v[i] - cmp;
-                const float s2 = sum + y;
-                cmp = (s2 - sum) - y;
-                sum = s2;
+        for (int i = 0; i < BATCH; ++i) {
+            if (!use[i]) continue;
+#pragma unroll
+            for (int j = 0; j < EPT; ++j) {
+                const float y = v[i][j] - cmp[j];
+                const float s2 = sum[j] + y;
+                cmp[j] = (s2 - sum[j]) - y;
+                sum[j] = s2;
             }
         }
     }
     const Tile d = decode_tile<GROUPED>(p, t);
     const int64_t tile_cols = d.ncols - static_cast<int64_t>(d.nt) * BN;
     float *out = GROUPED ? p.dst : p.dst + d.slice * p.N * p.M;
-    const int64_t m = static_cast<int64_t>(d.mt) * BM + e % BM;
-    const int64_t col = e / BM;                                   // column in the tile
-    if (m >= p.M || col >= tile_cols) return;
-    const int64_t row = GROUPED ? p.grp_rows[d.brow0 + col] : static_cast<int64_t>(d.nt) * BN + col;
-    out[row * p.M + m] = sum - cmp;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        const int e = e0 + j * FIX_THREADS;
+        const int64_t m = static_cast<int64_t>(d.mt) * BM + e % BM;
+        const int64_t col = e / BM;                               // column in the tile
+        if (m >= p.M || col >= tile_cols) continue;
+        const int64_t row = GROUPED ? p.grp_rows[d.brow0 + col]
+                                    : static_cast<int64_t>(d.nt) * BN + col;
+        out[row * p.M + m] = sum[j] - cmp[j];
+    }
+}
+
+// The fix-up for `tiles` tiles (an upper bound for the grouped product)
+// shared out among p.ctas CTAs: the per-element form once a tile has about
+// four partials or more.
+template <bool GROUPED>
+void launch_fixup(const float *partial, const TcParams &p, int64_t tiles, cudaStream_t stream) {
+    if (p.ctas >= 4 * tiles)
+        sk_fixup_kernel<GROUPED, 1, FIX_BATCH>
+            <<<dim3(static_cast<unsigned>(tiles), FIX_CHUNKS), FIX_THREADS, 0, stream>>>(partial, p);
+    else
+        sk_fixup_kernel<GROUPED, FIX_CHUNKS, 1>
+            <<<static_cast<unsigned>(tiles), FIX_THREADS, 0, stream>>>(partial, p);
 }
 
 // b[slice][k][n] (n fastest) -> bhi, blo [slice][n][Kp] (k fastest), TF32
@@ -1060,9 +1088,10 @@ int plan_ctas(int64_t tiles, int num_kb, int sms, size_t partial_room) {
     if (G <= 0 || g_schedule == 1 || partial_room < static_cast<size_t>(G) * 2 * kSlotBytes)
         return 0;
     if (g_schedule == 2) return G;
-    if (iters < 4LL * G) return 0;
+    // in k-block times: data-parallel waves x the k-blocks of a tile, against
+    // an even share of the iterations plus the partials and the fix-up (~12)
     const int64_t dp = (tiles + G - 1) / G * num_kb;
-    const int64_t sk = (iters + G - 1) / G + 8;
+    const int64_t sk = (iters + G - 1) / G + 12;
     return 10 * sk < 9 * dp ? G : 0;
 }
 
@@ -1206,8 +1235,7 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     }
     if (e != cudaSuccess || p.ctas == 0) return e;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    sk_fixup_kernel<false><<<dim3(static_cast<unsigned>(tiles), FIX_CHUNKS), FIX_THREADS, 0, stream>>>(
-        partial, p);
+    launch_fixup<false>(partial, p, tiles, stream);
     e = cudaGetLastError();
     if (e == cudaSuccess) ++g_kernel_launches;
     return e;
@@ -1340,8 +1368,7 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     else
         return cudaErrorInvalidValue;
     if (e != cudaSuccess || p.ctas == 0) return e;
-    sk_fixup_kernel<true><<<dim3(static_cast<unsigned>(max_grid), FIX_CHUNKS), FIX_THREADS, 0, stream>>>(
-        p.partial, p);
+    launch_fixup<true>(p.partial, p, max_grid, stream);
     e = cudaGetLastError();
     if (e == cudaSuccess) ++g_kernel_launches;
     return e;

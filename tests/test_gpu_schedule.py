@@ -105,13 +105,14 @@ def test_below_minimum_workspace_rejected(op):
 def test_auto_schedule_choice(op):
     """The automatic schedule takes stream-K exactly when the data-parallel
     waves (tiles / SMs, rounded up, times the k-blocks per tile) would cost
-    more than 10/9 of an even share of the iterations plus eight k-blocks;
+    more than 10/9 of an even share of the iterations plus twelve k-blocks;
     shown on the dense shapes and on small problems: a wave that is mostly
-    empty with long K (stream-K), short K (data-parallel)."""
+    empty with long K (stream-K), short K (data-parallel), a single tile."""
     import torch
     sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 160)
     for m, k, n in ((5120, 5120, 1024), (5120, 17408, 1024), (1536, 1536, 1024),
-                    (256, 8192, 96), (512, 4096, 256), (1024, 512, 128)):
+                    (256, 8192, 96), (512, 4096, 256), (1024, 512, 128), (128, 2048, 96),
+                    (1536, 1536, 256)):
         ta = torch.zeros(k * m // 32 * 34, dtype=torch.uint8, device="cuda")
         tb = torch.zeros((k, n), dtype=torch.float32, device="cuda")
         op.out_prod(ta, tb, a_type=Q8, ne_a=(m, k, 1, 1), path=op.PATH_TCGEN05)
@@ -121,8 +122,8 @@ def test_auto_schedule_choice(op):
         nkb = -(-k // 32)
         g = min(sms, tiles * nkb)
         dp = -(-tiles // g) * nkb
-        sk = -(-(tiles * nkb) // g) + 8
-        want_sk = tiles * nkb >= 4 * g and 10 * sk < 9 * dp
+        sk = -(-(tiles * nkb) // g) + 12
+        want_sk = 10 * sk < 9 * dp
         assert got == (3 if want_sk else 2), (m, k, n, got)
 
 
