@@ -357,6 +357,12 @@ __global__ void __maxnreg__(MAX_REGS)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // The tile kernel is launched as a programmatic dependent of the split
+    // pass before it (bsplit / mmid_gsplit): nothing that pass (or the routing
+    // before it) writes is read before griddep_wait().  The grouped kernel
+    // reads the device-side tile count at once, so it waits here; the other
+    // waits after its prologue.
+    if constexpr (GROUPED) ptx::griddep_wait();
     // this CTA's iterations [it0, it1)
     int64_t it0, it1;
     Span span = {};
@@ -413,6 +419,7 @@ __global__ void __maxnreg__(MAX_REGS)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    if constexpr (!GROUPED) ptx::griddep_wait();   // the split of src1 is complete
     const uint32_t tmem = bars->tmem_base;
     bool timed_out = false;
 
@@ -916,6 +923,9 @@ __global__ void __launch_bounds__(256) bsplit_kernel(const float *__restrict__ b
             *reinterpret_cast<uint2 *>(blo + o) = make_uint2(l0, l1);
         }
     }
+    // the tile kernel after this one may start launching (it waits for this
+    // grid to complete before it reads bhi / blo)
+    ptx::griddep_launch_dependents();
 }
 
 // ---- MUL_MAT_ID_BACK as a grouped product ----------------------------------
@@ -991,6 +1001,7 @@ __global__ void __launch_bounds__(256) mmid_gsplit_kernel(const float *__restric
             glo[j * Kp + r] = l;
         }
     }
+    ptx::griddep_launch_dependents();   // as in bsplit_kernel
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
@@ -1117,7 +1128,19 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
         cudaEvent_t before = g_ev_before, after = g_ev_after;
         g_ev_before = g_ev_after = nullptr;
         if (before && (e = cudaEventRecord(before, stream)) != cudaSuccess) return e;
-        kern<<<grid, THREADS, smem, stream>>>(mhi, mlo, ma, p);
+        // a programmatic dependent of the split pass launched just before it
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t le = cudaLaunchKernelEx(&cfg, kern, mhi, mlo, ma, p);
+        if (le != cudaSuccess) return le;
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         ++g_kernel_launches;

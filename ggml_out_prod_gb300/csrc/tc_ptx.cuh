@@ -342,6 +342,16 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) 
     lo = tf32_round_bits(__float_as_uint(rest));
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the kernel before it on the stream is still
+// running; griddep_wait() returns once that kernel has completed and its
+// memory is visible.  launch_dependents() lets the next kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Two fp32 lanes in one 64-bit register (sm_100 packed arithmetic).
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
     uint64_t r;
