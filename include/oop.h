@@ -241,8 +241,9 @@ int oop_debug_inject_timeout(int enable);
 
 /* Test hook (no counterpart on the pages): the schedule of the tensor-core
  * OUT_PROD tile kernel for the calls that follow on this process.  mode 0 =
- * automatic (the default: stream-K when the last data-parallel wave would
- * run mostly empty and the workspace holds the partials), 1 = always
+ * automatic (the default: stream-K when an even share of the tile x k-block
+ * iterations per SM, plus the cost of the partials and the fix-up, beats the
+ * data-parallel waves by 10%, and the workspace holds the partials), 1 = always
  * data-parallel (one 128 x 96 dst tile per CTA), 2 = always stream-K (one
  * CTA per SM sharing the tile x k-block iterations, then a fix-up kernel),
  * when the workspace allows.  MUL_MAT_ID_BACK's grouped product (its tile
