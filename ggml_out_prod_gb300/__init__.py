@@ -65,6 +65,7 @@ EXPORTS = (
     "oop_last_cuda_error", "oop_out_prod_noalloc", "oop_out_prod_noalloc_scratch_bytes",
     "oop_profile_main_kernel", "oop_out_prod_workspace_min_size", "oop_debug_set_tc_schedule",
     "oop_last_launch_count", "oop_out_prod_host", "oop_out_prod_host_buffer_size",
+    "oop_out_prod_plan",
 )
 
 
@@ -140,6 +141,9 @@ def lib():
             L.oop_out_prod_host.restype = ctypes.c_int
             L.oop_out_prod_host.argtypes = [_vp, ctypes.c_int, _vp, _vp, _i64p, _i64p, _i64p,
                                             _vp, ctypes.c_size_t, _vp]
+            L.oop_out_prod_plan.restype = ctypes.c_int
+            L.oop_out_prod_plan.argtypes = [ctypes.c_int, _i64p, _i64p, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_size_t, ctypes.POINTER(OopPlan)]
             _lib = L
     return _lib
 
@@ -159,6 +163,36 @@ def _ne(v):
 
 def oop_out_prod_workspace_size(a_type, ne_a, ne_b) -> int:
     return int(lib().oop_out_prod_workspace_size(int(a_type), _ne(ne_a), _ne(ne_b)))
+
+
+class OopPlan(ctypes.Structure):
+    """oop_plan: the kernels an OUT_PROD call would enqueue."""
+    _fields_ = [("path", ctypes.c_int), ("kernel", ctypes.c_int), ("item_m", ctypes.c_int),
+                ("ctas", ctypes.c_int), ("launches", ctypes.c_int)]
+
+
+KERNEL_NONE, KERNEL_SKINNY, KERNEL_SKINNY_TMA = 0, 1, 2
+KERNEL_TC_DATA_PARALLEL, KERNEL_TC_STREAM_K, KERNEL_SIMT = 3, 4, 5
+
+
+def oop_out_prod_plan(a_type, ne_a, ne_b, path, sms, workspace_bytes):
+    """(status, OopPlan) from the library's planner; no device is needed."""
+    plan = OopPlan()
+    rc = lib().oop_out_prod_plan(int(a_type), _ne(ne_a), _ne(ne_b), int(path), int(sms),
+                                 int(workspace_bytes), ctypes.byref(plan))
+    return int(rc), plan
+
+
+def out_prod_plan(a_type, ne_a, ne_b, sms, path=0, workspace_bytes=None) -> dict:
+    """The plan of an OUT_PROD call on a GPU with `sms` SMs (default workspace:
+    oop_out_prod_workspace_size); raises OopError on an argument error."""
+    if workspace_bytes is None:
+        workspace_bytes = oop_out_prod_workspace_size(a_type, ne_a, ne_b)
+    rc, p = oop_out_prod_plan(a_type, ne_a, ne_b, path, sms, workspace_bytes)
+    if rc != 0:
+        raise OopError(rc, "oop_out_prod_plan")
+    return {"path": p.path, "kernel": p.kernel, "item_m": p.item_m, "ctas": p.ctas,
+            "launches": p.launches}
 
 
 def oop_out_prod_workspace_min_size(a_type, ne_a, ne_b) -> int:

@@ -212,6 +212,45 @@ int oop_out_prod(const void *a, int a_type, const float *b, float *dst, const in
                            stream, OOP_PATH_AUTO);
 }
 
+int oop_out_prod_plan(int a_type, const int64_t ne_a[4], const int64_t ne_b[4], int path, int sms,
+                      size_t workspace_bytes, oop_plan *plan) {
+    if (!plan) return OOP_ERR_NULL;
+    *plan = oop_plan{};
+    OutProdShape s = {};
+    int rc = check_out_prod_shape(a_type, ne_a, ne_b, &s);
+    if (rc != OOP_OK) return rc;
+    if (path < OOP_PATH_AUTO || path > OOP_PATH_SIMT) return OOP_ERR_PATH;
+    if (sms < 1) return OOP_ERR_DEVICE;
+    if (s.M * s.N * s.ne12 * s.ne13 == 0) return OOP_OK;          // nothing to do
+    const int chosen = choose_path(s, path);
+    if (chosen == OOP_PATH_SKINNY && !skinny_ok(s)) return OOP_ERR_PATH;
+    const size_t need = workspace_min(s, chosen);
+    if (need > 0 && workspace_bytes < need) return OOP_ERR_WORKSPACE;
+    plan->path = chosen;
+    if (s.K == 0) return OOP_OK;                                   // one memset
+    switch (chosen) {
+    case OOP_PATH_SKINNY:
+        if (skinny_tma_shape_ok(s, sms)) {
+            plan->kernel = OOP_KERNEL_SKINNY_TMA;
+            plan->item_m = static_cast<int>(skinny_tma_tile_m(s, sms));
+        } else {
+            plan->kernel = OOP_KERNEL_SKINNY;
+        }
+        plan->launches = 1;
+        break;
+    case OOP_PATH_TCGEN05:
+        plan->ctas = tc_plan_ctas(s, sms, workspace_bytes);
+        plan->kernel = plan->ctas > 0 ? OOP_KERNEL_TC_STREAM_K : OOP_KERNEL_TC_DATA_PARALLEL;
+        plan->launches = plan->ctas > 0 ? 3 : 2;
+        break;
+    default:
+        plan->kernel = OOP_KERNEL_SIMT;
+        plan->launches = 1;
+        break;
+    }
+    return OOP_OK;
+}
+
 }  // extern "C"
 
 namespace oop {

@@ -1185,6 +1185,14 @@ void tc_set_profile_events(cudaEvent_t before, cudaEvent_t after) {
 
 size_t tc_workspace_min_bytes(const OutProdShape &s) { return 2 * split_bytes(s); }
 
+int tc_plan_ctas(const OutProdShape &s, int sms, size_t workspace_bytes) {
+    const int64_t num_kb = (s.K + BK - 1) / BK;
+    if (num_kb <= 0 || num_kb > 0x7fffffffLL) return 0;
+    const size_t split = 2 * split_bytes(s);
+    const size_t room = workspace_bytes > split ? workspace_bytes - split : 0;
+    return plan_ctas(tile_count(s), static_cast<int>(num_kb), sms, room);
+}
+
 size_t tc_workspace_bytes(const OutProdShape &s) {
     const int64_t iters = tile_count(s) * ((s.K + BK - 1) / BK);
     const int64_t ctas = std::min<int64_t>(kSkMaxCtas, iters);
@@ -1235,8 +1243,7 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     p.inject = g_inject;
     g_inject = 0;
     const int64_t tiles = mtiles * ntiles * slices;
-    const size_t room = workspace_bytes > 2 * one ? workspace_bytes - 2 * one : 0;
-    p.ctas = plan_ctas(tiles, p.num_kb, device_sms(), room);
+    p.ctas = tc_plan_ctas(s, device_sms(), workspace_bytes);
     p.iters = tiles * p.num_kb;
     p.partial = partial;
     const dim3 grid = p.ctas > 0 ? dim3(static_cast<unsigned>(p.ctas))

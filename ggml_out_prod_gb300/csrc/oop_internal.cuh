@@ -60,6 +60,10 @@ cudaError_t launch_skinny(const float *a, const float *b, float *dst,
 // Its persistent TMA-fed form for large problems (N % 4 == 0, M % 4 == 0,
 // 16-byte aligned a and b, at least two m-tile x slice items per SM).
 bool skinny_tma_ok(const float *a, const float *b, const OutProdShape &s);
+// The shape part of that rule on a GPU with `sms` SMs (no device calls), and
+// the m-width of its items: 128, 64, or 0 when the form does not apply.
+bool skinny_tma_shape_ok(const OutProdShape &s, int sms);
+int64_t skinny_tma_tile_m(const OutProdShape &s, int sms);
 cudaError_t launch_skinny_tma(const float *a, const float *b, float *dst,
                               const OutProdShape &s, int *status, cudaStream_t stream);
 
@@ -79,6 +83,9 @@ size_t tc_workspace_min_bytes(const OutProdShape &s);
 void tc_set_inject(int v);   // test hook: the next tensor-core launch drops one TMA stage
 void tc_set_schedule(int v); // test hook: 0 automatic, 1 data-parallel, 2 stream-K
 void tc_set_profile_events(cudaEvent_t before, cudaEvent_t after);
+// The tile kernel's schedule on a GPU with `sms` SMs and this much workspace
+// (no device calls): the stream-K CTA count, 0 for data-parallel.
+int tc_plan_ctas(const OutProdShape &s, int sms, size_t workspace_bytes);
 cudaError_t launch_dense_tc(const void *a, const float *b, float *dst,
                             const OutProdShape &s, void *workspace, size_t workspace_bytes,
                             int *status, cudaStream_t stream);

@@ -373,7 +373,7 @@ cudaError_t launch_tma(const float *a, const float *b, float *dst, const OutProd
 // Items of 128 m (four m per lane) up to N = 24, of 64 m above; N = 20 and
 // 24 fall back to 64 when 128-wide items would leave fewer than two per SM.
 // 0: the persistent form does not apply (fewer than two items per SM).
-static int64_t tma_tile_m(const OutProdShape &s, int sms) {
+int64_t skinny_tma_tile_m(const OutProdShape &s, int sms) {
     const int64_t slices = s.ne12 * s.ne13;
     const int64_t need = 2LL * sms;
     if (s.N <= 24 && (s.M + 127) / 128 * slices >= need) return 128;
@@ -381,17 +381,20 @@ static int64_t tma_tile_m(const OutProdShape &s, int sms) {
     return 0;
 }
 
+bool skinny_tma_shape_ok(const OutProdShape &s, int sms) {
+    return sms > 0 && s.N % 4 == 0 && s.M % 4 == 0 && s.K * s.ne02 * s.ne03 < (1LL << 31) &&
+           s.K < (1LL << 31) && skinny_tma_tile_m(s, sms) > 0;
+}
+
 bool skinny_tma_ok(const float *a, const float *b, const OutProdShape &s) {
-    const int sms = device_sm_count();
-    return sms > 0 && s.N % 4 == 0 && s.M % 4 == 0 && reinterpret_cast<uintptr_t>(a) % 16 == 0 &&
-           reinterpret_cast<uintptr_t>(b) % 16 == 0 && s.K * s.ne02 * s.ne03 < (1LL << 31) &&
-           s.K < (1LL << 31) && tma_tile_m(s, sms) > 0;
+    return reinterpret_cast<uintptr_t>(a) % 16 == 0 && reinterpret_cast<uintptr_t>(b) % 16 == 0 &&
+           skinny_tma_shape_ok(s, device_sm_count());
 }
 
 cudaError_t launch_skinny_tma(const float *a, const float *b, float *dst, const OutProdShape &s,
                               int *status, cudaStream_t stream) {
     const int sms = device_sm_count();
-    const bool wide = tma_tile_m(s, sms) == 128;
+    const bool wide = skinny_tma_tile_m(s, sms) == 128;
     switch (s.N) {
     case 4: return launch_tma<4, 4>(a, b, dst, s, status, sms, stream);
     case 8: return launch_tma<8, 4>(a, b, dst, s, status, sms, stream);

@@ -239,6 +239,35 @@ int oop_profile_main_kernel(void *before, void *after);
  * that one launch.  Returns OOP_OK. */
 int oop_debug_inject_timeout(int enable);
 
+/* The kernels an OUT_PROD call would enqueue, decided by the same host rules
+ * as oop_out_prod_ex (no counterpart on the pages; nothing runs and no device
+ * is needed): for a GPU with `sms` SMs, `workspace_bytes` of workspace and
+ * 16-byte aligned a and b.  The tile schedule follows
+ * oop_debug_set_tc_schedule like the calls do. */
+typedef enum {
+    OOP_KERNEL_NONE = 0,             /* empty dst: nothing; K == 0: one memset of dst */
+    OOP_KERNEL_SKINNY = 1,           /* register-pipelined skinny-N kernel */
+    OOP_KERNEL_SKINNY_TMA = 2,       /* persistent, TMA-fed skinny-N kernel */
+    OOP_KERNEL_TC_DATA_PARALLEL = 3, /* split of src1, then one 128 x 96 dst tile per CTA */
+    OOP_KERNEL_TC_STREAM_K = 4,      /* split of src1, stream-K tile kernel, fix-up */
+    OOP_KERNEL_SIMT = 5              /* CUDA-core tiled kernel */
+} oop_kernel;
+
+typedef struct {
+    int path;     /* OOP_PATH_SKINNY / _TCGEN05 / _SIMT; 0 (AUTO) when dst is empty */
+    int kernel;   /* an oop_kernel */
+    int item_m;   /* OOP_KERNEL_SKINNY_TMA: m columns per work item (128 or 64), else 0 */
+    int ctas;     /* OOP_KERNEL_TC_STREAM_K: CTAs sharing the tile x k-block iterations, else 0 */
+    int launches; /* kernels the call enqueues (as oop_last_launch_count reports) */
+} oop_plan;
+
+/* Fills *plan.  Returns OOP_OK, the argument errors of oop_out_prod_ex (shape,
+ * type, broadcast, path, OOP_ERR_WORKSPACE when workspace_bytes is below the
+ * chosen path's minimum), OOP_ERR_NULL for a NULL plan, or OOP_ERR_DEVICE
+ * when sms < 1. */
+int oop_out_prod_plan(int a_type, const int64_t ne_a[4], const int64_t ne_b[4], int path,
+                      int sms, size_t workspace_bytes, oop_plan *plan);
+
 /* Test hook (no counterpart on the pages): the schedule of the tensor-core
  * OUT_PROD tile kernel for the calls that follow on this process.  mode 0 =
  * automatic (the default: stream-K when an even share of the tile x k-block
