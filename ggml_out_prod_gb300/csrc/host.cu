@@ -158,7 +158,7 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
     // copy stream: src1 chunk c in, then (once product c is done) dst chunk c out
     // compute (caller's) stream: product c once its src1 chunk is in
     int launches = 0;
-    for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+    for (int c = 0; c < chunks && e == cudaSuccess && rc == OOP_OK; ++c) {
         const int64_t nc = nb[c + 1] - nb[c];
         float *bc = b_dev + K * nb[c];                          // [K][nc] contiguous
         e = cudaMemcpy2DAsync(bc, nc * 4, b_host + nb[c], N * 4, nc * 4, K,
@@ -170,20 +170,25 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
         const int64_t ne_dc[4] = {M, nc, 1, 1};
         rc = oop_out_prod(a_dev, a_type, bc, dst_dev + nb[c] * M, ne_a, ne_bc, ne_dc, ws,
                           L.ws_bytes, stream);
-        if (rc != OOP_OK) return rc;
+        if (rc != OOP_OK) break;
         launches += g_kernel_launches;
         e = cudaEventRecord(ev[1 + kMaxChunks + c], st);
     }
-    for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+    for (int c = 0; c < chunks && e == cudaSuccess && rc == OOP_OK; ++c) {
         e = cudaStreamWaitEvent(cs, ev[1 + kMaxChunks + c], 0);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(dst_host + nb[c] * M, dst_dev + nb[c] * M,
                                 static_cast<size_t>((nb[c + 1] - nb[c]) * M) * 4,
                                 cudaMemcpyDeviceToHost, cs);
     }
-    if (e == cudaSuccess) e = cudaEventRecord(ev[2 * kMaxChunks + 1], cs);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[2 * kMaxChunks + 1], 0);
-    g_kernel_launches = launches;
+    // Whatever failed, the caller's stream is made to wait for every copy
+    // already enqueued on the copy stream, so that synchronising it still
+    // means no copy touches the caller's buffers any more.
+    cudaError_t j = cudaEventRecord(ev[2 * kMaxChunks + 1], cs);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(st, ev[2 * kMaxChunks + 1], 0);
+    g_kernel_launches = rc == OOP_OK && e == cudaSuccess ? launches : 0;
+    if (rc != OOP_OK) return rc;
+    if (e == cudaSuccess) e = j;
     return rc_of(e);
 }
 
