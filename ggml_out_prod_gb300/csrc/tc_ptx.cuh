@@ -292,10 +292,6 @@ __device__ __forceinline__ void tmem_ld16x2_wait(uint32_t ta, uint32_t (&a)[16],
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
