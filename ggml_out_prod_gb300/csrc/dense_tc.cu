@@ -64,6 +64,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "oop_internal.cuh"
@@ -1067,8 +1068,9 @@ int64_t padded_k(int64_t K) { return (K + 3) / 4 * 4; }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-int g_inject = 0;
-int g_schedule = 0;     // test hook: 0 automatic, 1 data-parallel, 2 stream-K
+// test hooks, set from any host thread
+std::atomic<int> g_inject{0};     // the next launch drops one TMA stage
+std::atomic<int> g_schedule{0};   // 0 automatic, 1 data-parallel, 2 stream-K
 thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 
 // Stream-K uses at most this many CTAs (one per SM); its partial slots are
@@ -1240,8 +1242,7 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     p.num_kb = static_cast<int>((s.K + BK - 1) / BK);
     p.mtiles = static_cast<int>(mtiles);
     p.ntiles = static_cast<int>(ntiles);
-    p.inject = g_inject;
-    g_inject = 0;
+    p.inject = g_inject.exchange(0);
     const int64_t tiles = mtiles * ntiles * slices;
     p.ctas = tc_plan_ctas(s, device_sms(), workspace_bytes);
     p.iters = tiles * p.num_kb;
