@@ -10,14 +10,15 @@
 //  * a TMA warp streams each item's src0 rows (boxes of 64 k x TM m, zero
 //    filled past M) and the matching rows of src1 (64 k x N words, one bulk
 //    copy) through a ring of shared-memory stages, independently of the
-//    consumers, so several stages (~34 KB each) stay in flight per SM and the
-//    next item's rows arrive while the current one is being reduced;
+//    consumers, so several stages (17-41 KB each) stay in flight per SM and
+//    the next item's rows arrive while the current one is being reduced;
 //  * eight consumer warps split each stage's 64 k rows (8 each); lane = VW
 //    consecutive m, N*VW fp32 accumulators per thread held as (n, n+1)
 //    pairs and updated with packed f32x2 FMAs (half the issue slots of
 //    scalar FMAs; the same round-to-nearest products and sums), b read as
-//    broadcast float4s; in a full stage each row's loads are issued before
-//    the previous row's FMAs;
+//    broadcast float4s; in a full stage, where the registers allow (N <= 20
+//    at four m per lane), each row's loads are issued before the previous
+//    row's FMAs;
 //  * at the end of an item warps 4-7 hand their partials to warps 0-3
 //    through shared memory, then warps 0-3 publish theirs and one thread per
 //    output adds the four in warp order and writes dst: deterministic, one
@@ -26,7 +27,8 @@
 // memory delivers 4 bytes per wavefront whatever the load width, so a row
 // costs N wavefronts for src1 against VW for src0: four m per lane (TM = 128)
 // halves that cost per byte against two; N = 28 and 32 keep two m per lane
-// (four would not fit in the registers).
+// (four would not fit in the registers), and so do N = 20 and 24 when items
+// of 128 m would leave fewer than two per SM.
 // Waits are bounded like the tensor-core kernel's: running out records
 // OOP_ERR_DEVICE_TIMEOUT, every role stops, the TMA warp drains its copies.
 #include <algorithm>
