@@ -622,8 +622,16 @@ __global__ void __maxnreg__(MAX_REGS)
             uint32_t hi[KH], lo[KH];
 #pragma unroll
             for (int e = 0; e < KH; e += 2) {
-                hi[e] = ptx::tf32_round_bits(__float_as_uint(x[e]));
-                hi[e + 1] = ptx::tf32_round_bits(__float_as_uint(x[e + 1]));
+                // f32 src0 may hold any finite value: the saturating form
+                // keeps fp32's top binade finite; dequantised and bf16 values
+                // never reach it
+                if constexpr (TYPE == OOP_TYPE_F32) {
+                    hi[e] = ptx::tf32_round_bits_sat(__float_as_uint(x[e]));
+                    hi[e + 1] = ptx::tf32_round_bits_sat(__float_as_uint(x[e + 1]));
+                } else {
+                    hi[e] = ptx::tf32_round_bits(__float_as_uint(x[e]));
+                    hi[e + 1] = ptx::tf32_round_bits(__float_as_uint(x[e + 1]));
+                }
                 // x - hi is exact in fp32 (two elements per instruction)
                 float r0, r1;
                 ptx::unpack2(ptx::sub2(ptx::pack2(x[e], x[e + 1]),

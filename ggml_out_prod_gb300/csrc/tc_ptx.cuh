@@ -323,17 +323,34 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
 
 // Round an fp32 bit pattern to the nearest TF32 value, ties away from zero:
 // add half of the lowest kept bit (bit 13) to the magnitude, clear the 13
-// dropped bits.  Exact integer arithmetic on the full-rate ALU; valid for
-// every finite x below 2^128 * (1 - 2^-12) in magnitude.
+// dropped bits.  Exact integer arithmetic on the full-rate ALU.  Only for
+// values below (2 - 2^-11) * 2^127 in magnitude (a dequantised q8_0 / q4_0
+// element, at most 65504 * 127, always is): above that the carry reaches the
+// exponent and the result is +-Inf.
 __device__ __forceinline__ uint32_t tf32_round_bits(uint32_t xb) {
     return (xb + 0x1000u) & 0xFFFFE000u;
 }
 
+// The same rounding for any finite fp32 value: where rounding to nearest
+// would carry into the all-ones exponent (the top 2^-11 of fp32's top
+// binade), the result is the largest finite TF32 value of x's sign instead,
+// which is x with its 13 low bits cleared.  As unsigned integers, every
+// finite value of one sign lies at or below that limit and the carried
+// +-Inf pattern lies above it, so one unsigned minimum does it.  A NaN or
+// Inf x also comes out finite here; the remainder x - hi is then NaN or Inf,
+// so a split of a non-finite value still carries it.
+__device__ __forceinline__ uint32_t tf32_round_bits_sat(uint32_t xb) {
+    const uint32_t r = (xb + 0x1000u) & 0xFFFFE000u;
+    const uint32_t limit = (xb & 0x80000000u) | 0x7F7FE000u;
+    return r < limit ? r : limit;
+}
+
 // x = hi + lo + r with hi, lo TF32 (low 13 bits zero): hi = x rounded to
-// nearest TF32, lo = (x - hi) rounded to nearest TF32 (x - hi is exact in
-// f32), |r| <= 2^-22 |x|.  Never passes through a 16-bit format.
+// nearest TF32 (saturating, so every finite x gives a finite hi), lo = (x -
+// hi) rounded to nearest TF32 (x - hi is exact in f32 and far below the
+// top binade), |r| <= 2^-22 |x|.  Never passes through a 16-bit format.
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    hi = tf32_round_bits(__float_as_uint(x));
+    hi = tf32_round_bits_sat(__float_as_uint(x));
     const float rest = x - __uint_as_float(hi);
     lo = tf32_round_bits(__float_as_uint(rest));
 }
