@@ -5,6 +5,7 @@
 // contract ("metal: OUT_PROD runs batched, broadcast and narrow shapes on the
 // GPU", review comment, first bullet): dst = {a.ne0, b.ne0, b.ne2, b.ne3},
 // b.ne2 % a.ne2 == 0 and b.ne3 % a.ne3 == 0.
+#include <atomic>
 #include <mutex>
 
 #include "oop_internal.cuh"
@@ -12,6 +13,26 @@
 namespace oop {
 
 thread_local int g_kernel_launches = 0;
+
+namespace {
+constexpr int kSmCacheDevices = 64;
+std::atomic<int> g_sm_count[kSmCacheDevices];   // 0 = not yet queried
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= kSmCacheDevices) {
+        int v = 0;
+        return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? v : 0;
+    }
+    int v = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        return 0;
+    g_sm_count[dev].store(v, std::memory_order_relaxed);   // every thread stores the same value
+    return v;
+}
 
 namespace {
 
@@ -115,6 +136,28 @@ size_t workspace_min(const OutProdShape &s, int path) {
 }
 
 thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+}  // namespace
+
+int out_prod_check_shape(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
+    OutProdShape s = {};
+    return check_out_prod_shape(a_type, ne_a, ne_b, &s);
+}
+
+int out_prod_auto_workspace(int a_type, const int64_t ne_a[4], const int64_t ne_b[4],
+                            size_t *min_bytes, size_t *full_bytes) {
+    *min_bytes = *full_bytes = 0;
+    OutProdShape s = {};
+    const int rc = check_out_prod_shape(a_type, ne_a, ne_b, &s);
+    if (rc != OOP_OK) return rc;
+    if (choose_path(s, OOP_PATH_AUTO) == OOP_PATH_TCGEN05) {
+        *min_bytes = tc_workspace_min_bytes(s);
+        *full_bytes = tc_workspace_bytes(s);
+    }
+    return OOP_OK;
+}
+
+namespace {
 
 int cuda_rc(cudaError_t e) {
     if (e == cudaSuccess) return OOP_OK;

@@ -1086,18 +1086,7 @@ thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 constexpr int kSkMaxCtas = 160;
 constexpr size_t kSlotBytes = size_t(BM) * BN * 4;
 
-int device_sms() {
-    static int cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!cached[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return 0;
-        cached[dev] = n;
-    }
-    return cached[dev];
-}
+int device_sms() { return device_sm_count(); }
 
 // Stream-K or data-parallel for `tiles` tiles of `num_kb` k-blocks on `sms`
 // SMs.  Returns the stream-K CTA count, 0 for data-parallel.  Stream-K pays

@@ -97,8 +97,7 @@ extern "C" {
 size_t oop_out_prod_host_buffer_size(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
     if (!ne_a || !ne_b) return 0;
     HostLayout L;
-    if (oop_out_prod_workspace_min_size(a_type, ne_a, ne_b) == 0 ||
-        !plan_host(a_type, ne_a, ne_b, &L))
+    if (out_prod_check_shape(a_type, ne_a, ne_b) != OOP_OK || !plan_host(a_type, ne_a, ne_b, &L))
         return 0;
     return L.total;
 }

@@ -55,13 +55,16 @@ size_t oop_out_prod_noalloc_scratch_bytes(void) { return oop::kScratchBytes; }
 int oop_out_prod_noalloc(const void *a, int a_type, const float *b, float *dst,
                          const int64_t ne_a[4], const int64_t ne_b[4], const int64_t ne_dst[4],
                          void *stream) {
-    // Shape errors are reported exactly as oop_out_prod reports them.  The
-    // call needs at least the minimum workspace; whatever of the array is
-    // beyond that lets the tensor-core path pick its stream-K schedule.
-    const size_t need = oop_out_prod_workspace_min_size(a_type, ne_a, ne_b);
+    // The scratch the kernel oop_out_prod chooses needs: none for the skinny-N
+    // kernel (f32 src0, N <= 32), else the tensor-core minimum, with whatever
+    // of the array lies beyond it letting that kernel pick its stream-K
+    // schedule.  Shape errors are left to oop_out_prod, which reports them
+    // exactly as it always does.
+    size_t need = 0, full = 0;
+    if (oop::out_prod_auto_workspace(a_type, ne_a, ne_b, &need, &full) != OOP_OK)
+        return oop_out_prod(a, a_type, b, dst, ne_a, ne_b, ne_dst, nullptr, 0, stream);
     if (need > oop::kScratchBytes) return OOP_ERR_SCRATCH_LIMIT;
-    size_t give = oop_out_prod_workspace_size(a_type, ne_a, ne_b);
-    if (give > oop::kScratchBytes) give = oop::kScratchBytes;
+    const size_t give = full < oop::kScratchBytes ? full : oop::kScratchBytes;
     void *scratch = nullptr;
     if (give > 0) {
         const int rc = oop::scratch_for_current_device(&scratch);

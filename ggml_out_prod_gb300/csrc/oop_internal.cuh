@@ -75,6 +75,21 @@ cudaError_t launch_dense_simt(const void *a, const float *b, float *dst,
 // adds its own).
 extern thread_local int g_kernel_launches;
 
+// SM count of the current device, queried once per device (0 on failure).
+// Safe to call from several host threads at once.
+int device_sm_count();
+
+// The OUT_PROD shape contract as oop_out_prod checks it (OOP_OK or the
+// status it would return for these sizes and type).
+int out_prod_check_shape(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]);
+
+// The workspace of the kernel oop_out_prod would choose for these sizes: the
+// least it runs with and the size that lets it pick its fastest schedule
+// (both 0 for the skinny-N kernel, which needs none).  Returns the shape
+// check's status.
+int out_prod_auto_workspace(int a_type, const int64_t ne_a[4], const int64_t ne_b[4],
+                            size_t *min_bytes, size_t *full_bytes);
+
 // Tensor-core OUT_PROD (tcgen05, 3xTF32).  The workspace holds the TF32 split
 // of src1 (the minimum) and, after it, the stream-K partial slots; with less
 // than tc_workspace_bytes the data-parallel schedule is used.

@@ -211,15 +211,8 @@ cudaError_t launch_np(const SkinnyArgs &args0, const OutProdShape &s, cudaStream
 
     // Split K over a cluster of S CTAs: enough CTAs for about two per SM,
     // at least one chunk of rows each.
-    int sms = 152;
-    {
-        int dev = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess) {
-            int v = 0;
-            if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-                sms = v;
-        }
-    }
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 152;
     int S = 1;
     while (S < kMaxCluster && mtiles * slices * (S * 2) <= 2 * sms &&
            (s.K + S * 2 - 1) / (S * 2) >= kChunk)

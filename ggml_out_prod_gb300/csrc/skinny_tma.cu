@@ -323,13 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (timed_out) record_status(p.status, OOP_ERR_DEVICE_TIMEOUT);
 }
 
-int device_sm_count() {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return v;
-}
-
 template <int NP, int VW>
 cudaError_t launch_tma(const float *a, const float *b, float *dst, const OutProdShape &s,
                        int *status, int sms, cudaStream_t stream) {

@@ -16,6 +16,12 @@
  * caller.  The library allocates nothing per call and keeps no state except
  * one status word per device (see oop_device_status).
  *
+ * Device reset: the library looks up the device addresses of its own device
+ * variables (the status word, the scratch of oop_out_prod_noalloc) once per
+ * device and keeps them for the life of the process.  A cudaDeviceReset (or
+ * anything else that destroys the device's primary context) makes those
+ * addresses stale: do not call the library on that device afterwards.
+ *
  * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  * work is enqueued on it in order; no entry point synchronises except
  * oop_device_status.
@@ -156,17 +162,21 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
  * Same operation, arguments, errors and precision as oop_out_prod, minus the
  * workspace: the scratch is a 64 MiB device array inside this library
  * (oop_out_prod_noalloc_scratch_bytes()), present on every GPU that loads the
- * library until the process exits.  A call whose least scratch need
- * (oop_out_prod_workspace_min_size) exceeds it returns OOP_ERR_SCRATCH_LIMIT
- * and enqueues nothing.  The call allocates nothing: no cudaMalloc, cudaFree or
- * allocating library routine.
+ * library until the process exits.  The scratch a call needs is that of the
+ * kernel oop_out_prod picks for it: none for the skinny-N kernel (f32 src0,
+ * N <= 32, any K and slice count), otherwise the tensor-core kernel's
+ * minimum (oop_out_prod_workspace_min_size).  A call needing more than the
+ * array returns OOP_ERR_SCRATCH_LIMIT and enqueues nothing; scratch beyond
+ * the minimum only widens the tensor-core kernel's choice of schedule.  The
+ * call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.
  *
- * The first call on a device looks up that array's device address (once per
- * device, with the device current); make that first call before any stream
- * capture begins.  Every call on a device shares the one array, and each call
- * rewrites all of the scratch it reads, so nothing needs clearing between
- * calls; but two calls that overlap on the GPU (other streams, or another
- * host thread) race on it -- order them on one stream.
+ * The first call on a device that needs scratch looks up that array's
+ * device address (once per device, with the device current); make that first
+ * call before any stream capture begins.  Every call on a device shares the
+ * one array, and each call rewrites all of the scratch it reads, so nothing
+ * needs clearing between calls; but two calls that overlap on the GPU (other
+ * streams, or another host thread) race on it -- order them on one stream.
  */
 size_t oop_out_prod_noalloc_scratch_bytes(void);
 

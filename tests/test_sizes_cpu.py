@@ -76,3 +76,17 @@ def test_mul_mat_id_back_workspace():
     assert op.oop_mul_mat_id_back_workspace_size(Q8, ne_w, ne_ids) == 0
     assert op.oop_mul_mat_id_back_workspace_size(F32, (2048, 768, 6145), ne_ids) == 0
     assert op.oop_mul_mat_id_back_workspace_size(F32, ne_w, (0, 512)) == 0
+
+
+@pytest.mark.parametrize("a_type,ne_a,ne_b", [
+    (F32, (256, 0, 1, 1), (8, 0, 1, 1)),          # skinny-N shape, empty sum
+    (Q8, (512, 0, 1, 1), (300, 0, 1, 1)),         # tensor-core shape, empty sum
+    (F32, (128, 0, 2, 1), (70, 0, 4, 3)),         # broadcast, empty sum
+])
+def test_host_buffer_empty_sum(a_type, ne_a, ne_b):
+    """K == 0 is a valid call (dst is zero-filled, then copied out): the host
+    entry still needs room for dst, although no workspace."""
+    assert op.oop_out_prod_workspace_min_size(a_type, ne_a, ne_b) == 0
+    _, _, dst = _bytes(a_type, ne_a, ne_b)
+    total = op.oop_out_prod_host_buffer_size(a_type, ne_a, ne_b)
+    assert dst <= total <= dst + 4 * 255
