@@ -2,17 +2,30 @@
 """Benchmark: OUT_PROD / MUL_MAT_ID_BACK on one GB300 (or N replicas).
 
 One step is one pass of the hot path over one batch of synthetic input.  The
-headline workload is the dense training OUT_PROD through a frozen quantised
-weight: a = q8_0 of a N(0, 0.02) [5120, 5120] matrix, b = an f32 gradient
-[1024, 5120] ~ N(0,1)*1e3 with 0.2% outliers of magnitude U(6.6e4, 1.5e5);
-`value` is its algorithmic TFLOP/s (2*M*N*K per call).  The same line carries
-`parts`: the other rows of the path measured in the same run (rank-r LoRA
-gradient GB/s, grouped-head broadcast, MUL_MAT_ID_BACK).
+headline workload is the largest dense training OUT_PROD through a frozen
+quantised weight: a = q8_0 of a N(0, 0.02) [5120, 17408] matrix, b = an f32
+gradient [1024, 17408] ~ N(0,1)*1e3 with 0.2% outliers of magnitude
+U(6.6e4, 1.5e5); `value` is its algorithmic TFLOP/s (2*M*N*K per call).  The
+same line carries `parts`: the other rows of the path measured in the same run
+(rank-r LoRA gradient GB/s, grouped-head broadcast, the other dense shapes,
+MUL_MAT_ID_BACK), each with its own roofline.
 
-Timing: W warm-up steps, then K timed steps; before every timed step a 512 MB
-buffer is written to flush L2 (129 MB); each step is bracketed by CUDA events
-on the launching stream.  With torchrun each rank runs an independent replica
-(no data-path collective); rank 0 prints the max over ranks.
+Timing: W warm-up steps, then K timed steps, each bracketed by CUDA events on
+the launching stream, each preceded by a ~100 us device-side wait so that the
+host has enqueued the step before the GPU reaches it.  No L2 flush is written: the headline's inputs (166 MB)
+are larger than L2 (129 MB), and every smaller workload rotates through
+ceil(2 * L2 / bytes) + 1 copies of its inputs and outputs, so each call reads
+data that the previous calls have evicted.  With torchrun each rank runs an
+independent replica (no data-path collective); rank 0 prints the max over
+ranks.
+
+Roofline of the dense kernels: tensor-pipe utilisation, i.e. the TF32 tensor
+work of the 3xTF32 scheme (three TF32 products per multiply-add, 3 * 2MNK
+flops) per second over the dense TF32 peak measured in the same run (cuBLAS
+TF32 GEMM 8192^3, best of 10); the algorithmic 2MNK/t is printed beside it.
+Skinny rank-r kernels: algorithmic bytes per second over the measured HBM
+copy bandwidth.  MUL_MAT_ID_BACK: the larger of its HBM and tensor-pipe times
+over the measured time.
 
 `--impl reference` times the CPU oracle on a bounded sample of the same
 workload on the host's cores (there is no other implementation to run).
@@ -21,7 +34,9 @@ workload on the host's cores (there is no other implementation to run).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -38,16 +53,32 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "OUT_PROD TFLOP/s (dense) and GB/s (rank-r) on 1 GB300, % of roofline"
-DENSE_M, DENSE_K, DENSE_N = 5120, 5120, 1024
+DENSE_M, DENSE_K, DENSE_N = 5120, 17408, 1024
 WORKLOAD = (f"dense OUT_PROD q8_0 x f32 m{DENSE_M} k{DENSE_K} n{DENSE_N} "
             "(frozen quantised weight, gradient with 0.2% outliers to 1.5e5)")
-L2_FLUSH_BYTES = 512 << 20
-NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense ratio
+L2_BYTES = 129 << 20
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense ratio (context only)
 # DRAM bytes (read + write) of one launch of the tensor-core tile kernel on the
 # headline workload, from the ncu capture summarised in
-# profiles/tc_out_prod_q8_m5120_k5120_n1024.md; None while that capture does
-# not match the kernel in this tree.
-TC_TRAFFIC_BYTES = 83_122_688
+# profiles/tc_out_prod_q8_m5120_k17408_n1024.md, and the digest of the kernel
+# sources it was taken on: the figure is reported only while the sources in
+# this tree still hash to that digest (null once the kernel has changed).
+TC_TRAFFIC = {"bytes": None, "sources_sha256": None}
+TC_SOURCES = ("ggml_out_prod_gb300/csrc/dense_tc.cu", "ggml_out_prod_gb300/csrc/tc_ptx.cuh")
+
+
+def _sources_digest():
+    h = hashlib.sha256()
+    for rel in TC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic():
+    if TC_TRAFFIC["bytes"] is None or TC_TRAFFIC["sources_sha256"] != _sources_digest():
+        return None
+    return TC_TRAFFIC["bytes"]
 
 
 def _peaks():
@@ -59,6 +90,15 @@ def _peaks():
     except OSError:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
             "fallback"
+
+
+def rotation_sets(bytes_per_set):
+    """Copies of a workload's inputs and outputs to cycle through so that
+    every call reads HBM, not L2: ceil(2 * L2 / bytes) + 1 (1 once one set is
+    larger than twice L2)."""
+    if bytes_per_set >= 2 * L2_BYTES:
+        return 1
+    return int(math.ceil(2 * L2_BYTES / bytes_per_set)) + 1
 
 
 # ---------------------------------------------------------------------------
@@ -125,38 +165,35 @@ class ClockSampler:
 # the GPU arm
 # ---------------------------------------------------------------------------
 
-class Timer:
-    """Per-step CUDA events on the launching stream, with an L2 flush before
-    each timed step."""
+# A device-side wait of ~100 us enqueued before each timed call: while the
+# GPU runs it the host enqueues the call and its closing event, so the events
+# bracket device time only, not the host's launch overhead (a 10 us kernel
+# costs more than that to launch from Python).  It touches no memory.
+HOST_LEAD_CYCLES = 200_000
 
-    def __init__(self, torch, device):
-        self.torch = torch
-        self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
-    def flush(self):
-        self.flush_buf.fill_(1.0)
+def host_lead(torch):
+    torch.cuda._sleep(HOST_LEAD_CYCLES)
 
-    def run(self, fn, steps, warmup, flush=True):
-        """flush=False only for inputs larger than L2, which evict themselves."""
-        torch = self.torch
-        for _ in range(warmup):
-            if flush:
-                self.flush()
-            fn()
-        torch.cuda.synchronize()
-        stream = torch.cuda.current_stream()
-        evs = []
-        for _ in range(steps):
-            if flush:
-                self.flush()
-            s = torch.cuda.Event(enable_timing=True)
-            e = torch.cuda.Event(enable_timing=True)
-            s.record(stream)
-            fn()
-            e.record(stream)
-            evs.append((s, e))
-        torch.cuda.synchronize()
-        return [s.elapsed_time(e) for s, e in evs]
+
+def time_rotating(torch, calls, steps, warmup):
+    """Per-call CUDA-event times (ms) on the current stream, cycling through
+    `calls` (one per rotation set), after `warmup` untimed calls."""
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        calls[i % len(calls)]()
+    torch.cuda.synchronize()
+    evs = []
+    for i in range(steps):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        host_lead(torch)
+        s.record(stream)
+        calls[(warmup + i) % len(calls)]()
+        e.record(stream)
+        evs.append((s, e))
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
 
 
 def _dist():
@@ -183,7 +220,7 @@ def whole_job_value(ws, flops_per_rank, ms_step_max):
 
 
 def _cublas_tf32(torch, device):
-    """cuBLAS TF32 GEMM throughput (context for the TF32 roofline)."""
+    """Dense TF32 peak: cuBLAS TF32 GEMM 8192^3, best of 10 (TFLOP/s)."""
     prev = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = True
     try:
@@ -194,7 +231,7 @@ def _cublas_tf32(torch, device):
             x @ y
         torch.cuda.synchronize()
         best = float("inf")
-        for _ in range(5):
+        for _ in range(10):
             s = torch.cuda.Event(enable_timing=True)
             e = torch.cuda.Event(enable_timing=True)
             s.record()
@@ -205,6 +242,27 @@ def _cublas_tf32(torch, device):
         return 2.0 * n ** 3 / (best * 1e-3) / 1e12
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def dense_roofline(flops, us, tf32_peak, products=3):
+    """Tensor-pipe utilisation of a 3xTF32 (or 2xTF32) product."""
+    pipe = products * flops / (us * 1e-6) / 1e12
+    return {"bound": "tensor", "achieved": round(pipe, 2), "peak": round(tf32_peak, 1),
+            "unit": "TFLOP/s", "frac": round(pipe / tf32_peak, 4),
+            "algorithmic_TFLOP/s": round(flops / (us * 1e-6) / 1e12, 2)}
+
+
+def hbm_roofline(byts, us, hbm):
+    gbs = byts / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(gbs / hbm, 4)}
+
+
+def bench_config(ws):
+    """The `config` of both arms' lines (the same workload and layout)."""
+    return {"workload": WORKLOAD, "parallelism": f"replicas x{ws}",
+            "l2": "inputs larger than L2 (166 MB), no flush; smaller parts rotate "
+                  "ceil(2*L2/bytes)+1 input sets"}
 
 
 def gpu_arm(args):
@@ -222,18 +280,21 @@ def gpu_arm(args):
     op.build()
     op.lib()
     peaks, peak_kind = _peaks()
-    timer = Timer(torch, device)
+    hbm = peaks["hbm_gbs"]
+    tf32_peak = _cublas_tf32(torch, device)
     clocks = ClockSampler(device.index if device.index is not None else 0)
 
-    # ---- headline: dense q8_0 OUT_PROD -------------------------------------
+    # ---- headline: dense q8_0 OUT_PROD, the largest shape ----------------
     a_np, b_np = synth.dense_quant(synth.TYPE_Q8_0, DENSE_M, DENSE_K, DENSE_N)
     a = torch.from_numpy(a_np).to(device)
     b = torch.from_numpy(b_np).to(device)
-    ne_a = (DENSE_M, DENSE_K, 1, 1)
+    ne_a, ne_b = (DENSE_M, DENSE_K, 1, 1), (DENSE_N, DENSE_K, 1, 1)
     out = torch.empty((1, 1, DENSE_N, DENSE_M), dtype=torch.float32, device=device)
-    nws = op.oop_out_prod_workspace_size(op.TYPE_Q8_0, ne_a, (DENSE_N, DENSE_K, 1, 1))
+    nws = op.oop_out_prod_workspace_size(op.TYPE_Q8_0, ne_a, ne_b)
     ws_buf = torch.empty(max(nws, 1), dtype=torch.uint8, device=device)
     flops = 2.0 * DENSE_M * DENSE_N * DENSE_K
+    in_bytes = a_np.nbytes + b_np.nbytes
+    assert in_bytes > L2_BYTES, "the headline's inputs must be larger than L2"
 
     def dense_call():
         op.out_prod(a, b, a_type=op.TYPE_Q8_0, ne_a=ne_a, out=out, workspace=ws_buf,
@@ -245,7 +306,6 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     clocks.start()
     for _ in range(args.warmup):
-        timer.flush()
         dense_call()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -253,7 +313,6 @@ def gpu_arm(args):
     launches = 0
     t_region0 = time.perf_counter()
     for _ in range(args.steps):
-        timer.flush()
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
         k0 = torch.cuda.Event(enable_timing=True)
@@ -261,6 +320,7 @@ def gpu_arm(args):
         for e in (k0, k1):          # create the events before handing them over
             e.record(stream)
         op.profile_main_kernel(k0, k1)
+        host_lead(torch)
         s0.record(stream)
         dense_call()
         launches += op.last_launch_count()
@@ -281,7 +341,7 @@ def gpu_arm(args):
     a_host = torch.from_numpy(a_np).pin_memory()
     b_host = torch.from_numpy(b_np).pin_memory()
     dst_host = torch.empty((1, 1, DENSE_N, DENSE_M), dtype=torch.float32, pin_memory=True)
-    nbuf = op.oop_out_prod_host_buffer_size(op.TYPE_Q8_0, ne_a, (DENSE_N, DENSE_K, 1, 1))
+    nbuf = op.oop_out_prod_host_buffer_size(op.TYPE_Q8_0, ne_a, ne_b)
     dev_buf = torch.empty(nbuf, dtype=torch.uint8, device=device)
 
     def e2e_call():
@@ -293,36 +353,36 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     e2e_t = []
     for _ in range(args.steps):
-        timer.flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_call()
         e2e_t.append(time.perf_counter() - t0)
     e2e_s = _barrier_max(torch, statistics.mean(e2e_t), ws)
+    del dev_buf, a_host, b_host, dst_host
 
     # ---- the other rows of the path (same run) ----------------------------
     parts = {}
-    hbm = peaks["hbm_gbs"]
+    psteps = max(args.steps, 20)
 
-    def skinny_part(r, steps):
+    def skinny_part(r):
         an, bn = synth.lora_rank(r)
-        ta, tb = torch.from_numpy(an).to(device), torch.from_numpy(bn).to(device)
-        o = torch.empty((1, 1, r, 2560), dtype=torch.float32, device=device)
-        t = timer.run(lambda: op.out_prod(ta, tb, out=o, path=op.PATH_SKINNY), steps, 3)
         byts = 4.0 * (2560 * 512 + r * 512 + 2560 * r)
-        us = statistics.mean(t) * 1e3
+        sets = rotation_sets(byts)
+        ta = [torch.from_numpy(an).to(device) for _ in range(sets)]
+        tb = [torch.from_numpy(bn).to(device) for _ in range(sets)]
+        o = [torch.empty((1, 1, r, 2560), dtype=torch.float32, device=device) for _ in range(sets)]
+        calls = [(lambda i=i: op.out_prod(ta[i], tb[i], out=o[i], path=op.PATH_SKINNY))
+                 for i in range(sets)]
+        us = statistics.mean(time_rotating(torch, calls, psteps, 3)) * 1e3
         return {"workload": f"LoRA rank-{r} gradient: a [2560, 512] f32, b [{r}, 512]",
-                "us": round(us, 3), "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
-                "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / hbm, 4),
-                "frac_of_8TBs": round(byts / (us * 1e-6) / 8e12, 4), "bytes": byts}
+                "us": round(us, 3), "bytes": byts, "rotation_sets": sets,
+                "roofline": hbm_roofline(byts, us, hbm)}
 
     for r in synth.LORA_RANKS:
-        parts[f"lora_r{r}"] = skinny_part(r, max(args.steps, 20))
+        parts[f"lora_r{r}"] = skinny_part(r)
 
-    # rank-r gradients for many slices in one launch (steady-state streaming).
-    # src0 is 335 MB, larger than L2, so these steps need no flush; the
-    # figure after a flush is reported beside it (the flush leaves up to 129 MB
-    # of dirty lines that are written back during the call).
+    # rank-r gradients for many slices in one launch (steady-state streaming;
+    # src0 is 335 MB, larger than twice L2, so one set suffices)
     nsl = 64
     an = synth.make_a(synth.TYPE_F32, (2560, 512, nsl, 1), 70)
     ta = torch.from_numpy(an).to(device)
@@ -331,123 +391,135 @@ def gpu_arm(args):
         bn = synth.make_b((r, 512, nsl, 1), 71, std=100.0, outliers=True)
         tb = torch.from_numpy(bn).to(device)
         o = torch.empty((1, nsl, r, 2560), dtype=torch.float32, device=device)
-        call = (lambda tb=tb, o=o: op.out_prod(ta, tb, out=o, path=op.PATH_SKINNY))
-        t = timer.run(call, max(args.steps, 10), 3, flush=False)
-        tf = timer.run(call, max(args.steps, 10), 3)
         byts = 4.0 * nsl * (2560 * 512 + r * 512 + 2560 * r)
-        us, usf = statistics.mean(t) * 1e3, statistics.mean(tf) * 1e3
+        call = (lambda tb=tb, o=o: op.out_prod(ta, tb, out=o, path=op.PATH_SKINNY))
+        us = statistics.mean(time_rotating(torch, [call], max(args.steps, 10), 3)) * 1e3
         parts[f"lora_r{r}_x64_slices"] = {
             "workload": f"64 rank-{r} gradients in one launch: a [2560, 512, 64] f32, b [{r}, 512, 64]",
-            "us": round(us, 3), "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
-            "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / hbm, 4),
-            "l2": "inputs larger than L2, no flush",
-            "us_after_l2_flush": round(usf, 3),
-            "frac_of_measured_hbm_after_flush": round(byts / (usf * 1e-6) / 1e9 / hbm, 4)}
+            "us": round(us, 3), "bytes": byts, "rotation_sets": rotation_sets(byts),
+            "roofline": hbm_roofline(byts, us, hbm)}
         del tb, o
     del ta
 
     for n_seq in (1, 2):
         an, bn = synth.grouped_heads(n_seq)
-        ta, tb = torch.from_numpy(an).to(device), torch.from_numpy(bn).to(device)
-        o = torch.empty((n_seq, 16, 128, 128), dtype=torch.float32, device=device)
-        t = timer.run(lambda: op.out_prod(ta, tb, out=o), max(args.steps, 20), 3)
-        us = statistics.mean(t) * 1e3
+        byts = an.nbytes + bn.nbytes + 4 * 128 * 128 * 16 * n_seq
+        sets = rotation_sets(byts)
+        ta = [torch.from_numpy(an).to(device) for _ in range(sets)]
+        tb = [torch.from_numpy(bn).to(device) for _ in range(sets)]
+        o = [torch.empty((n_seq, 16, 128, 128), dtype=torch.float32, device=device)
+             for _ in range(sets)]
+        calls = [(lambda i=i: op.out_prod(ta[i], tb[i], out=o[i])) for i in range(sets)]
+        us = statistics.mean(time_rotating(torch, calls, psteps, 3)) * 1e3
         fl = 2.0 * 128 * 128 * 512 * 16 * n_seq
-        # the same slices as one launch per slice (the per-slice loop)
-        o2 = torch.empty_like(o)
 
-        def per_slice():
+        # the same slices as one launch per slice (the per-slice loop)
+        def per_slice(i):
             for i3 in range(n_seq):
                 for i2 in range(16):
-                    op.out_prod(ta[i3, i2 // 4], tb[i3, i2], out=o2[i3, i2], ne_a=(128, 512, 1, 1))
+                    op.out_prod(ta[i][i3, i2 // 4], tb[i][i3, i2], out=o[i][i3, i2],
+                                ne_a=(128, 512, 1, 1))
 
-        t2 = timer.run(per_slice, max(args.steps // 2, 5), 2)
+        loops = [(lambda i=i: per_slice(i)) for i in range(sets)]
+        t2 = time_rotating(torch, loops, max(args.steps // 2, 5), 2)
         parts[f"grouped_heads_x{n_seq}"] = {
             "workload": f"a [128, 512, 4, {n_seq}], b [128, 512, 16, {n_seq}], dps2 = 4",
-            "us_one_launch": round(us, 3), "TFLOP/s": round(fl / (us * 1e-6) / 1e12, 3),
+            "us_one_launch": round(us, 3), "rotation_sets": sets,
             "us_per_slice_loop": round(statistics.mean(t2) * 1e3, 3),
-            "launches_per_slice_loop": 16 * n_seq}
-        del ta, tb, o, o2
+            "launches_per_slice_loop": 16 * n_seq,
+            "roofline": dense_roofline(fl, us, tf32_peak)}
+        del ta, tb, o
 
     # every dense shape, q8_0 and q4_0: whole call and tile kernel alone
     for m, k in synth.DENSE_MK:
         x = synth.normal(synth.tensor_seed(30), m * k, std=0.02).reshape(1, 1, k, m)
         bn = synth.make_b((DENSE_N, k, 1, 1), 31, std=1e3, outliers=True)
-        tb = torch.from_numpy(bn).to(device)
-        o = torch.empty((1, 1, DENSE_N, m), dtype=torch.float32, device=device)
+        fl = 2.0 * m * DENSE_N * k
         wsz = op.oop_out_prod_workspace_size(op.TYPE_Q8_0, (m, k, 1, 1), (DENSE_N, k, 1, 1))
         wsb = torch.empty(max(wsz, 1), dtype=torch.uint8, device=device)
-        fl = 2.0 * m * DENSE_N * k
         for tid, tname, quant in ((synth.TYPE_Q8_0, "q8_0", synth.quantize_q8_0),
                                   (synth.TYPE_Q4_0, "q4_0", synth.quantize_q4_0)):
-            ta = torch.from_numpy(quant(x)).to(device)
+            an = quant(x)
+            byts = an.nbytes + bn.nbytes + 4 * m * DENSE_N
+            sets = rotation_sets(byts)
+            ta = [torch.from_numpy(an).to(device) for _ in range(sets)]
+            tb = [torch.from_numpy(bn).to(device) for _ in range(sets)]
+            o = [torch.empty((1, 1, DENSE_N, m), dtype=torch.float32, device=device)
+                 for _ in range(sets)]
 
-            def call():
-                op.out_prod(ta, tb, a_type=tid, ne_a=(m, k, 1, 1), out=o, workspace=wsb,
+            def call(i):
+                op.out_prod(ta[i], tb[i], a_type=tid, ne_a=(m, k, 1, 1), out=o[i], workspace=wsb,
                             path=op.PATH_TCGEN05)
 
-            for _ in range(3):
-                timer.flush()
-                call()
+            for i in range(3):
+                call(i % sets)
             torch.cuda.synchronize()
             rec = []
-            for _ in range(max(3, args.steps // 4)):
-                timer.flush()
+            for i in range(max(3, args.steps // 4)):
                 ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
                 ev[2].record(stream)
                 ev[3].record(stream)
                 op.profile_main_kernel(ev[2], ev[3])
+                host_lead(torch)
                 ev[0].record(stream)
-                call()
+                call((3 + i) % sets)
                 ev[1].record(stream)
                 rec.append(ev)
             torch.cuda.synchronize()
             us_call = statistics.mean(e[0].elapsed_time(e[1]) for e in rec) * 1e3
             us_kern = statistics.mean(e[2].elapsed_time(e[3]) for e in rec) * 1e3
-            peak_tf32 = peaks["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
             parts[f"dense_{tname}_m{m}_k{k}_n{DENSE_N}"] = {
                 "us_call": round(us_call, 2), "us_tile_kernel": round(us_kern, 2),
                 "TFLOP/s_call": round(fl / (us_call * 1e-6) / 1e12, 2),
-                "TFLOP/s_tile_kernel": round(fl / (us_kern * 1e-6) / 1e12, 2),
-                "pipe_frac_3xtf32": round(3 * fl / (us_kern * 1e-6) / 1e12 / peak_tf32, 4)}
-            del ta
-        del tb, o, wsb, x
+                "rotation_sets": sets,
+                "roofline": dense_roofline(fl, us_kern, tf32_peak)}
+            del ta, tb, o
+        del wsb, x, bn
 
     for wt, nm in ((synth.TYPE_F32, "f32"), (synth.TYPE_BF16, "bf16")):
         W, ids, g = synth.moe_back(wt)
-        tW = torch.from_numpy(W.view(np.int16) if wt == synth.TYPE_BF16 else W).to(device)
-        tids, tg = torch.from_numpy(ids).to(device), torch.from_numpy(g).to(device)
-        o = torch.empty((512, 8, 2048), dtype=torch.float32, device=device)
-        wsz = op.oop_mul_mat_id_back_workspace_size(wt, (2048, 768, 32), (8, 512))
-        wsb = torch.empty(max(wsz, 1), dtype=torch.uint8, device=device)
+        Wt = W.view(np.int16) if wt == synth.TYPE_BF16 else W
         fl = 2.0 * 2048 * 768 * 8 * 512
         byts = W.nbytes + g.nbytes + 4.0 * 2048 * 8 * 512 + ids.nbytes
-        entry = {"workload": f"E=32 W {nm} [2048, 768], 8 of 32 experts per token, 512 tokens"}
+        sets = rotation_sets(byts)
+        tW = [torch.from_numpy(Wt).to(device) for _ in range(sets)]
+        tids = [torch.from_numpy(ids).to(device) for _ in range(sets)]
+        tg = [torch.from_numpy(g).to(device) for _ in range(sets)]
+        o = [torch.empty((512, 8, 2048), dtype=torch.float32, device=device) for _ in range(sets)]
+        wsz = op.oop_mul_mat_id_back_workspace_size(wt, (2048, 768, 32), (8, 512))
+        wsb = torch.empty(max(wsz, 1), dtype=torch.uint8, device=device)
+        # roof: the larger of the HBM time and the tensor-pipe time (three
+        # TF32 products per multiply-add for f32 W, two for bf16 W)
+        products = 3 if wt == synth.TYPE_F32 else 2
+        roof_us = max(byts / (hbm * 1e9), products * fl / (tf32_peak * 1e12)) * 1e6
+        entry = {"workload": f"E=32 W {nm} [2048, 768], 8 of 32 experts per token, 512 tokens",
+                 "bytes": byts, "rotation_sets": sets, "roof_us": round(roof_us, 2)}
         for path, pname in ((op.PATH_TCGEN05, "grouped_tcgen05"), (op.PATH_SIMT, "per_slot")):
-            t = timer.run(lambda: op.mul_mat_id_back(tW, tids, tg, w_type=wt, out=o, workspace=wsb,
-                                                     path=path), max(3, args.steps // 4), 2)
-            us = statistics.mean(t) * 1e3
+            calls = [(lambda i=i, path=path: op.mul_mat_id_back(
+                tW[i], tids[i], tg[i], w_type=wt, out=o[i], workspace=wsb, path=path))
+                for i in range(sets)]
+            n = psteps if path == op.PATH_TCGEN05 else max(3, args.steps // 4)
+            us = statistics.mean(time_rotating(torch, calls, n, 2)) * 1e3
             entry[pname] = {"us": round(us, 3), "TFLOP/s": round(fl / (us * 1e-6) / 1e12, 3),
-                            "GB/s": round(byts / (us * 1e-6) / 1e9, 1)}
+                            "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
+                            "roofline_frac": round(roof_us / us, 4)}
         parts[f"mul_mat_id_back_{nm}"] = entry
         del tW, tids, tg, o, wsb
 
     clk = clocks.stop()
     assert op.device_status() == 0, "device status word set"
-    tf32_cublas = _cublas_tf32(torch, device)
 
     # ---- roofline of the dominant kernel (the tensor-core tile kernel) ----
-    achieved = flops / (ms_main * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
-    roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
-            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-            "pipe_frac_3xtf32": round(3 * achieved / peak, 4),
-            "peak_note": f"TF32 = {peak_kind} bf16 burst {peaks['bf16_tflops']} x nominal "
-                         f"1.1/2.25 (of {peak_kind}); cuBLAS TF32 8192^3 in this run: "
-                         f"{tf32_cublas:.0f} TFLOP/s",
-            "kernel": "tc_out_prod_kernel (tcgen05 3xTF32), algorithmic 2*M*N*K per launch",
-            "kernel_ms": round(ms_main, 4), "split_prepass_ms": round(ms_step - ms_main, 4),
-            "traffic": TC_TRAFFIC_BYTES}
+    roof = dense_roofline(flops, ms_main * 1e3, tf32_peak)
+    roof.update({
+        "peak_note": f"dense TF32 peak measured in this run: cuBLAS TF32 GEMM 8192^3, best of "
+                     f"10 (of measured); for context, {peak_kind} bf16 burst "
+                     f"{peaks['bf16_tflops']} x nominal 1.1/2.25 = "
+                     f"{peaks['bf16_tflops'] * NOMINAL_TF32_OVER_BF16:.1f}",
+        "kernel": "tc_out_prod_kernel (tcgen05 3xTF32): achieved = 3 * 2*M*N*K TF32 flops per "
+                  "launch / its mean CUDA-event time",
+        "kernel_ms": round(ms_main, 4), "split_prepass_ms": round(ms_step - ms_main, 4),
+        "traffic": _traffic()})
 
     cpu = cpu_baseline(args.cpu_seconds) if rank == 0 and ws == 1 else None
     line = {
@@ -455,9 +527,7 @@ def gpu_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded splitmix64 normals, q8_0-quantised weight, 0.2% outliers)",
-        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{ws}",
-                   "l2": "512 MB buffer written before every timed step",
-                   "precision": "3xTF32 split on tensor cores, fp32 accumulation with Kahan fold"},
+        "config": bench_config(ws),
         "e2e": {"value": round(ws * flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(a_np.nbytes + b_np.nbytes),
                 "d2h_bytes_per_step": int(4 * DENSE_M * DENSE_N)},
@@ -543,7 +613,7 @@ def reference_arm(args):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "parallelism": "host cores"},
+            "config": bench_config(ws),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

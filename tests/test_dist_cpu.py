@@ -77,4 +77,4 @@ def test_reference_arm_line_on_rank_zero():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
-    assert "workload" in d["config"] and "m5120 k5120 n1024" in d["config"]["workload"]
+    assert "workload" in d["config"] and "m5120 k17408 n1024" in d["config"]["workload"]
