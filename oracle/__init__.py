@@ -86,6 +86,10 @@ def lib():
                                                     ctypes.c_int]
             L.oracle_mul_mat.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_int64, _dp]
+            L.oracle_out_prod_strided.argtypes = [_vp, ctypes.c_int, _vp, _i64p, _i64p,
+                                                  _i64p, _fp, _dp, _dp, ctypes.c_int]
+            L.oracle_mul_mat_back.argtypes = [_vp, ctypes.c_int, _fp, _fp, _i64p, _i64p,
+                                              _fp, _dp, _dp, _fp, _dp, _dp, ctypes.c_int]
             _lib = L
     return _lib
 
@@ -232,3 +236,64 @@ def mul_mat(W, x):
     if rc:
         raise ValueError("oracle_mul_mat rejected its arguments")
     return y
+
+
+def view_ne_nb(b):
+    """ggml ne and byte strides nb of a float32 numpy view with shape
+    (ne3, ne2, ne1, ne0) (fewer axes allowed); strides must be >= 0."""
+    b = np.asarray(b)
+    shp = (1,) * (4 - b.ndim) + tuple(b.shape)
+    st = (0,) * (4 - b.ndim) + tuple(b.strides)
+    ne = (shp[3], shp[2], shp[1], shp[0])
+    nb = (st[3], st[2], st[1], st[0])
+    if any(x < 0 for x in nb):
+        raise ValueError("negative strides are not supported")
+    return ne, nb
+
+
+def out_prod_strided(a, a_type, b_view, ne_a, nthreads=0):
+    """OUT_PROD with src1 read through the strides of the float32 numpy view
+    ``b_view`` (shape (ne13, ne12, K, N), any non-negative strides).  Returns
+    the same dict as out_prod."""
+    a = np.ascontiguousarray(a)
+    if b_view.dtype != np.float32:
+        raise ValueError("b must be float32")
+    ne_b, nb_b = view_ne_nb(b_view)
+    M, N, n2, n3 = ne_a[0], ne_b[0], ne_b[2], ne_b[3]
+    shape = (n3, n2, N, M)
+    dst = np.empty(shape, np.float32)
+    f64 = np.empty(shape, np.float64)
+    ab = np.empty(shape, np.float64)
+    bp = ctypes.c_void_p(b_view.ctypes.data) if b_view.size else None
+    rc = lib().oracle_out_prod_strided(
+        _vptr(a), a_type, bp, _ne(nb_b), _ne(ne_a), _ne(ne_b),
+        _ptr(dst, ctypes.c_float), _ptr(f64, ctypes.c_double), _ptr(ab, ctypes.c_double),
+        nthreads)
+    if rc:
+        raise ValueError("oracle_out_prod_strided rejected its arguments")
+    return {"dst": dst, "f64": f64, "abs": ab}
+
+
+def mul_mat_back(W, w_type, x, dy, ne_w, nthreads=0):
+    """Both gradients of y = MUL_MAT(W, x) given dy.  W: src0 bytes or array of
+    ggml shape ne_w = {K, R, ne02, ne03}; x: float32 (ne13, ne12, T, K);
+    dy: float32 (ne13, ne12, T, R).  Returns {"dx": {...}, "dW": {...}}, each
+    with "dst", "f64" and "abs" (dx shaped like x, dW (ne03, ne02, R, K))."""
+    W = np.ascontiguousarray(W)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    dy = np.ascontiguousarray(dy, dtype=np.float32)
+    ne_x = ne_of(x)
+    K, R, n02, n03 = ne_w
+    out = {}
+    for name, shape in (("dx", (ne_x[3], ne_x[2], ne_x[1], K)), ("dW", (n03, n02, R, K))):
+        out[name] = {"dst": np.empty(shape, np.float32), "f64": np.empty(shape, np.float64),
+                     "abs": np.empty(shape, np.float64)}
+    rc = lib().oracle_mul_mat_back(
+        _vptr(W), w_type, _ptr(x, ctypes.c_float), _ptr(dy, ctypes.c_float), _ne(ne_w),
+        _ne(ne_x), _ptr(out["dW"]["dst"], ctypes.c_float),
+        _ptr(out["dW"]["f64"], ctypes.c_double), _ptr(out["dW"]["abs"], ctypes.c_double),
+        _ptr(out["dx"]["dst"], ctypes.c_float), _ptr(out["dx"]["f64"], ctypes.c_double),
+        _ptr(out["dx"]["abs"], ctypes.c_double), nthreads)
+    if rc:
+        raise ValueError("oracle_mul_mat_back rejected its arguments")
+    return out

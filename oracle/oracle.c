@@ -303,6 +303,179 @@ int oracle_out_prod_at(const void *a, int a_type, const float *b,
     return 0;
 }
 
+/* OUT_PROD with src1 read through byte strides: the loop of
+ * out_prod_impl with only the address of b changed. */
+int oracle_out_prod_strided(const void *a, int a_type, const void *b,
+                            const int64_t nb_b[4], const int64_t ne_a[4],
+                            const int64_t ne_b[4], float *dst, double *dst_f64,
+                            double *abssum, int nthreads)
+{
+    shape_t s;
+    if (check_shape(a_type, ne_a, ne_b, &s) || !nb_b) return -1;
+    for (int i = 0; i < 4; ++i)
+        if (nb_b[i] < 0 || nb_b[i] % 4) return -1;
+    if (!dst && !dst_f64 && !abssum) return -1;
+    const int64_t nslice = s.ne12 * s.ne13;
+    if (s.M == 0 || s.N == 0 || nslice == 0) return 0;
+    if ((!a || !b) && s.K > 0) return -1;
+    set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)s.M * sizeof(double));
+        double *sab = (double *)malloc((size_t)s.M * sizeof(double));
+        double *arow = (double *)malloc((size_t)s.M * sizeof(double));
+        if (!acc || !sab || !arow) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t w = 0; w < nslice * s.N; ++w) {
+            if (!acc || !sab || !arow) continue;
+            const int64_t n = w % s.N;
+            const int64_t sl = w / s.N;
+            const int64_t i2 = sl % s.ne12, i3 = sl / s.ne12;
+            const int64_t j2 = i2 / s.dps2, j3 = i3 / s.dps3;
+            for (int64_t m = 0; m < s.M; ++m) acc[m] = sab[m] = 0.0;
+            for (int64_t k = 0; k < s.K; ++k) {
+                const uint8_t *row = a_row(a, &s, k, j2, j3);
+                for (int64_t m = 0; m < s.M; ++m) arow[m] = elem(a_type, row, m);
+                float f;
+                memcpy(&f, (const uint8_t *)b + n * nb_b[0] + k * nb_b[1] + i2 * nb_b[2] +
+                               i3 * nb_b[3], 4);
+                const double y = (double)f;
+                for (int64_t m = 0; m < s.M; ++m) {
+                    double p = arow[m] * y;
+                    acc[m] += p;
+                    sab[m] += fabs(p);
+                }
+            }
+            const int64_t base = (sl * s.N + n) * s.M;
+            for (int64_t m = 0; m < s.M; ++m) {
+                if (dst) dst[base + m] = (float)acc[m];
+                if (dst_f64) dst_f64[base + m] = acc[m];
+                if (abssum) abssum[base + m] = sab[m];
+            }
+        }
+        free(acc);
+        free(sab);
+        free(arow);
+    }
+    return failed ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* the MUL_MAT backward pair ("metal: OUT_PROD multiplies in float     */
+/* staging", scope paragraph: both gradients of a MUL_MAT)            */
+/* ------------------------------------------------------------------ */
+
+int oracle_mul_mat_back(const void *W, int w_type, const float *x, const float *dy,
+                        const int64_t ne_w[4], const int64_t ne_x[4],
+                        float *dW, double *dW_f64, double *dW_abs,
+                        float *dx, double *dx_f64, double *dx_abs, int nthreads)
+{
+    if (!ne_w || !ne_x) return -1;
+    const int64_t K = ne_w[0], R = ne_w[1], ne02 = ne_w[2], ne03 = ne_w[3];
+    const int64_t T = ne_x[1], ne12 = ne_x[2], ne13 = ne_x[3];
+    for (int i = 0; i < 4; ++i)
+        if (ne_w[i] < 0 || ne_x[i] < 0) return -1;
+    if (ne_x[0] != K || ne02 == 0 || ne03 == 0) return -1;
+    if (ne12 % ne02 || ne13 % ne03) return -1;
+    const int64_t dps2 = ne12 / ne02, dps3 = ne13 / ne03;
+    shape_t s;   /* W as an OUT_PROD src0 {K, R, ne02, ne03}: row r holds K elements */
+    {
+        const int64_t ne_a[4] = {K, R, ne02, ne03}, ne_b[4] = {T, R, ne12, ne13};
+        if (check_shape(w_type, ne_a, ne_b, &s)) return -1;
+    }
+    const int want_dx = dx || dx_f64 || dx_abs;
+    const int want_dw = dW || dW_f64 || dW_abs;
+    if ((want_dx && (!W || !dy) && R > 0 && K > 0 && T > 0) ||
+        (want_dw && (!x || !dy) && T > 0 && K > 0 && R > 0))
+        return -1;
+    set_threads(nthreads);
+    int failed = 0;
+    if (want_dx && K > 0) {
+        /* one work item per (slice, t): a row of K results, sum over r ascending */
+#pragma omp parallel
+        {
+            double *acc = (double *)malloc((size_t)K * sizeof(double));
+            double *sab = (double *)malloc((size_t)K * sizeof(double));
+            double *wrow = (double *)malloc((size_t)K * sizeof(double));
+            if (!acc || !sab || !wrow) {
+#pragma omp atomic write
+                failed = 1;
+            }
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t w = 0; w < ne12 * ne13 * T; ++w) {
+                if (!acc || !sab || !wrow) continue;
+                const int64_t t = w % T, sl = w / T;
+                const int64_t i2 = sl % ne12, i3 = sl / ne12;
+                for (int64_t k = 0; k < K; ++k) acc[k] = sab[k] = 0.0;
+                for (int64_t r = 0; r < R; ++r) {
+                    const uint8_t *row = a_row(W, &s, r, i2 / dps2, i3 / dps3);
+                    for (int64_t k = 0; k < K; ++k) wrow[k] = elem(w_type, row, k);
+                    const double g = (double)dy[(sl * T + t) * R + r];
+                    for (int64_t k = 0; k < K; ++k) {
+                        const double p = wrow[k] * g;
+                        acc[k] += p;
+                        sab[k] += fabs(p);
+                    }
+                }
+                const int64_t base = (sl * T + t) * K;
+                for (int64_t k = 0; k < K; ++k) {
+                    if (dx) dx[base + k] = (float)acc[k];
+                    if (dx_f64) dx_f64[base + k] = acc[k];
+                    if (dx_abs) dx_abs[base + k] = sab[k];
+                }
+            }
+            free(acc);
+            free(sab);
+            free(wrow);
+        }
+    }
+    if (want_dw && K > 0 && R > 0) {
+        /* one work item per (W slice, r): a row of K results */
+#pragma omp parallel
+        {
+            double *acc = (double *)malloc((size_t)K * sizeof(double));
+            double *sab = (double *)malloc((size_t)K * sizeof(double));
+            if (!acc || !sab) {
+#pragma omp atomic write
+                failed = 1;
+            }
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t w = 0; w < ne02 * ne03 * R; ++w) {
+                if (!acc || !sab) continue;
+                const int64_t r = w % R, wsl = w / R;
+                const int64_t j2 = wsl % ne02, j3 = wsl / ne02;
+                for (int64_t k = 0; k < K; ++k) acc[k] = sab[k] = 0.0;
+                for (int64_t i3 = j3 * dps3; i3 < (j3 + 1) * dps3; ++i3)
+                    for (int64_t i2 = j2 * dps2; i2 < (j2 + 1) * dps2; ++i2) {
+                        const int64_t sl = i3 * ne12 + i2;
+                        for (int64_t t = 0; t < T; ++t) {
+                            const double g = (double)dy[(sl * T + t) * R + r];
+                            const float *xr = x + (sl * T + t) * K;
+                            for (int64_t k = 0; k < K; ++k) {
+                                const double p = (double)xr[k] * g;
+                                acc[k] += p;
+                                sab[k] += fabs(p);
+                            }
+                        }
+                    }
+                const int64_t base = (wsl * R + r) * K;
+                for (int64_t k = 0; k < K; ++k) {
+                    if (dW) dW[base + k] = (float)acc[k];
+                    if (dW_f64) dW_f64[base + k] = acc[k];
+                    if (dW_abs) dW_abs[base + k] = sab[k];
+                }
+            }
+            free(acc);
+            free(sab);
+        }
+    }
+    return failed ? -1 : 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* MUL_MAT_ID_BACK                                                    */
 /* ------------------------------------------------------------------ */

@@ -85,6 +85,30 @@ int oracle_mul_mat_id_back_at(const void *W, int w_type, const int32_t *ids,
                               int64_t n_pts, double *val, double *abssum,
                               int nthreads);
 
+/* OUT_PROD with src1 given as a strided view: element b[n,k,i2,i3] is the
+ * f32 at byte offset n*nb_b[0] + k*nb_b[1] + i2*nb_b[2] + i3*nb_b[3] from b
+ * (strides non-negative multiples of 4).  Otherwise exactly oracle_out_prod:
+ * the same sums in the same order. */
+int oracle_out_prod_strided(const void *a, int a_type, const void *b,
+                            const int64_t nb_b[4], const int64_t ne_a[4],
+                            const int64_t ne_b[4], float *dst, double *dst_f64,
+                            double *abssum, int nthreads);
+
+/* The backward of ggml's MUL_MAT with its broadcast.  Forward:
+ *   y[r,t,i2,i3] = sum_k W[k,r,i2/dps2,i3/dps3] * x[k,t,i2,i3]
+ * with W {K, R, ne02, ne03} (f32, f16, bf16, q8_0, q4_0), x {K, T, ne12, ne13}
+ * f32, dps2 = ne12/ne02, dps3 = ne13/ne03.  Given dy {R, T, ne12, ne13} f32:
+ *   dx[k,t,i2,i3] = sum_r W[k,r,i2/dps2,i3/dps3] * dy[r,t,i2,i3]
+ *   dW[k,r,j2,j3] = sum over i3 with i3/dps3 == j3 (ascending), i2 with
+ *                   i2/dps2 == j2 (ascending), then t (ascending) of
+ *                   x[k,t,i2,i3] * dy[r,t,i2,i3]
+ * dx is {K, T, ne12, ne13}, dW {K, R, ne02, ne03}.  Any output pointer may
+ * be NULL (that output is skipped). */
+int oracle_mul_mat_back(const void *W, int w_type, const float *x, const float *dy,
+                        const int64_t ne_w[4], const int64_t ne_x[4],
+                        float *dW, double *dW_f64, double *dW_abs,
+                        float *dx, double *dx_f64, double *dx_abs, int nthreads);
+
 /* Forward MUL_MAT in fp64: W {K, R} (k fastest), x {K, T};
  * y[r,t] = sum_k W[k,r] * x[k,t], y {R, T} (r fastest). */
 int oracle_mul_mat(const double *W, const double *x, int64_t K, int64_t R,

@@ -435,3 +435,124 @@ def test_finite_difference_of_forward(orc):
             Wm[r, k] -= 1.0
             fd = (loss(Wp, xf) - loss(Wm, xf)) / 2.0
             assert abs(fd - gw[r, k]) <= 1e-12 * (1 + abs(fd))
+
+
+# --------------------------------------------------------------------------
+# src1 as a strided view, and the MUL_MAT backward pair
+# ("metal: OUT_PROD multiplies in float staging", scope paragraph: the
+#  gradient of src1 is out_prod(src0, grad^T), a transposed view of grad)
+# --------------------------------------------------------------------------
+
+def _views(rng):
+    """(name, src1 view) pairs: a transpose, padded rows, a slice step, a
+    zero stride (one row read for every n)."""
+    base = rng.normal(size=(2, 3, 40, 30)).astype(np.float32) * np.float32(100)
+    return [
+        ("transposed", np.swapaxes(base, 2, 3)),                  # (2, 3, 30, 40): k fastest
+        ("padded rows", base[:, :, :, 3:20]),                     # row stride 30, N = 17
+        ("every other slice", base[:, ::2]),
+        ("broadcast row", np.broadcast_to(base[:, :, :, :1], (2, 3, 40, 9))),
+    ]
+
+
+def test_strided_equals_contiguous(orc):
+    rng = np.random.default_rng(21)
+    for name, v in _views(rng):
+        ne_b, nb = orc.view_ne_nb(v)
+        ne_a = (48, ne_b[1], 1, ne_b[3])
+        a = synth.make_a(synth.TYPE_F32, ne_a, 120)
+        r1 = orc.out_prod_strided(a, synth.TYPE_F32, v, ne_a)
+        r2 = orc.out_prod(a, synth.TYPE_F32, np.ascontiguousarray(v), ne_a, ne_b)
+        for key in ("dst", "f64", "abs"):
+            assert np.array_equal(r1[key], r2[key]), f"{name} {key}"
+
+
+def test_strided_integer_exact(orc):
+    """Small-integer inputs through a transposed view equal an int64 einsum of
+    the transposed integers (every sum exact)."""
+    rng = np.random.default_rng(22)
+    M, K, N = 40, 33, 19
+    a = rng.integers(-8, 9, size=(1, 1, K, M)).astype(np.float32)
+    g = rng.integers(-8, 9, size=(1, 1, N, K)).astype(np.float32)   # g[n, k] row-major
+    v = np.swapaxes(g, 2, 3)                                          # b[k][n] view of g
+    r = orc.out_prod_strided(a, synth.TYPE_F32, v, (M, K, 1, 1))
+    exact = np.einsum("km,nk->nm", a[0, 0].astype(np.int64), g[0, 0].astype(np.int64))
+    assert np.array_equal(r["f64"][0, 0], exact.astype(np.float64))
+
+
+def _forward_f64(W, x, ne_w, ne_x):
+    """y[r,t,i2,i3] = sum_k W[k,r,i2/dps2,i3/dps3] x[k,t,i2,i3], in numpy."""
+    d2, d3 = ne_x[2] // ne_w[2], ne_x[3] // ne_w[3]
+    Wr = np.repeat(np.repeat(W, d2, axis=1), d3, axis=0)      # (ne13, ne12, R, K)
+    return np.einsum("abrk,abtk->abtr", Wr, x)
+
+
+@pytest.mark.parametrize("ne_w,ne_x", [
+    ((9, 6, 1, 1), (9, 5, 1, 1)),
+    ((8, 5, 2, 1), (8, 4, 4, 1)),      # dps2 = 2: dW sums over adjacent slices
+    ((7, 4, 2, 1), (7, 3, 4, 2)),      # dps2 = 2, dps3 = 2: groups not adjacent
+])
+def test_mul_mat_back_finite_differences(orc, ne_w, ne_x):
+    """The loss L = sum(y * G) is linear in W and in x, so a central
+    difference with step 1 in fp64 is the gradient up to rounding."""
+    rng = np.random.default_rng(sum(ne_w) + 7 * sum(ne_x))
+    K, R, w2, w3 = ne_w
+    _, T, x2, x3 = ne_x
+    W = rng.normal(size=(w3, w2, R, K)).astype(np.float32)
+    x = rng.normal(size=(x3, x2, T, K)).astype(np.float32)
+    G = rng.normal(size=(x3, x2, T, R)).astype(np.float32)
+    Wd, xd, Gd = (v.astype(np.float64) for v in (W, x, G))
+    out = orc.mul_mat_back(W, synth.TYPE_F32, x, G, ne_w)
+
+    def loss(Wm, xm):
+        return float((_forward_f64(Wm, xm, ne_w, ne_x) * Gd).sum())
+
+    for idx in np.ndindex(xd.shape):
+        xp, xm = xd.copy(), xd.copy()
+        xp[idx] += 1.0
+        xm[idx] -= 1.0
+        fd = (loss(Wd, xp) - loss(Wd, xm)) / 2.0
+        assert abs(fd - out["dx"]["f64"][idx]) <= 1e-12 * (1 + abs(fd)), idx
+    for idx in np.ndindex(Wd.shape):
+        Wp, Wm = Wd.copy(), Wd.copy()
+        Wp[idx] += 1.0
+        Wm[idx] -= 1.0
+        fd = (loss(Wp, xd) - loss(Wm, xd)) / 2.0
+        assert abs(fd - out["dW"]["f64"][idx]) <= 1e-12 * (1 + abs(fd)), idx
+
+
+@pytest.mark.parametrize("tid", [synth.TYPE_F32, synth.TYPE_Q8_0, synth.TYPE_Q4_0])
+def test_mul_mat_back_dx_is_out_prod_of_transposed_grad(orc, tid):
+    """dx = OUT_PROD(W, dy^T) with the same products in the same order: bit
+    for bit, for quantised W too."""
+    ne_w, ne_x = (64, 24, 2, 1), (64, 10, 4, 1)
+    W = synth.make_a(tid, ne_w, 121, std=0.02)
+    x = synth.make_b((64, 10, 4, 1), 122)
+    dy = synth.make_b((24, 10, 4, 1), 123, std=1e3, outliers=True)
+    out = orc.mul_mat_back(W, tid, x, dy, ne_w)
+    ref = orc.out_prod_strided(W, tid, np.swapaxes(dy, 2, 3), ne_w)
+    for key in ("dst", "f64", "abs"):
+        assert np.array_equal(out["dx"][key], ref[key]), key
+
+
+@pytest.mark.parametrize("ne_w,ne_x", [
+    ((48, 12, 1, 1), (48, 20, 1, 1)),
+    ((48, 12, 2, 1), (48, 20, 6, 1)),        # dps2 = 3, adjacent slices
+    ((48, 12, 1, 2), (48, 20, 3, 4)),        # ne02 = 1, dps3 = 2: adjacent too
+])
+def test_mul_mat_back_dw_is_out_prod_over_grouped_slices(orc, ne_w, ne_x):
+    """Where each broadcast group of slices is adjacent in memory (dps3 = 1 or
+    ne02 = 1), dW = OUT_PROD(x, dy) over the group's rows taken as one longer
+    reduction: bit for bit (the same products in the same order)."""
+    K, R, w2, w3 = ne_w
+    _, T, x2, x3 = ne_x
+    x = synth.make_b((K, T, x2, x3), 124)
+    dy = synth.make_b((R, T, x2, x3), 125, std=1e3, outliers=True)
+    W = synth.make_a(synth.TYPE_F32, ne_w, 126)
+    out = orc.mul_mat_back(W, synth.TYPE_F32, x, dy, ne_w)
+    group = (x2 // w2) * (x3 // w3)
+    ref = orc.out_prod(x.reshape(w3, w2, group * T, K), synth.TYPE_F32,
+                       dy.reshape(w3, w2, group * T, R), (K, group * T, w2, w3),
+                       (R, group * T, w2, w3))
+    for key in ("dst", "f64", "abs"):
+        assert np.array_equal(out["dW"][key], ref[key]), key
