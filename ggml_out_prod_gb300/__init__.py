@@ -65,7 +65,8 @@ EXPORTS = (
     "oop_last_cuda_error", "oop_out_prod_noalloc", "oop_out_prod_noalloc_scratch_bytes",
     "oop_profile_main_kernel", "oop_out_prod_workspace_min_size", "oop_debug_set_tc_schedule",
     "oop_last_launch_count", "oop_out_prod_host", "oop_out_prod_host_buffer_size",
-    "oop_out_prod_plan",
+    "oop_out_prod_plan", "oop_out_prod_strided", "oop_out_prod_strided_workspace_size",
+    "oop_mul_mat_back", "oop_mul_mat_back_workspace_size",
 )
 
 
@@ -144,6 +145,16 @@ def lib():
             L.oop_out_prod_plan.restype = ctypes.c_int
             L.oop_out_prod_plan.argtypes = [ctypes.c_int, _i64p, _i64p, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_size_t, ctypes.POINTER(OopPlan)]
+            L.oop_out_prod_strided_workspace_size.restype = ctypes.c_size_t
+            L.oop_out_prod_strided_workspace_size.argtypes = [ctypes.c_int, _i64p, _i64p, _i64p]
+            L.oop_out_prod_strided.restype = ctypes.c_int
+            L.oop_out_prod_strided.argtypes = [_vp, ctypes.c_int, _vp, _i64p, _vp, _i64p, _i64p,
+                                               _i64p, _vp, ctypes.c_size_t, _vp, ctypes.c_int]
+            L.oop_mul_mat_back_workspace_size.restype = ctypes.c_size_t
+            L.oop_mul_mat_back_workspace_size.argtypes = [ctypes.c_int, _i64p, _i64p]
+            L.oop_mul_mat_back.restype = ctypes.c_int
+            L.oop_mul_mat_back.argtypes = [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _i64p, _i64p,
+                                           _vp, ctypes.c_size_t, _vp]
             _lib = L
     return _lib
 
@@ -229,6 +240,28 @@ def oop_out_prod_noalloc(a, a_type, b, dst, ne_a, ne_b, ne_dst, stream) -> int:
                                           _ne(ne_dst), stream))
 
 
+def oop_out_prod_strided_workspace_size(a_type, ne_a, ne_b, nb_b) -> int:
+    return int(lib().oop_out_prod_strided_workspace_size(int(a_type), _ne(ne_a), _ne(ne_b),
+                                                         _ne(nb_b)))
+
+
+def oop_out_prod_strided(a, a_type, b, nb_b, dst, ne_a, ne_b, ne_dst, workspace,
+                         workspace_bytes, stream, path=PATH_AUTO) -> int:
+    return int(lib().oop_out_prod_strided(a, int(a_type), b, _ne(nb_b), dst, _ne(ne_a),
+                                          _ne(ne_b), _ne(ne_dst), workspace,
+                                          int(workspace_bytes), stream, int(path)))
+
+
+def oop_mul_mat_back_workspace_size(w_type, ne_w, ne_x) -> int:
+    return int(lib().oop_mul_mat_back_workspace_size(int(w_type), _ne(ne_w), _ne(ne_x)))
+
+
+def oop_mul_mat_back(W, w_type, x, dy, dW, dx, ne_w, ne_x, workspace, workspace_bytes,
+                     stream) -> int:
+    return int(lib().oop_mul_mat_back(W, int(w_type), x, dy, dW, dx, _ne(ne_w), _ne(ne_x),
+                                      workspace, int(workspace_bytes), stream))
+
+
 def oop_mul_mat_id_back_workspace_size(w_type, ne_w, ne_ids) -> int:
     return int(lib().oop_mul_mat_id_back_workspace_size(int(w_type), _ne(ne_w), _ne(ne_ids)))
 
@@ -273,11 +306,19 @@ def ne_of(t, type_id=TYPE_F32, ne0=None):
     return (shp[3], shp[2], shp[1], shp[0])
 
 
-def _check_cuda(t, name):
+def _check_cuda(t, name, contiguous=True):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
+    if contiguous and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def nb_of(t):
+    """ggml byte strides nb of a float32 tensor view in this layout."""
+    st = (0,) * (4 - t.dim()) + tuple(t.stride())
+    if any(x < 0 for x in st):
+        raise ValueError("negative strides are not supported")
+    return (4 * st[3], 4 * st[2], 4 * st[1], 4 * st[0])
 
 
 def _workspace(nbytes, device, workspace):
@@ -293,13 +334,15 @@ def out_prod(a, b, a_type=None, ne_a=None, out=None, workspace=None, stream=None
              path=PATH_AUTO):
     """dst = OUT_PROD(a, b) on a's device and the current (or given) stream.
 
-    a: float32 tensor, or uint8 q8_0/q4_0 rows (give ``a_type``); b: float32.
+    a: float32 tensor, or uint8 q8_0/q4_0 rows (give ``a_type``); b: float32,
+    contiguous or any view with non-negative strides (a transpose, a slice),
+    which is read in place through oop_out_prod_strided.
     Returns dst, float32 of shape (ne13, ne12, N, M)."""
     torch = _torch()
     if a_type is None:
         a_type = TYPE_F32
     _check_cuda(a, "a")
-    _check_cuda(b, "b")
+    _check_cuda(b, "b", contiguous=False)
     if b.dtype != torch.float32:
         raise ValueError("b must be float32")
     if a_type == TYPE_F32 and a.dtype != torch.float32:
@@ -314,13 +357,53 @@ def out_prod(a, b, a_type=None, ne_a=None, out=None, workspace=None, stream=None
         out = torch.empty((ne_dst[3], ne_dst[2], ne_dst[1], ne_dst[0]), dtype=torch.float32,
                           device=a.device)
     _check_cuda(out, "out")
-    nws = oop_out_prod_workspace_size(a_type, ne_a, ne_b)
+    if b.is_contiguous():
+        nws = oop_out_prod_workspace_size(a_type, ne_a, ne_b)
+        ws = _workspace(nws, a.device, workspace)
+        rc = oop_out_prod(_ptr(a), a_type, _ptr(b), _ptr(out), ne_a, ne_b, ne_dst, _ptr(ws),
+                          ws.numel() if ws is not None else 0, _stream_ptr(stream), path)
+        if rc != OK:
+            raise OopError(rc, "oop_out_prod")
+        return out
+    nb_b = nb_of(b)
+    nws = oop_out_prod_strided_workspace_size(a_type, ne_a, ne_b, nb_b)
     ws = _workspace(nws, a.device, workspace)
-    rc = oop_out_prod(_ptr(a), a_type, _ptr(b), _ptr(out), ne_a, ne_b, ne_dst, _ptr(ws),
-                      ws.numel() if ws is not None else 0, _stream_ptr(stream), path)
+    rc = oop_out_prod_strided(_ptr(a), a_type, _ptr(b), nb_b, _ptr(out), ne_a, ne_b, ne_dst,
+                              _ptr(ws), ws.numel() if ws is not None else 0,
+                              _stream_ptr(stream), path)
     if rc != OK:
-        raise OopError(rc, "oop_out_prod")
+        raise OopError(rc, "oop_out_prod_strided")
     return out
+
+
+def mul_mat_back(W, x, dy, w_type=None, ne_w=None, want_dW=True, want_dx=True,
+                 workspace=None, stream=None):
+    """Both gradients of y = MUL_MAT(W, x) from dy, in one call.
+
+    W: float32 (ne03, ne02, R, K), or uint8 q8_0/q4_0 rows (give ``w_type``
+    and ``ne_w``); x: float32 (ne13, ne12, T, K); dy: float32
+    (ne13, ne12, T, R).  Returns (dW, dx): dW float32 (ne03, ne02, R, K) or
+    None, dx float32 like x or None."""
+    torch = _torch()
+    if w_type is None:
+        w_type = TYPE_F32
+    for t, n in ((W, "W"), (x, "x"), (dy, "dy")):
+        _check_cuda(t, n)
+    if x.dtype != torch.float32 or dy.dtype != torch.float32:
+        raise ValueError("x and dy must be float32")
+    if ne_w is None:
+        ne_w = ne_of(W, w_type)
+    ne_x = ne_of(x)
+    dW = torch.empty((ne_w[3], ne_w[2], ne_w[1], ne_w[0]), dtype=torch.float32,
+                     device=W.device) if want_dW else None
+    dx = torch.empty_like(x) if want_dx else None
+    nws = oop_mul_mat_back_workspace_size(w_type, ne_w, ne_x)
+    ws = _workspace(nws, W.device, workspace)
+    rc = oop_mul_mat_back(_ptr(W), w_type, _ptr(x), _ptr(dy), _ptr(dW), _ptr(dx), ne_w, ne_x,
+                          _ptr(ws), ws.numel() if ws is not None else 0, _stream_ptr(stream))
+    if rc != OK:
+        raise OopError(rc, "oop_mul_mat_back")
+    return dW, dx
 
 
 def mul_mat_id_back(W, ids, g, w_type=None, out=None, workspace=None, stream=None,

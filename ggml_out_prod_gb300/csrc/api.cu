@@ -5,6 +5,7 @@
 // contract ("metal: OUT_PROD runs batched, broadcast and narrow shapes on the
 // GPU", review comment, first bullet): dst = {a.ne0, b.ne0, b.ne2, b.ne3},
 // b.ne2 % a.ne2 == 0 and b.ne3 % a.ne3 == 0.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -165,32 +166,41 @@ int cuda_rc(cudaError_t e) {
     return OOP_ERR_CUDA;
 }
 
+// Byte strides of a src1 view: non-negative multiples of 4 (strides of size-1
+// dimensions are ignored).  Sets s->b_strided unless the view is the dense
+// layout, and s->bs to element strides.
+int check_b_strides(const int64_t nb_b[4], OutProdShape *s) {
+    s->b_strided = false;
+    if (!nb_b) return OOP_OK;
+    for (int i = 0; i < 4; ++i)
+        if (nb_b[i] < 0 || nb_b[i] % 4 != 0) return OOP_ERR_SHAPE;
+    const int64_t ne[4] = {s->N, s->K, s->ne12, s->ne13};
+    const int64_t dense[4] = {1, s->N, s->N * s->K, s->N * s->K * s->ne12};
+    for (int i = 0; i < 4; ++i) {
+        s->bs[i] = ne[i] > 1 ? nb_b[i] / 4 : 0;
+        if (ne[i] > 1 && s->bs[i] != dense[i]) s->b_strided = true;
+    }
+    return OOP_OK;
+}
+
+// The least workspace of a path; a strided src1 adds its gather into the
+// dense layout for the CUDA-core kernels (the tensor-core split reads views).
+size_t workspace_need(const OutProdShape &s, int path) {
+    if (s.b_strided && path != OOP_PATH_TCGEN05) return strided_gather_bytes(s);
+    return workspace_min(s, path);
+}
+
 }  // namespace
-}  // namespace oop
 
-using namespace oop;
-
-extern "C" {
-
-size_t oop_out_prod_workspace_size(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
-    OutProdShape s = {};
-    if (check_out_prod_shape(a_type, ne_a, ne_b, &s) != OOP_OK) return 0;
-    // cover every path a caller may pick with oop_out_prod_ex
-    return tc_workspace_bytes(s);
-}
-
-size_t oop_out_prod_workspace_min_size(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
-    OutProdShape s = {};
-    if (check_out_prod_shape(a_type, ne_a, ne_b, &s) != OOP_OK) return 0;
-    return workspace_min(s, OOP_PATH_TCGEN05);
-}
-
-int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst, const int64_t ne_a[4],
-                    const int64_t ne_b[4], const int64_t ne_dst[4], void *workspace,
-                    size_t workspace_bytes, void *stream, int path) {
+int run_out_prod(const void *a, int a_type, const float *b, const int64_t nb_b[4], float *dst,
+                 const int64_t ne_a[4], const int64_t ne_b[4], const int64_t ne_dst[4],
+                 void *workspace, size_t workspace_bytes, void *stream, int path,
+                 bool check_only) {
     g_kernel_launches = 0;
     OutProdShape s = {};
     int rc = check_out_prod_shape(a_type, ne_a, ne_b, &s);
+    if (rc != OOP_OK) return rc;
+    rc = check_b_strides(nb_b, &s);
     if (rc != OOP_OK) return rc;
     if (!ne_dst) return OOP_ERR_NULL;
     if (ne_dst[0] != s.M || ne_dst[1] != s.N || ne_dst[2] != s.ne12 || ne_dst[3] != s.ne13)
@@ -213,25 +223,35 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst, const
 
     const int chosen = choose_path(s, path);
     if (chosen == OOP_PATH_SKINNY && !skinny_ok(s)) return OOP_ERR_PATH;
-    const size_t need = workspace_min(s, chosen);
+    const size_t need = workspace_need(s, chosen);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
         return OOP_ERR_WORKSPACE;
+    if (check_only) return OOP_OK;
 
     if (s.K == 0)   // an empty sum
         return cuda_rc(cudaMemsetAsync(dst, 0, static_cast<size_t>(n_dst) * sizeof(float), st));
 
+    cudaError_t e = cudaSuccess;
+    if (s.b_strided && chosen != OOP_PATH_TCGEN05) {
+        // the CUDA-core kernels read the dense layout: gather the view first
+        float *dense = static_cast<float *>(workspace);
+        e = launch_b_gather(b, s, dense, st);
+        if (e != cudaSuccess) return cuda_rc(e);
+        b = dense;
+        s.b_strided = false;
+    }
+    const int gathered = g_kernel_launches;
     s.a_vec16 = aligned(a, 16) && (s.a_row_bytes % 16 == 0);
-    s.b_vec16 = aligned(b, 16) && (s.N % 4 == 0);
+    s.b_vec16 = !s.b_strided && aligned(b, 16) && (s.N % 4 == 0);
     s.dst_vec16 = aligned(dst, 16) && (s.M % 4 == 0);
 
-    cudaError_t e;
     switch (chosen) {
     case OOP_PATH_SKINNY:
         if (skinny_tma_ok(static_cast<const float *>(a), b, s))
             e = launch_skinny_tma(static_cast<const float *>(a), b, dst, s, status, st);
         else
             e = launch_skinny(static_cast<const float *>(a), b, dst, s, st);
-        if (e == cudaSuccess) g_kernel_launches = 1;
+        if (e == cudaSuccess) g_kernel_launches = gathered + 1;
         break;
     case OOP_PATH_TCGEN05:
         e = launch_dense_tc(a, b, dst, s, workspace, workspace_bytes, status, st);
@@ -239,13 +259,60 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst, const
         break;
     case OOP_PATH_SIMT:
         e = launch_dense_simt(a, b, dst, s, st);
-        if (e == cudaSuccess) g_kernel_launches = 1;
+        if (e == cudaSuccess) g_kernel_launches = gathered + 1;
         break;
     default:
         return OOP_ERR_PATH;
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     return cuda_rc(e);
+}
+
+}  // namespace oop
+
+using namespace oop;
+
+extern "C" {
+
+size_t oop_out_prod_workspace_size(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
+    OutProdShape s = {};
+    if (check_out_prod_shape(a_type, ne_a, ne_b, &s) != OOP_OK) return 0;
+    // cover every path a caller may pick with oop_out_prod_ex
+    return tc_workspace_bytes(s);
+}
+
+size_t oop_out_prod_workspace_min_size(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
+    OutProdShape s = {};
+    if (check_out_prod_shape(a_type, ne_a, ne_b, &s) != OOP_OK) return 0;
+    return workspace_min(s, OOP_PATH_TCGEN05);
+}
+
+int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst, const int64_t ne_a[4],
+                    const int64_t ne_b[4], const int64_t ne_dst[4], void *workspace,
+                    size_t workspace_bytes, void *stream, int path) {
+    return oop::run_out_prod(a, a_type, b, nullptr, dst, ne_a, ne_b, ne_dst, workspace,
+                             workspace_bytes, stream, path);
+}
+
+size_t oop_out_prod_strided_workspace_size(int a_type, const int64_t ne_a[4],
+                                           const int64_t ne_b[4], const int64_t nb_b[4]) {
+    OutProdShape s = {};
+    if (check_out_prod_shape(a_type, ne_a, ne_b, &s) != OOP_OK) return 0;
+    if (check_b_strides(nb_b, &s) != OOP_OK) return 0;
+    if (!s.b_strided) return tc_workspace_bytes(s);
+    return std::max(tc_workspace_bytes(s), strided_gather_bytes(s));
+}
+
+int oop_out_prod_strided(const void *a, int a_type, const float *b, const int64_t nb_b[4],
+                         float *dst, const int64_t ne_a[4], const int64_t ne_b[4],
+                         const int64_t ne_dst[4], void *workspace, size_t workspace_bytes,
+                         void *stream, int path) {
+    if (!nb_b) {
+        g_kernel_launches = 0;
+        return OOP_ERR_NULL;
+    }
+    return oop::run_out_prod(a, a_type, b, nb_b, dst, ne_a, ne_b, ne_dst, workspace,
+                             workspace_bytes, stream, path);
 }
 
 int oop_out_prod(const void *a, int a_type, const float *b, float *dst, const int64_t ne_a[4],

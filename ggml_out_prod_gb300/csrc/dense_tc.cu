@@ -891,6 +891,68 @@ void launch_fixup(const float *partial, const TcParams &p, int64_t tiles, cudaSt
 // consecutive k per thread (8-byte stores) on the way out.
 constexpr int kSplitTile = 64;
 
+// The output half shared by both split passes: tile[k][n] (64 x 64, k0, n0)
+// -> bhi, blo [slice][n][Kp], two consecutive k per thread (8-byte stores).
+__device__ __forceinline__ void store_split_tile(const float (&tile)[kSplitTile][kSplitTile + 1],
+                                                 uint32_t *__restrict__ bhi,
+                                                 uint32_t *__restrict__ blo, int64_t slice,
+                                                 int64_t k0, int64_t n0, int64_t N, int64_t Kp) {
+    const int tx = threadIdx.x, ty = threadIdx.y;           // 32 x 8
+#pragma unroll
+    for (int i = ty; i < kSplitTile; i += 8) {
+        const int64_t n = n0 + i, k = k0 + 2 * tx;          // Kp is a multiple of 4
+        if (n < N && k < Kp) {
+            uint32_t h0, l0, h1, l1;
+            ptx::split_tf32(tile[2 * tx][i], h0, l0);
+            ptx::split_tf32(tile[2 * tx + 1][i], h1, l1);
+            const int64_t o = (slice * N + n) * Kp + k;
+            *reinterpret_cast<uint2 *>(bhi + o) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(blo + o) = make_uint2(l0, l1);
+        }
+    }
+}
+
+// The split of a strided src1 view (element strides s0 for n, s1 for k, s2,
+// s3 for the slice indices).  When k is the contiguous index (s1 == 1: the
+// transposed gradient dy^T of a MUL_MAT backward), lanes read along k, so
+// each warp reads 128 contiguous bytes per row; otherwise along n.  Zero
+// padding for k in [K, Kp) as in bsplit_kernel.
+__global__ void __launch_bounds__(256) bsplit_strided_kernel(
+    const float *__restrict__ b, uint32_t *__restrict__ bhi, uint32_t *__restrict__ blo,
+    int64_t K, int64_t N, int64_t Kp, int64_t ne12, int64_t s0, int64_t s1, int64_t s2,
+    int64_t s3) {
+    __shared__ float tile[kSplitTile][kSplitTile + 1];      // [k][n]
+    const int64_t slice = blockIdx.z;
+    const float *bs = b + (slice % ne12) * s2 + (slice / ne12) * s3;
+    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * kSplitTile;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kSplitTile;
+    const int tx = threadIdx.x, ty = threadIdx.y;           // 32 x 8
+    if (s1 == 1) {
+#pragma unroll 4
+        for (int i = ty; i < kSplitTile; i += 8) {          // i: n offset
+            const int64_t n = n0 + i;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t k = k0 + tx + 32 * h;
+                tile[tx + 32 * h][i] = (n < N && k < K) ? __ldg(bs + n * s0 + k) : 0.f;
+            }
+        }
+    } else {
+#pragma unroll 4
+        for (int i = ty; i < kSplitTile; i += 8) {          // i: k offset
+            const int64_t k = k0 + i;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t n = n0 + tx + 32 * h;
+                tile[i][tx + 32 * h] = (n < N && k < K) ? __ldg(bs + n * s0 + k * s1) : 0.f;
+            }
+        }
+    }
+    __syncthreads();
+    store_split_tile(tile, bhi, blo, slice, k0, n0, N, Kp);
+    ptx::griddep_launch_dependents();   // as in bsplit_kernel
+}
+
 __global__ void __launch_bounds__(256) bsplit_kernel(const float *__restrict__ b,
                                                      uint32_t *__restrict__ bhi,
                                                      uint32_t *__restrict__ blo, int64_t K,
@@ -920,18 +982,7 @@ __global__ void __launch_bounds__(256) bsplit_kernel(const float *__restrict__ b
         tile[i][2 * tx + 1] = v1;
     }
     __syncthreads();
-#pragma unroll
-    for (int i = ty; i < kSplitTile; i += 8) {
-        const int64_t n = n0 + i, k = k0 + 2 * tx;          // Kp is a multiple of 4
-        if (n < N && k < Kp) {
-            uint32_t h0, l0, h1, l1;
-            ptx::split_tf32(tile[2 * tx][i], h0, l0);
-            ptx::split_tf32(tile[2 * tx + 1][i], h1, l1);
-            const int64_t o = (slice * N + n) * Kp + k;
-            *reinterpret_cast<uint2 *>(bhi + o) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2 *>(blo + o) = make_uint2(l0, l1);
-        }
-    }
+    store_split_tile(tile, bhi, blo, slice, k0, n0, N, Kp);
     // the tile kernel after this one may start launching (it waits for this
     // grid to complete before it reads bhi / blo)
     ptx::griddep_launch_dependents();
@@ -1210,9 +1261,13 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
 
     const int64_t gk = (Kp + kSplitTile - 1) / kSplitTile, gn = (s.N + kSplitTile - 1) / kSplitTile;
     if (gk > 0x7fffffffLL || gn > 65535 || slices > 65535) return cudaErrorInvalidConfiguration;
-    bsplit_kernel<<<dim3(static_cast<unsigned>(gk), static_cast<unsigned>(gn),
-                         static_cast<unsigned>(slices)),
-                    dim3(32, 8), 0, stream>>>(b, bhi, blo, s.K, s.N, Kp);
+    const dim3 sgrid(static_cast<unsigned>(gk), static_cast<unsigned>(gn),
+                     static_cast<unsigned>(slices));
+    if (s.b_strided)
+        bsplit_strided_kernel<<<sgrid, dim3(32, 8), 0, stream>>>(
+            b, bhi, blo, s.K, s.N, Kp, s.ne12, s.bs[0], s.bs[1], s.bs[2], s.bs[3]);
+    else
+        bsplit_kernel<<<sgrid, dim3(32, 8), 0, stream>>>(b, bhi, blo, s.K, s.N, Kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++g_kernel_launches;

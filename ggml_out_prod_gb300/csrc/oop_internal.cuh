@@ -28,6 +28,12 @@ struct OutProdShape {
     bool a_vec16;                 // a base and row stride 16-byte aligned
     bool b_vec16;                 // b base and row stride 16-byte aligned
     bool dst_vec16;               // dst base and row stride 16-byte aligned
+    // src1 as a strided view: element (n, k, i2, i3) at
+    // n*bs[0] + k*bs[1] + i2*bs[2] + i3*bs[3] floats from b.  Only the
+    // tensor-core split reads such a view; b_strided false means the dense
+    // layout ((i3*ne12 + i2)*K + k)*N + n.
+    bool b_strided;
+    int64_t bs[4];
 };
 
 struct MmidShape {
@@ -89,6 +95,20 @@ int out_prod_check_shape(int a_type, const int64_t ne_a[4], const int64_t ne_b[4
 // check's status.
 int out_prod_auto_workspace(int a_type, const int64_t ne_a[4], const int64_t ne_b[4],
                             size_t *min_bytes, size_t *full_bytes);
+
+// Every OUT_PROD entry point ends here: host checks, kernel choice, launch.
+// nb_b: byte strides of a src1 view, or NULL for the dense layout.  With
+// check_only the call returns after the host checks, having enqueued nothing.
+int run_out_prod(const void *a, int a_type, const float *b, const int64_t nb_b[4], float *dst,
+                 const int64_t ne_a[4], const int64_t ne_b[4], const int64_t ne_dst[4],
+                 void *workspace, size_t workspace_bytes, void *stream, int path,
+                 bool check_only = false);
+
+// A strided src1 view gathered into the dense layout [slice][k][n] (for the
+// CUDA-core kernels), and the bytes that takes.
+size_t strided_gather_bytes(const OutProdShape &s);
+cudaError_t launch_b_gather(const float *b, const OutProdShape &s, float *out,
+                            cudaStream_t stream);
 
 // Tensor-core OUT_PROD (tcgen05, 3xTF32).  The workspace holds the TF32 split
 // of src1 (the minimum) and, after it, the stream-K partial slots; with less

@@ -124,6 +124,63 @@ int oop_out_prod_ex(const void *a, int a_type, const float *b, float *dst,
                     size_t workspace_bytes, void *stream, int path);
 
 /*
+ * OUT_PROD with src1 given as a strided view: element b[n, k, i2, i3] is the
+ * f32 at byte offset n*nb_b[0] + k*nb_b[1] + i2*nb_b[2] + i3*nb_b[3] from b.
+ * The gradient of a MUL_MAT's src1 is out_prod(src0, grad^T) ("metal:
+ * OUT_PROD multiplies in float staging; a training gradient overflowed half",
+ * scope paragraph); with nb_b = {4*R, 4, 4*R*T, 4*R*T*ne12} for a grad of
+ * {R, T, ne12, ne13}, grad^T is read in place, never materialised.
+ *
+ * Strides: non-negative multiples of 4 (any order, repeats allowed; a stride
+ * of a size-1 dimension is ignored); anything else returns OOP_ERR_SHAPE.
+ * The operation, the other arguments, dst, path and errors are those of
+ * oop_out_prod_ex.  workspace: oop_out_prod_strided_workspace_size(...)
+ * bytes (which covers every path): the tensor-core kernel's split pre-pass
+ * reads the view itself; the CUDA-core kernels first gather it into the dense
+ * layout in the workspace (4*N*K bytes per slice), so with a strided view
+ * they need a workspace too.  A view that is the dense layout is exactly
+ * oop_out_prod_ex.
+ */
+size_t oop_out_prod_strided_workspace_size(int a_type, const int64_t ne_a[4],
+                                           const int64_t ne_b[4], const int64_t nb_b[4]);
+
+int oop_out_prod_strided(const void *a, int a_type, const float *b, const int64_t nb_b[4],
+                         float *dst, const int64_t ne_a[4], const int64_t ne_b[4],
+                         const int64_t ne_dst[4], void *workspace, size_t workspace_bytes,
+                         void *stream, int path);
+
+/*
+ * Both gradients of a MUL_MAT, in one call ("metal: OUT_PROD multiplies in
+ * float staging", scope paragraph: src0's gradient is out_prod(src1, grad),
+ * src1's is out_prod(src0, grad^T)).  Forward, with ggml's broadcast:
+ *
+ *   y[r, t, i2, i3] = sum_k W[k, r, i2/dps2, i3/dps3] * x[k, t, i2, i3]
+ *
+ *   ne_w = {K, R, ne02, ne03}   W: f32, q8_0 or q4_0
+ *   ne_x = {K, T, ne12, ne13}   x: f32;  dy: f32 {R, T, ne12, ne13}
+ *
+ *   dx[k, t, i2, i3] = sum_r W[k, r, i2/dps2, i3/dps3] * dy[r, t, i2, i3]
+ *                      (OUT_PROD(W, dy^T), dy^T read in place);  dx like x
+ *   dW[k, r, j2, j3] = sum of x[k, t, i2, i3] * dy[r, t, i2, i3] over t and
+ *                      over the slices (i2, i3) of broadcast group (j2, j3)
+ *                      (OUT_PROD(x, dy) with each group's rows as one longer
+ *                      reduction);  dW {K, R, ne02, ne03}, f32
+ *
+ * Either output may be NULL (not computed); both are OVERWRITTEN.  dW needs
+ * each group's slices adjacent in memory (dps3 == 1 or ne02 == 1), else
+ * OOP_ERR_BROADCAST.  Precision as oop_out_prod.  workspace: at least
+ * oop_mul_mat_back_workspace_size(...) bytes, 256-byte aligned; the two
+ * products run one after the other on `stream` and share it.  Every check of
+ * both products runs before anything is enqueued.
+ */
+size_t oop_mul_mat_back_workspace_size(int w_type, const int64_t ne_w[4],
+                                       const int64_t ne_x[4]);
+
+int oop_mul_mat_back(const void *W, int w_type, const float *x, const float *dy, float *dW,
+                     float *dx, const int64_t ne_w[4], const int64_t ne_x[4], void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/*
  * OUT_PROD from HOST buffers (no counterpart on the pages; the benchmark's
  * end-to-end figure goes through it): enqueues on `stream` the copies of a
  * and b into `device_buffer`, the product, and the copy of dst back into
