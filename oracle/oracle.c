@@ -23,6 +23,12 @@
  *    dx[k,i,t] = sum_r W_e[k,r] * g[r,i,t].
  *  - The fp16 staging defect ("metal: OUT_PROD multiplies in float staging",
  *    opening paragraph): inputs staged through half overflow past 65504.
+ *  - The other src0 types ("Metal kernel_mul_mat_id_back", first bullet:
+ *    out_prod's instantiation set f32, f16, bf16, q4_0, q4_1, q5_0, q5_1,
+ *    q8_0, q2_K .. q6_K; q4_K is the weight of the dense timings of "metal:
+ *    OUT_PROD multiplies in float staging", answer (2)).  The pages do not
+ *    spell the block layouts out; these are ggml's published formats, each
+ *    decoded below from its description, every value exact in fp64.
  */
 #include "oracle.h"
 
@@ -36,6 +42,7 @@
 #endif
 
 #define QK 32
+#define QK_K 256
 
 /* ------------------------------------------------------------------ */
 /* scalar decoders, written from the IEEE 754 binary16 definition      */
@@ -87,15 +94,131 @@ static uint16_t rd16(const uint8_t *p)
     return (uint16_t)(p[0] | ((uint16_t)p[1] << 8));
 }
 
+/* bytes of one block of each quantised type */
+static int block_bytes(int type)
+{
+    switch (type) {
+    case ORACLE_Q4_0: return 18;   /* d, 16 bytes of nibbles */
+    case ORACLE_Q4_1: return 20;   /* d, m, 16 bytes of nibbles */
+    case ORACLE_Q5_0: return 22;   /* d, 4 bytes of fifth bits, 16 bytes of nibbles */
+    case ORACLE_Q5_1: return 24;   /* d, m, 4 bytes of fifth bits, 16 bytes of nibbles */
+    case ORACLE_Q8_0: return 34;   /* d, 32 int8 */
+    case ORACLE_Q2_K: return 84;   /* 16 scale bytes, 64 code bytes, d, dmin */
+    case ORACLE_Q3_K: return 110;  /* 32 third-bit bytes, 64 code bytes, 12 scale bytes, d */
+    case ORACLE_Q4_K: return 144;  /* d, dmin, 12 scale bytes, 128 nibble bytes */
+    case ORACLE_Q5_K: return 176;  /* d, dmin, 12 scale bytes, 32 fifth-bit bytes, 128 nibbles */
+    case ORACLE_Q6_K: return 210;  /* 128 nibble bytes, 64 high-bit bytes, 16 int8 scales, d */
+    default: return -1;
+    }
+}
+
+int oracle_block_elems(int type)
+{
+    switch (type) {
+    case ORACLE_F32:
+    case ORACLE_F16:
+    case ORACLE_BF16: return 1;
+    case ORACLE_Q2_K:
+    case ORACLE_Q3_K:
+    case ORACLE_Q4_K:
+    case ORACLE_Q5_K:
+    case ORACLE_Q6_K: return QK_K;
+    default: return block_bytes(type) > 0 ? QK : -1;
+    }
+}
+
 static int64_t row_bytes(int type, int64_t n)
 {
     switch (type) {
     case ORACLE_F32: return 4 * n;
     case ORACLE_F16:
     case ORACLE_BF16: return 2 * n;
-    case ORACLE_Q8_0: return n / QK * 34;
-    case ORACLE_Q4_0: return n / QK * 18;
-    default: return -1;
+    default:
+        if (block_bytes(type) < 0) return -1;
+        return n / oracle_block_elems(type) * block_bytes(type);
+    }
+}
+
+/* ---- the K-quant super-blocks (256 elements in sub-blocks) ---------- */
+
+/* q4_K and q5_K keep eight 6-bit scales and eight 6-bit offsets in 12
+ * bytes: scale i and offset i of the first four sub-blocks are the low six
+ * bits of bytes i and i+4; for sub-blocks 4..7 the low four bits of scale
+ * and offset are the low and high nibbles of byte i+4 (i = sub-block), and
+ * their top two bits are the top two bits of bytes i-4 (scale) and i
+ * (offset). */
+static void k4_scale_offset(const uint8_t *s12, int sub, int *scale, int *offset)
+{
+    if (sub < 4) {
+        *scale = s12[sub] & 0x3f;
+        *offset = s12[sub + 4] & 0x3f;
+    } else {
+        *scale = (s12[sub + 4] & 0x0f) | ((s12[sub - 4] >> 6) << 4);
+        *offset = (s12[sub + 4] >> 4) | ((s12[sub] >> 6) << 4);
+    }
+}
+
+/* q3_K keeps sixteen 6-bit scales (stored plus 32) in 12 bytes: the low four
+ * bits of scale i are the low nibble of byte i for i < 8 and the high nibble
+ * of byte i-8 for i >= 8; the top two bits are bits 2*(i/4) .. 2*(i/4)+1 of
+ * byte 8 + i%4. */
+static int k3_scale(const uint8_t *s12, int i)
+{
+    int low = i < 8 ? (s12[i] & 0x0f) : (s12[i - 8] >> 4);
+    int high = (s12[8 + i % 4] >> (2 * (i / 4))) & 3;
+    return (low | (high << 4)) - 32;
+}
+
+/* element j (0..255) of a K-quant super-block */
+static double k_elem(int type, const uint8_t *blk, int j)
+{
+    const int sub = j / 32, l = j % 32;        /* 32-element sub-block, lane */
+    const int half = j / 128, g = (j % 128) / 32;
+    switch (type) {
+    case ORACLE_Q4_K:
+    case ORACLE_Q5_K: {
+        double d = oracle_half_to_double(rd16(blk));
+        double dmin = oracle_half_to_double(rd16(blk + 2));
+        int sc, off;
+        k4_scale_offset(blk + 4, sub, &sc, &off);
+        /* nibbles: byte 32*(sub/2) + l, low nibble for even sub-blocks */
+        const uint8_t *qs = blk + (type == ORACLE_Q4_K ? 16 : 48);
+        int q = (qs[32 * (sub / 2) + l] >> (4 * (sub % 2))) & 0x0f;
+        if (type == ORACLE_Q5_K) q += ((blk[16 + l] >> sub) & 1) * 16;
+        return d * sc * q - dmin * off;
+    }
+    case ORACLE_Q6_K: {
+        /* half h: low nibbles in bytes 64h.., two high bits in bytes 32h..,
+         * scales 8h..; group g of 32 elements: nibble byte 64h + l + 32(g%2),
+         * high nibble when g >= 2; high bits 2g..2g+1; scale 8h + l/16 + 2g */
+        const uint8_t *ql = blk, *qh = blk + 128;
+        const int8_t *sc = (const int8_t *)(blk + 192);
+        double d = oracle_half_to_double(rd16(blk + 208));
+        int byte = ql[64 * half + l + 32 * (g % 2)];
+        int low = g >= 2 ? (byte >> 4) : (byte & 0x0f);
+        int high = (qh[32 * half + l] >> (2 * g)) & 3;
+        int q = (low | (high << 4)) - 32;
+        return d * sc[8 * half + l / 16 + 2 * g] * q;
+    }
+    case ORACLE_Q2_K: {
+        /* element 128h + 32g + l: bits 2g..2g+1 of code byte 32h + l; scale
+         * byte 8h + 2g + l/16: low nibble times d, high nibble times dmin */
+        double d = oracle_half_to_double(rd16(blk + 80));
+        double dmin = oracle_half_to_double(rd16(blk + 82));
+        int q = (blk[16 + 32 * half + l] >> (2 * g)) & 3;
+        int s = blk[8 * half + 2 * g + l / 16];
+        return d * (s & 0x0f) * q - dmin * (s >> 4);
+    }
+    case ORACLE_Q3_K: {
+        /* element 128h + 32g + l: bits 2g..2g+1 of code byte 32 + 32h + l,
+         * minus 4 unless bit 4h + g of byte l is set; scale 8h + 2g + l/16 */
+        double d = oracle_half_to_double(rd16(blk + 108));
+        int q = (blk[32 + 32 * half + l] >> (2 * g)) & 3;
+        if (!((blk[l] >> (4 * half + g)) & 1)) q -= 4;
+        return d * k3_scale(blk + 96, 8 * half + 2 * g + l / 16) * q;
+    }
+    default:
+        return NAN;
     }
 }
 
@@ -126,6 +249,36 @@ static double elem(int type, const uint8_t *row, int64_t j)
         int v = jj < 16 ? (byte & 0x0f) : (byte >> 4);
         return d * (double)(v - 8);
     }
+    case ORACLE_Q4_1: {
+        /* d, m, then the nibbles as in q4_0; value d*v + m */
+        const uint8_t *blk = row + (j / QK) * 20;
+        int jj = (int)(j % QK);
+        uint8_t byte = blk[4 + (jj & 15)];
+        int v = jj < 16 ? (byte & 0x0f) : (byte >> 4);
+        return oracle_half_to_double(rd16(blk)) * v + oracle_half_to_double(rd16(blk + 2));
+    }
+    case ORACLE_Q5_0:
+    case ORACLE_Q5_1: {
+        /* header (d; or d, m), a 32-bit little-endian word whose bit jj is
+         * element jj's fifth bit, then the nibbles as in q4_0.
+         * q5_0: d*(v - 16); q5_1: d*v + m */
+        const int hdr = type == ORACLE_Q5_0 ? 2 : 4;
+        const uint8_t *blk = row + (j / QK) * block_bytes(type);
+        int jj = (int)(j % QK);
+        uint32_t qh = (uint32_t)blk[hdr] | ((uint32_t)blk[hdr + 1] << 8) |
+                      ((uint32_t)blk[hdr + 2] << 16) | ((uint32_t)blk[hdr + 3] << 24);
+        uint8_t byte = blk[hdr + 4 + (jj & 15)];
+        int v = (jj < 16 ? (byte & 0x0f) : (byte >> 4)) | (int)(((qh >> jj) & 1) << 4);
+        double d = oracle_half_to_double(rd16(blk));
+        if (type == ORACLE_Q5_0) return d * (v - 16);
+        return d * v + oracle_half_to_double(rd16(blk + 2));
+    }
+    case ORACLE_Q2_K:
+    case ORACLE_Q3_K:
+    case ORACLE_Q4_K:
+    case ORACLE_Q5_K:
+    case ORACLE_Q6_K:
+        return k_elem(type, row + (j / QK_K) * block_bytes(type), (int)(j % QK_K));
     default:
         return NAN;
     }
@@ -134,7 +287,7 @@ static double elem(int type, const uint8_t *row, int64_t j)
 int oracle_dequant_row(int type, const void *row, int64_t n, double *out)
 {
     if (!row || !out || n < 0 || row_bytes(type, n) < 0) return -1;
-    if ((type == ORACLE_Q8_0 || type == ORACLE_Q4_0) && n % QK) return -1;
+    if (n % oracle_block_elems(type)) return -1;
     for (int64_t j = 0; j < n; ++j) out[j] = elem(type, (const uint8_t *)row, j);
     return 0;
 }
@@ -160,11 +313,8 @@ static int check_shape(int a_type, const int64_t ne_a[4], const int64_t ne_b[4],
     if (s->ne12 % s->ne02 || s->ne13 % s->ne03) return -1;
     s->dps2 = s->ne12 / s->ne02;
     s->dps3 = s->ne13 / s->ne03;
-    if (a_type == ORACLE_Q8_0 || a_type == ORACLE_Q4_0) {
-        if (s->M % QK) return -1;
-    } else if (a_type != ORACLE_F32 && a_type != ORACLE_F16 && a_type != ORACLE_BF16) {
-        return -1;
-    }
+    if (oracle_block_elems(a_type) < 0) return -1;
+    if (s->M % oracle_block_elems(a_type)) return -1;
     s->rb = row_bytes(a_type, s->M);
     return 0;
 }

@@ -13,7 +13,8 @@
  *   a   (src0): ne_a = {M, K, ne02, ne03}, element a[m,k,j2,j3]
  *   b   (src1): ne_b = {N, K, ne12, ne13}, element b[n,k,i2,i3]
  *   dst       : {M, N, ne12, ne13},        element dst[m,n,i2,i3]
- * Quantised src0 stores each row of M elements as M/32 blocks of 32.
+ * Quantised src0 stores each row of M elements as M/QK blocks of QK (32, or
+ * 256 for the K-quants).
  *
  * Return codes: 0 = ok, -1 = bad argument (null, shape, type, broadcast).
  */
@@ -30,9 +31,21 @@ enum {
     ORACLE_F32 = 0,
     ORACLE_F16 = 1,
     ORACLE_Q4_0 = 2,
+    ORACLE_Q4_1 = 3,
+    ORACLE_Q5_0 = 6,
+    ORACLE_Q5_1 = 7,
     ORACLE_Q8_0 = 8,
+    ORACLE_Q2_K = 10,
+    ORACLE_Q3_K = 11,
+    ORACLE_Q4_K = 12,
+    ORACLE_Q5_K = 13,
+    ORACLE_Q6_K = 14,
     ORACLE_BF16 = 30
 };
+
+/* Elements per block of a type (1 for f32, f16, bf16; 32; 256 for the
+ * K-quants), or -1 for an unknown type. */
+int oracle_block_elems(int type);
 
 /* IEEE 754 binary16 bit pattern -> its exact value (Inf/NaN included). */
 double oracle_half_to_double(uint16_t h);

@@ -556,3 +556,93 @@ def test_mul_mat_back_dw_is_out_prod_over_grouped_slices(orc, ne_w, ne_x):
                        (R, group * T, w2, w3))
     for key in ("dst", "f64", "abs"):
         assert np.array_equal(out["dW"][key], ref[key]), key
+
+
+# --------------------------------------------------------------------------
+# the other src0 types ("Metal kernel_mul_mat_id_back", first bullet: out_prod's
+# instantiation set; q4_K: "metal: OUT_PROD multiplies in float staging",
+# answer (2)).  The oracle's decoders and synth's quantisers are separate
+# implementations of each block layout; these pins tie them together on data
+# that makes a misplaced bit, nibble or scale index show up as a gross error.
+# --------------------------------------------------------------------------
+
+_LEVELS = {synth.TYPE_Q4_0: 15, synth.TYPE_Q4_1: 15, synth.TYPE_Q5_0: 31,
+           synth.TYPE_Q5_1: 31, synth.TYPE_Q8_0: 254, synth.TYPE_Q2_K: 3,
+           synth.TYPE_Q3_K: 7, synth.TYPE_Q4_K: 15, synth.TYPE_Q5_K: 31,
+           synth.TYPE_Q6_K: 63}
+_SUB = {synth.TYPE_Q2_K: 16, synth.TYPE_Q3_K: 16, synth.TYPE_Q6_K: 16}
+
+
+def _graded(rows, ne0, sub, seed, offset, grades=8):
+    """Normals whose consecutive `sub`-element groups are scaled by
+    2^(i % grades) (and, with `offset`, shifted by a group-dependent amount)."""
+    x = synth.normal(seed, rows * ne0).reshape(rows, ne0).astype(np.float64)
+    g = np.arange(ne0) // sub
+    x *= 2.0 ** (g % grades)
+    if offset:
+        x += 0.5 * (2.0 ** (g % grades)) * ((g % 3) - 1)
+    return x.astype(np.float32)
+
+
+@pytest.mark.parametrize("tid", sorted(_LEVELS))
+def test_quantiser_decoder_round_trip(orc, tid):
+    """dequant(quant(x)) stays within about one code step of x in every group
+    of elements that shares a scale; a decoder reading the wrong scale, nibble
+    or bit would be off by the magnitude of another group (2x to 128x)."""
+    qk, _ = synth.BLOCK[tid]
+    sub = _SUB.get(tid, 32)
+    ne0, rows = 2 * 256, 6
+    # a K-quant's sub-block scales are 6-bit (4-bit for q2_K) multiples of one
+    # super-block scale, so its groups may differ by 8x at most
+    grades = 4 if qk == 256 else 8
+    for offset in (False, True):
+        x = _graded(rows, ne0, sub, 140 + tid, offset, grades)
+        q = synth.quantize(tid, x)
+        deq = np.stack([orc.dequant_row(tid, q[r], ne0) for r in range(rows)])
+        xs = x.astype(np.float64).reshape(rows, -1, sub)
+        ds = deq.reshape(rows, -1, sub)
+        span = np.maximum(xs.max(axis=2), 0) - np.minimum(xs.min(axis=2), 0)
+        # one code step of the group, widened for the binary16 / 6-bit scale
+        # rounding; a group's neighbours differ from it by a factor of 2 or more
+        err = np.abs(ds - xs).max(axis=2)
+        ratio = float((err / np.maximum(span / _LEVELS[tid], 1e-30)).max())
+        assert ratio <= 1.25, (tid, offset, ratio)
+
+
+@pytest.mark.parametrize("tid", sorted(_LEVELS))
+def test_decoder_scales_with_the_block_scales(orc, tid):
+    """Multiplying every binary16 scale field of a block by 2 (exponent + 1)
+    doubles every decoded element (the scales multiply every term)."""
+    qk, nbytes = synth.BLOCK[tid]
+    x = _graded(2, 256, _SUB.get(tid, 32), 150 + tid, True, 4)
+    q = synth.quantize(tid, x).reshape(-1, nbytes).copy()
+    fields = {synth.TYPE_Q4_0: [0], synth.TYPE_Q4_1: [0, 2], synth.TYPE_Q5_0: [0],
+              synth.TYPE_Q5_1: [0, 2], synth.TYPE_Q8_0: [0], synth.TYPE_Q2_K: [80, 82],
+              synth.TYPE_Q3_K: [108], synth.TYPE_Q4_K: [0, 2], synth.TYPE_Q5_K: [0, 2],
+              synth.TYPE_Q6_K: [208]}[tid]
+    before = np.stack([orc.dequant_row(tid, b, qk) for b in q])
+    q2 = q.copy()
+    for off in fields:
+        h = q2[:, off:off + 2].copy().view(np.uint16)[:, 0]
+        exp = (h >> 10) & 31
+        assert np.all((exp > 0) & (exp < 30)), "normal scales only"
+        q2[:, off:off + 2] = (h + (1 << 10)).astype(np.uint16).view(np.uint8).reshape(-1, 2)
+    after = np.stack([orc.dequant_row(tid, b, qk) for b in q2])
+    assert np.array_equal(after, 2 * before)
+
+
+@pytest.mark.parametrize("tid", [synth.TYPE_F16, synth.TYPE_BF16])
+def test_plain_16bit_types_out_prod(orc, tid):
+    """f16 / bf16 src0: OUT_PROD equals numpy's float64 product of numpy's own
+    decoding of the 16-bit patterns."""
+    ne_a, ne_b = (40, 33, 1, 1), (9, 33, 1, 1)
+    x = synth.normal(160, 40 * 33).reshape(1, 1, 33, 40)
+    bits = synth.quantize(tid, x)
+    if tid == synth.TYPE_F16:
+        vals = bits.view(np.float16).astype(np.float64)
+    else:
+        vals = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    b = synth.make_b(ne_b, 161)
+    r = orc.out_prod(bits, tid, b, ne_a, ne_b)
+    ref = np.einsum("km,kn->nm", vals[0, 0], b[0, 0].astype(np.float64))
+    assert np.all(np.abs(r["f64"][0, 0] - ref) <= 1e-13 * r["abs"][0, 0])
