@@ -19,8 +19,17 @@ import threading
 from . import _build
 
 TYPE_F32 = 0
+TYPE_F16 = 1
 TYPE_Q4_0 = 2
+TYPE_Q4_1 = 3
+TYPE_Q5_0 = 6
+TYPE_Q5_1 = 7
 TYPE_Q8_0 = 8
+TYPE_Q2_K = 10
+TYPE_Q3_K = 11
+TYPE_Q4_K = 12
+TYPE_Q5_K = 13
+TYPE_Q6_K = 14
 TYPE_BF16 = 30
 
 PATH_AUTO = 0
@@ -49,8 +58,13 @@ ERR_DEVICE = -10
 ERR_PATH = -11
 ERR_SCRATCH_LIMIT = -12
 
-_QK = 32
-_BLOCK_BYTES = {TYPE_Q8_0: 34, TYPE_Q4_0: 18}
+# (elements, bytes) per block of the quantised types; the plain 16-bit types
+# are tensors of 2-byte elements
+_BLOCKS = {TYPE_Q4_0: (32, 18), TYPE_Q4_1: (32, 20), TYPE_Q5_0: (32, 22),
+           TYPE_Q5_1: (32, 24), TYPE_Q8_0: (32, 34), TYPE_Q2_K: (256, 84),
+           TYPE_Q3_K: (256, 110), TYPE_Q4_K: (256, 144), TYPE_Q5_K: (256, 176),
+           TYPE_Q6_K: (256, 210)}
+_HALF_TYPES = (TYPE_F16, TYPE_BF16)
 
 _lock = threading.Lock()
 _lib = None
@@ -297,13 +311,25 @@ def _ptr(t):
 
 
 def ne_of(t, type_id=TYPE_F32, ne0=None):
-    """ggml ne of a contiguous tensor in this layout."""
+    """ggml ne of a contiguous tensor in this layout (a quantised src0's last
+    axis holds one row's block bytes)."""
     shp = (1,) * (4 - t.dim()) + tuple(t.shape)
-    if type_id in _BLOCK_BYTES:
+    if type_id in _BLOCKS:
         if ne0 is None:
-            ne0 = shp[3] // _BLOCK_BYTES[type_id] * _QK
+            qk, nbytes = _BLOCKS[type_id]
+            ne0 = shp[3] // nbytes * qk
         return (ne0, shp[2], shp[1], shp[0])
     return (shp[3], shp[2], shp[1], shp[0])
+
+
+def _check_src0(t, type_id, name):
+    torch = _torch()
+    if type_id == TYPE_F32 and t.dtype != torch.float32:
+        raise ValueError(f"f32 {name} must be a float32 tensor")
+    if type_id in _HALF_TYPES and t.element_size() != 2:
+        raise ValueError(f"f16 / bf16 {name} must hold 2-byte elements")
+    if type_id in _BLOCKS and t.dtype != torch.uint8:
+        raise ValueError(f"quantised {name} must be a uint8 tensor of block bytes")
 
 
 def _check_cuda(t, name, contiguous=True):
@@ -334,7 +360,8 @@ def out_prod(a, b, a_type=None, ne_a=None, out=None, workspace=None, stream=None
              path=PATH_AUTO):
     """dst = OUT_PROD(a, b) on a's device and the current (or given) stream.
 
-    a: float32 tensor, or uint8 q8_0/q4_0 rows (give ``a_type``); b: float32,
+    a: float32 tensor, a tensor of 2-byte f16 / bf16 elements, or uint8 rows of
+    quantised blocks (give ``a_type``); b: float32,
     contiguous or any view with non-negative strides (a transpose, a slice),
     which is read in place through oop_out_prod_strided.
     Returns dst, float32 of shape (ne13, ne12, N, M)."""
@@ -345,10 +372,7 @@ def out_prod(a, b, a_type=None, ne_a=None, out=None, workspace=None, stream=None
     _check_cuda(b, "b", contiguous=False)
     if b.dtype != torch.float32:
         raise ValueError("b must be float32")
-    if a_type == TYPE_F32 and a.dtype != torch.float32:
-        raise ValueError("f32 src0 must be a float32 tensor")
-    if a_type in _BLOCK_BYTES and a.dtype != torch.uint8:
-        raise ValueError("quantised src0 must be a uint8 tensor of block bytes")
+    _check_src0(a, a_type, "src0")
     if ne_a is None:
         ne_a = ne_of(a, a_type)
     ne_b = ne_of(b)
@@ -391,6 +415,7 @@ def mul_mat_back(W, x, dy, w_type=None, ne_w=None, want_dW=True, want_dx=True,
         _check_cuda(t, n)
     if x.dtype != torch.float32 or dy.dtype != torch.float32:
         raise ValueError("x and dy must be float32")
+    _check_src0(W, w_type, "W")
     if ne_w is None:
         ne_w = ne_of(W, w_type)
     ne_x = ne_of(x)

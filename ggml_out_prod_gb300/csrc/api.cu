@@ -80,13 +80,9 @@ int device_setup(int **status) {
 bool aligned(const void *p, uintptr_t n) { return reinterpret_cast<uintptr_t>(p) % n == 0; }
 
 int64_t row_bytes(int type, int64_t n) {
-    switch (type) {
-    case OOP_TYPE_F32: return 4 * n;
-    case OOP_TYPE_BF16: return 2 * n;
-    case OOP_TYPE_Q8_0: return n / kQK * kQ8Bytes;
-    case OOP_TYPE_Q4_0: return n / kQK * kQ4Bytes;
-    default: return -1;
-    }
+    const int qk = type_block_elems(type);
+    if (qk < 0) return -1;
+    return n / qk * type_block_bytes(type);
 }
 
 // Shape checks shared by the size query and the call.
@@ -95,12 +91,11 @@ int check_out_prod_shape(int a_type, const int64_t ne_a[4], const int64_t ne_b[4
     if (!ne_a || !ne_b) return OOP_ERR_NULL;
     for (int i = 0; i < 4; ++i)
         if (ne_a[i] < 0 || ne_b[i] < 0) return OOP_ERR_SHAPE;
-    if (a_type != OOP_TYPE_F32 && a_type != OOP_TYPE_Q8_0 && a_type != OOP_TYPE_Q4_0)
-        return OOP_ERR_TYPE;
+    if (type_block_elems(a_type) < 0) return OOP_ERR_TYPE;
     if (ne_a[1] != ne_b[1]) return OOP_ERR_SHAPE;
     if (ne_a[2] < 1 || ne_a[3] < 1) return OOP_ERR_BROADCAST;
     if (ne_b[2] % ne_a[2] != 0 || ne_b[3] % ne_a[3] != 0) return OOP_ERR_BROADCAST;
-    if (a_type != OOP_TYPE_F32 && ne_a[0] % kQK != 0) return OOP_ERR_SHAPE;
+    if (ne_a[0] % type_block_elems(a_type) != 0) return OOP_ERR_SHAPE;
     // element counts must fit comfortably in int64 arithmetic
     const double big = 9.0e18;
     if (static_cast<double>(ne_a[0]) * ne_a[1] * ne_a[2] * ne_a[3] * 4.0 > big ||

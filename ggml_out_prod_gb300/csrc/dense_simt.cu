@@ -4,10 +4,11 @@
 // k in steps of 16, each thread 8 m x 4 n outputs, fp32 FMA.  Each 16-term
 // partial sum is folded into a Kahan pair, so one gradient entry of 1e5
 // dominating a long sum does not carry sqrt(K) roundings of its size.
-// q8_0 / q4_0 src0 is dequantised while its tile is staged.  It is kept as a second,
+// A quantised or 16-bit src0 is decoded while its tile is staged.  It is kept as a second,
 // independent GPU path for cross-checks of the tensor-core kernel and for
 // devices paths that the tensor-core kernel rejects; it is not the fast path.
 #include "oop_internal.cuh"
+#include "quant.cuh"
 
 namespace oop {
 namespace {
@@ -23,23 +24,8 @@ struct SimtArgs {
 
 template <int TYPE>
 __device__ __forceinline__ float a_elem(const uint8_t *row, int64_t m) {
-    if constexpr (TYPE == OOP_TYPE_F32) {
-        return __ldg(reinterpret_cast<const float *>(row) + m);
-    } else if constexpr (TYPE == OOP_TYPE_Q8_0) {
-        const uint8_t *blk = row + (m / kQK) * kQ8Bytes;
-        const uint16_t d = static_cast<uint16_t>(__ldg(blk)) |
-                           (static_cast<uint16_t>(__ldg(blk + 1)) << 8);
-        const int8_t q = static_cast<int8_t>(__ldg(blk + 2 + m % kQK));
-        return half_bits_to_float(d) * static_cast<float>(q);
-    } else {
-        const uint8_t *blk = row + (m / kQK) * kQ4Bytes;
-        const uint16_t d = static_cast<uint16_t>(__ldg(blk)) |
-                           (static_cast<uint16_t>(__ldg(blk + 1)) << 8);
-        const int j = static_cast<int>(m % kQK);
-        const uint8_t byte = __ldg(blk + 2 + (j & 15));
-        const int v = j < 16 ? (byte & 0x0f) : (byte >> 4);
-        return half_bits_to_float(d) * static_cast<float>(v - 8);
-    }
+    if constexpr (TYPE == OOP_TYPE_F32) return __ldg(reinterpret_cast<const float *>(row) + m);
+    else return decode_row<TYPE>(row, m);
 }
 
 template <int TYPE>
@@ -144,9 +130,22 @@ cudaError_t launch_dense_simt(const void *a, const float *b, float *dst, const O
     if (gy > 65535 || slices > 65535 || gx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(slices));
     switch (s.a_type) {
-    case OOP_TYPE_F32: simt_kernel<OOP_TYPE_F32><<<grid, THREADS, 0, stream>>>(p); break;
-    case OOP_TYPE_Q8_0: simt_kernel<OOP_TYPE_Q8_0><<<grid, THREADS, 0, stream>>>(p); break;
-    case OOP_TYPE_Q4_0: simt_kernel<OOP_TYPE_Q4_0><<<grid, THREADS, 0, stream>>>(p); break;
+#define OOP_SIMT_CASE(T) \
+    case T: simt_kernel<T><<<grid, THREADS, 0, stream>>>(p); break;
+    OOP_SIMT_CASE(OOP_TYPE_F32)
+    OOP_SIMT_CASE(OOP_TYPE_F16)
+    OOP_SIMT_CASE(OOP_TYPE_BF16)
+    OOP_SIMT_CASE(OOP_TYPE_Q4_0)
+    OOP_SIMT_CASE(OOP_TYPE_Q4_1)
+    OOP_SIMT_CASE(OOP_TYPE_Q5_0)
+    OOP_SIMT_CASE(OOP_TYPE_Q5_1)
+    OOP_SIMT_CASE(OOP_TYPE_Q8_0)
+    OOP_SIMT_CASE(OOP_TYPE_Q2_K)
+    OOP_SIMT_CASE(OOP_TYPE_Q3_K)
+    OOP_SIMT_CASE(OOP_TYPE_Q4_K)
+    OOP_SIMT_CASE(OOP_TYPE_Q5_K)
+    OOP_SIMT_CASE(OOP_TYPE_Q6_K)
+#undef OOP_SIMT_CASE
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

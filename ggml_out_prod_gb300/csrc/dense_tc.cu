@@ -68,6 +68,7 @@
 #include <mutex>
 
 #include "oop_internal.cuh"
+#include "quant.cuh"
 #include "tc_ptx.cuh"
 
 namespace oop {
@@ -98,42 +99,37 @@ constexpr uint64_t WAIT_NS = 1000000000ull;
 constexpr int MAX_RSTAGES = 4;
 
 // Raw src0 staging per type: one TMA box covers 32 k rows of one m-tile.
-// Quantised rows: the tile's 4 blocks (136 or 72 bytes) start 0 or 8 bytes
-// past a 16-byte boundary, so the box is 8 bytes wider than the blocks.
+// Plain types (f32, f16, bf16): the tile's 128 elements of each row.  Blocks
+// of 32: the tile's four blocks; blocks of 256 (K-quants): the whole
+// super-block that the tile is one half of (its scales sit at the block's
+// start).  Those bytes start `off0` past a 16-byte boundary (TMA's rule), so
+// the box reaches back to the boundary and is as much wider as the largest
+// such offset needs.
+constexpr int gcd16(int x) { return (x % 16 == 0) ? 16 : (x % 8 == 0) ? 8 : (x % 4 == 0) ? 4 : (x % 2 == 0) ? 2 : 1; }
+
 template <int TYPE>
-struct RawA;
-template <>
-struct RawA<OOP_TYPE_F32> {
-    static constexpr int BLOCK = 0;
-    static constexpr int BOX_X = BM;                 // f32 elements
-    static constexpr int ROW_BYTES = BM * 4;         // bytes per staged k row
-    static constexpr int SLOT = ROW_BYTES * BK;      // 16 KB
-    static constexpr int RSTAGES = 3;
+struct RawA {
+    using F = QFormat<TYPE>;
+    static constexpr bool PLAIN = F::QK == 1;
+    static constexpr int BLOCK = F::BYTES;
+    // the bytes of a row one m-tile needs, and how far past a 16-byte boundary
+    // they may start
+    static constexpr int SPAN = PLAIN ? BM * F::BYTES : (F::QK == 32 ? 4 * F::BYTES : F::BYTES);
+    static constexpr int MAXOFF = PLAIN ? 0 : 16 - gcd16(F::QK == 32 ? 4 * F::BYTES : F::BYTES);
+    static constexpr int ROW_BYTES = (SPAN + MAXOFF + 15) / 16 * 16;   // bytes per staged k row
+    static constexpr int BOX_X = PLAIN ? BM : ROW_BYTES;              // in map elements
+    static constexpr int SLOT = (ROW_BYTES * BK + 1023) / 1024 * 1024;
+    static constexpr int RSTAGES = TYPE == OOP_TYPE_F32 ? 3 : 4;
 };
-template <>
-struct RawA<OOP_TYPE_BF16> {
-    static constexpr int BLOCK = 0;
-    static constexpr int BOX_X = BM;                 // bf16 elements
-    static constexpr int ROW_BYTES = BM * 2;
-    static constexpr int SLOT = ROW_BYTES * BK;      // 8 KB
-    static constexpr int RSTAGES = 4;
-};
-template <>
-struct RawA<OOP_TYPE_Q8_0> {
-    static constexpr int BLOCK = kQ8Bytes;
-    static constexpr int BOX_X = 4 * kQ8Bytes + 8;   // 144 bytes
-    static constexpr int ROW_BYTES = BOX_X;
-    static constexpr int SLOT = 5120;                // 144 * 32 rounded to 1 KB
-    static constexpr int RSTAGES = 4;
-};
-template <>
-struct RawA<OOP_TYPE_Q4_0> {
-    static constexpr int BLOCK = kQ4Bytes;
-    static constexpr int BOX_X = 4 * kQ4Bytes + 8;   // 80 bytes
-    static constexpr int ROW_BYTES = BOX_X;
-    static constexpr int SLOT = 3072;                // 80 * 32 rounded to 1 KB
-    static constexpr int RSTAGES = 4;
-};
+
+// Byte offset, in a src0 row, of the first byte m-tile `mt` needs.
+template <int TYPE>
+__host__ __device__ __forceinline__ int64_t raw_tile_byte0(int64_t mt) {
+    using F = QFormat<TYPE>;
+    if constexpr (F::QK == 1) return mt * BM * F::BYTES;
+    else if constexpr (F::QK == 32) return mt * 4 * F::BYTES;
+    else return (mt >> 1) * F::BYTES;
+}
 
 struct Bars {
     // Iteration g (one k-block of one tile) uses ring slot g % RSTAGES, B
@@ -152,7 +148,7 @@ struct Bars {
 };
 
 template <int TYPE>
-constexpr bool elementwise_type() { return TYPE == OOP_TYPE_F32 || TYPE == OOP_TYPE_BF16; }
+constexpr bool elementwise_type() { return is_plain_type<TYPE>(); }
 
 template <int TYPE>
 constexpr size_t smem_bytes() {
@@ -268,23 +264,7 @@ struct Ring {
 
 template <int TYPE>
 __device__ __forceinline__ float load_a(const uint8_t *row, int64_t m) {
-    if constexpr (TYPE == OOP_TYPE_F32) {
-        return __ldg(reinterpret_cast<const float *>(row) + m);
-    } else if constexpr (TYPE == OOP_TYPE_BF16) {
-        return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short *>(row) + m));
-    } else if constexpr (TYPE == OOP_TYPE_Q8_0) {
-        const uint8_t *blk = row + (m >> 5) * kQ8Bytes;
-        const uint16_t d = __ldg(reinterpret_cast<const unsigned short *>(blk));
-        const int8_t q = static_cast<int8_t>(__ldg(blk + 2 + (m & 31)));
-        return half_bits_to_float(d) * static_cast<float>(q);
-    } else {
-        const uint8_t *blk = row + (m >> 5) * kQ4Bytes;
-        const uint16_t d = __ldg(reinterpret_cast<const unsigned short *>(blk));
-        const int j = static_cast<int>(m & 31);
-        const uint8_t byte = __ldg(blk + 2 + (j & 15));
-        const int v = j < 16 ? (byte & 0x0f) : (byte >> 4);
-        return half_bits_to_float(d) * static_cast<float>(v - 8);
-    }
+    return decode_row<TYPE>(row, m);
 }
 
 // The 16 src0 values (k rows 16*kh .. 16*kh+15 of a staged k-block) of row
@@ -293,17 +273,29 @@ __device__ __forceinline__ float load_a(const uint8_t *row, int64_t m) {
 // reads k row j) and passed around with shuffles.
 template <int TYPE>
 __device__ __forceinline__ void staged_half(const uint8_t *slot, int r, int off0, int lane,
-                                            int kh, float (&x)[KH]) {
+                                            int kh, float (&x)[KH], int mt) {
     using Raw = RawA<TYPE>;
     const uint8_t *rows = slot + kh * KH * Raw::ROW_BYTES;
     if constexpr (TYPE == OOP_TYPE_F32) {
 #pragma unroll
         for (int j = 0; j < KH; ++j)
             x[j] = reinterpret_cast<const float *>(rows + j * Raw::ROW_BYTES)[r];
-    } else if constexpr (TYPE == OOP_TYPE_BF16) {
+    } else if constexpr (Raw::PLAIN) {
 #pragma unroll
-        for (int j = 0; j < KH; ++j)
-            x[j] = bf16_bits_to_float(reinterpret_cast<const uint16_t *>(rows + j * Raw::ROW_BYTES)[r]);
+        for (int j = 0; j < KH; ++j) x[j] = decode<TYPE>(rows + j * Raw::ROW_BYTES + 2 * r, 0);
+    } else if constexpr (TYPE != OOP_TYPE_Q8_0 && TYPE != OOP_TYPE_Q4_0) {
+        // the other block types: each thread decodes its own element of
+        // every row (the block header reads are warp-wide broadcasts)
+        if constexpr (QFormat<TYPE>::QK == 32) {
+            const uint8_t *blk = rows + off0 + (r >> 5) * Raw::BLOCK;
+#pragma unroll
+            for (int j = 0; j < KH; ++j) x[j] = decode<TYPE>(blk + j * Raw::ROW_BYTES, lane);
+        } else {
+            const uint8_t *blk = rows + off0;
+            const int e = (mt & 1) * BM + r;                 // element in the super-block
+#pragma unroll
+            for (int j = 0; j < KH; ++j) x[j] = decode<TYPE>(blk + j * Raw::ROW_BYTES, e);
+        }
     } else {
         const uint8_t *blk = rows + off0 + (r >> 5) * Raw::BLOCK;
         const float dl = half_bits_to_float(
@@ -347,7 +339,7 @@ __global__ void __maxnreg__(MAX_REGS)
                        const __grid_constant__ CUtensorMap map_blo,
                        const __grid_constant__ CUtensorMap map_a, const TcParams p) {
     using Raw = RawA<TYPE>;
-    constexpr bool HAS_ALO = TYPE != OOP_TYPE_BF16;   // bf16 values are TF32 values
+    constexpr bool HAS_ALO = !is_tf32_exact<TYPE>();   // bf16 / f16 values are TF32 values
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -450,7 +442,7 @@ __global__ void __maxnreg__(MAX_REGS)
                 if constexpr (TMA_A) {
                     const int box_x = elementwise_type<TYPE>()
                                           ? t.mt * BM
-                                          : ((t.mt * 4 * Raw::BLOCK) & ~15);
+                                          : static_cast<int>(raw_tile_byte0<TYPE>(t.mt) & ~15);
                     ptx::tma_load_2d(ring + r * Raw::SLOT, &map_a, &bars->rfull[r], box_x,
                                      static_cast<int>(t.a_row0 + static_cast<int64_t>(w.kb) * BK));
                 }
@@ -597,12 +589,10 @@ __global__ void __maxnreg__(MAX_REGS)
             }
             if constexpr (TMA_A) {
                 int off0 = 0;
-                if constexpr (!elementwise_type<TYPE>()) {
-                    const int byte0 = t.mt * 4 * Raw::BLOCK;
-                    off0 = byte0 - (byte0 & ~15);
-                }
+                if constexpr (!elementwise_type<TYPE>())
+                    off0 = static_cast<int>(raw_tile_byte0<TYPE>(t.mt) & 15);
                 __syncwarp();
-                staged_half<TYPE>(ring + rs * Raw::SLOT, r, off0, lane, kh, x);
+                staged_half<TYPE>(ring + rs * Raw::SLOT, r, off0, lane, kh, x, t.mt);
                 // rows past M and k past K read whatever the box holds there
                 if (!(__all_sync(0xffffffffu, mok) && kfull)) {
 #pragma unroll
@@ -637,11 +627,11 @@ __global__ void __maxnreg__(MAX_REGS)
                 ptx::unpack2(ptx::sub2(ptx::pack2(x[e], x[e + 1]),
                                        ptx::pack2(__uint_as_float(hi[e]), __uint_as_float(hi[e + 1]))),
                              r0, r1);
-                if constexpr (TYPE == OOP_TYPE_F32) {
+                if constexpr (split_needs_rounding<TYPE>()) {
                     lo[e] = ptx::tf32_round_bits(__float_as_uint(r0));
                     lo[e + 1] = ptx::tf32_round_bits(__float_as_uint(r1));
                 } else {
-                    // d*q has at most 18 significant bits: x - hi is already
+                    // d*q has at most 22 significant bits: x - hi is already
                     // a TF32 value, no second rounding needed
                     lo[e] = __float_as_uint(r0);
                     lo[e + 1] = __float_as_uint(r1);
@@ -1108,7 +1098,7 @@ bool make_a_map(CUtensorMap *map, const void *base, const OutProdShape &s) {
     if constexpr (elementwise_type<TYPE>()) {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.M), static_cast<cuuint64_t>(rows)};
         const CUtensorMapDataType dt = TYPE == OOP_TYPE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+                                                             : CU_TENSOR_MAP_DATA_TYPE_UINT16;
         return fn(map, dt, 2, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1304,15 +1294,22 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
                                         static_cast<unsigned>(slices));
 
     switch (s.a_type) {
-    case OOP_TYPE_F32:
-        e = launch_typed<OOP_TYPE_F32, false>(a, s, mhi, mlo, p, grid, stream);
-        break;
-    case OOP_TYPE_Q8_0:
-        e = launch_typed<OOP_TYPE_Q8_0, false>(a, s, mhi, mlo, p, grid, stream);
-        break;
-    case OOP_TYPE_Q4_0:
-        e = launch_typed<OOP_TYPE_Q4_0, false>(a, s, mhi, mlo, p, grid, stream);
-        break;
+#define OOP_TC_CASE(T) \
+    case T: e = launch_typed<T, false>(a, s, mhi, mlo, p, grid, stream); break;
+    OOP_TC_CASE(OOP_TYPE_F32)
+    OOP_TC_CASE(OOP_TYPE_F16)
+    OOP_TC_CASE(OOP_TYPE_BF16)
+    OOP_TC_CASE(OOP_TYPE_Q4_0)
+    OOP_TC_CASE(OOP_TYPE_Q4_1)
+    OOP_TC_CASE(OOP_TYPE_Q5_0)
+    OOP_TC_CASE(OOP_TYPE_Q5_1)
+    OOP_TC_CASE(OOP_TYPE_Q8_0)
+    OOP_TC_CASE(OOP_TYPE_Q2_K)
+    OOP_TC_CASE(OOP_TYPE_Q3_K)
+    OOP_TC_CASE(OOP_TYPE_Q4_K)
+    OOP_TC_CASE(OOP_TYPE_Q5_K)
+    OOP_TC_CASE(OOP_TYPE_Q6_K)
+#undef OOP_TC_CASE
     default:
         return cudaErrorInvalidValue;
     }

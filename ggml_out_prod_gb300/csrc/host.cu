@@ -40,12 +40,9 @@ struct HostLayout {
 
 int64_t src0_bytes(int a_type, const int64_t ne_a[4]) {
     const int64_t rows = ne_a[1] * ne_a[2] * ne_a[3];
-    switch (a_type) {
-    case OOP_TYPE_F32: return 4 * ne_a[0] * rows;
-    case OOP_TYPE_Q8_0: return ne_a[0] / 32 * 34 * rows;
-    case OOP_TYPE_Q4_0: return ne_a[0] / 32 * 18 * rows;
-    default: return -1;
-    }
+    const int qk = type_block_elems(a_type);
+    if (qk < 0) return -1;
+    return ne_a[0] / qk * type_block_bytes(a_type) * rows;
 }
 
 bool plan_host(int a_type, const int64_t ne_a[4], const int64_t ne_b[4], HostLayout *L) {

@@ -12,9 +12,36 @@
 
 namespace oop {
 
-constexpr int kQK = 32;           // elements per q8_0 / q4_0 block
-constexpr int kQ8Bytes = 34;      // fp16 scale + 32 int8
-constexpr int kQ4Bytes = 18;      // fp16 scale + 16 packed bytes
+
+// Elements and bytes per block of a src0 type (1 and the element size for the
+// plain types), -1 for an unknown type.  Host and device.
+__host__ __device__ constexpr int type_block_elems(int type) {
+    switch (type) {
+    case OOP_TYPE_F32: case OOP_TYPE_F16: case OOP_TYPE_BF16: return 1;
+    case OOP_TYPE_Q4_0: case OOP_TYPE_Q4_1: case OOP_TYPE_Q5_0: case OOP_TYPE_Q5_1:
+    case OOP_TYPE_Q8_0: return 32;
+    case OOP_TYPE_Q2_K: case OOP_TYPE_Q3_K: case OOP_TYPE_Q4_K: case OOP_TYPE_Q5_K:
+    case OOP_TYPE_Q6_K: return 256;
+    default: return -1;
+    }
+}
+__host__ __device__ constexpr int type_block_bytes(int type) {
+    switch (type) {
+    case OOP_TYPE_F32: return 4;
+    case OOP_TYPE_F16: case OOP_TYPE_BF16: return 2;
+    case OOP_TYPE_Q4_0: return 18;
+    case OOP_TYPE_Q4_1: return 20;
+    case OOP_TYPE_Q5_0: return 22;
+    case OOP_TYPE_Q5_1: return 24;
+    case OOP_TYPE_Q8_0: return 34;
+    case OOP_TYPE_Q2_K: return 84;
+    case OOP_TYPE_Q3_K: return 110;
+    case OOP_TYPE_Q4_K: return 144;
+    case OOP_TYPE_Q5_K: return 176;
+    case OOP_TYPE_Q6_K: return 210;
+    default: return -1;
+    }
+}
 
 // One OUT_PROD call after validation.  Slice (i2, i3) of dst reads src0
 // slice (i2/dps2, i3/dps3): the CPU backend's broadcast map ("metal: OUT_PROD

@@ -42,13 +42,36 @@ extern "C" {
 #endif
 
 /* Element types.  The numbers are ggml's public type ids, so a ggml caller
- * passes its own tensor type unchanged. */
+ * passes its own tensor type unchanged; the block layouts are ggml's
+ * published formats ("Metal kernel_mul_mat_id_back", first bullet: out_prod
+ * is instantiated for all of these).  Blocks run along ne0, so a quantised
+ * src0 needs ne0 % 32 == 0 (% 256 for the K-quants).  Little-endian fields;
+ * d, m, dmin are binary16. */
 typedef enum {
     OOP_TYPE_F32 = 0,
-    OOP_TYPE_Q4_0 = 2,  /* 18-byte blocks of 32: fp16 d, 16 bytes; byte j holds
+    OOP_TYPE_F16 = 1,
+    OOP_TYPE_Q4_0 = 2,  /* 18-byte blocks of 32: d, 16 bytes; byte j holds
                            element j (low nibble) and j+16 (high nibble);
                            value = d * (nibble - 8) */
-    OOP_TYPE_Q8_0 = 8,  /* 34-byte blocks of 32: fp16 d, 32 int8 q; value = d*q */
+    OOP_TYPE_Q4_1 = 3,  /* 20-byte blocks of 32: d, m, nibbles as q4_0;
+                           value = d * nibble + m */
+    OOP_TYPE_Q5_0 = 6,  /* 22-byte blocks of 32: d, a 32-bit word whose bit j is
+                           element j's fifth bit, nibbles as q4_0;
+                           value = d * (v - 16), v = nibble | fifth << 4 */
+    OOP_TYPE_Q5_1 = 7,  /* 24-byte blocks of 32: d, m, fifth bits, nibbles;
+                           value = d * v + m */
+    OOP_TYPE_Q8_0 = 8,  /* 34-byte blocks of 32: d, 32 int8 q; value = d*q */
+    OOP_TYPE_Q2_K = 10, /* 84-byte blocks of 256: 16 bytes of 4-bit scale and
+                           offset per 16 elements, 64 bytes of 2-bit codes, d, dmin */
+    OOP_TYPE_Q3_K = 11, /* 110-byte blocks of 256: 32 bytes of third bits, 64 bytes
+                           of 2-bit codes, 12 bytes of 6-bit scales, d */
+    OOP_TYPE_Q4_K = 12, /* 144-byte blocks of 256: d, dmin, 12 bytes of 6-bit scales
+                           and offsets per 32 elements, 128 bytes of 4-bit codes;
+                           value = d * scale * code - dmin * offset */
+    OOP_TYPE_Q5_K = 13, /* 176-byte blocks of 256: as q4_K plus 32 bytes of fifth bits */
+    OOP_TYPE_Q6_K = 14, /* 210-byte blocks of 256: 128 bytes of low nibbles, 64 of
+                           2-bit high parts, 16 int8 scales per 16 elements, d;
+                           value = d * scale * (code - 32) */
     OOP_TYPE_BF16 = 30
 } oop_type;
 
@@ -83,14 +106,16 @@ typedef enum {
  *
  *   dst[m, n, i2, i3] = sum_k a[m, k, i2/dps2, i3/dps3] * b[n, k, i2, i3]
  *
- *   ne_a   = {M, K, ne02, ne03}   a (src0): f32, q8_0 or q4_0
+ *   ne_a   = {M, K, ne02, ne03}   a (src0): any oop_type
  *   ne_b   = {N, K, ne12, ne13}   b (src1): f32
  *   ne_dst = {M, N, ne12, ne13}   dst: f32, OVERWRITTEN (not accumulated)
  *   dps2 = ne12/ne02 and dps3 = ne13/ne03 must divide exactly.
  *
- * Quantised a needs M % 32 == 0 (its blocks run along ne0).  Alignment: f32
- * pointers 4 bytes, quantised a 2 bytes; 16-byte alignment enables the vector
- * paths.  K == 0 writes zeros (an empty sum); any other zero size is a no-op.
+ * Quantised a needs M % 32 == 0 (M % 256 for the K-quants: its blocks run
+ * along ne0).  Alignment: f32 pointers 4 bytes, any other a 2 bytes; 16-byte
+ * alignment of a and of its rows enables the TMA-fed paths.  The skinny-N
+ * kernel takes f32 src0 only; every other type runs on the tensor-core (or
+ * CUDA-core) kernel.  K == 0 writes zeros (an empty sum); any other zero size is a no-op.
  * b may hold values far beyond binary16's range: no operand is ever rounded to
  * fp16.  Precision: every finite input gives a finite result within
  * 2e-6 * sum_k |a*b| of the exact sum.
@@ -156,7 +181,7 @@ int oop_out_prod_strided(const void *a, int a_type, const float *b, const int64_
  *
  *   y[r, t, i2, i3] = sum_k W[k, r, i2/dps2, i3/dps3] * x[k, t, i2, i3]
  *
- *   ne_w = {K, R, ne02, ne03}   W: f32, q8_0 or q4_0
+ *   ne_w = {K, R, ne02, ne03}   W: any oop_type
  *   ne_x = {K, T, ne12, ne13}   x: f32;  dy: f32 {R, T, ne12, ne13}
  *
  *   dx[k, t, i2, i3] = sum_r W[k, r, i2/dps2, i3/dps3] * dy[r, t, i2, i3]

@@ -58,7 +58,9 @@ def _ne(v):
     ((64, 8, 1, 1), (4, 7, 1, 1), (64, 4, 1, 1), 0, -3),       # K mismatch
     ((64, 8, 1, 1), (4, 8, 1, 1), (64, 5, 1, 1), 0, -3),       # wrong dst ne
     ((48, 8, 1, 1), (4, 8, 1, 1), (48, 4, 1, 1), 8, -3),       # q8_0 M % 32
-    ((64, 8, 1, 1), (4, 8, 1, 1), (64, 4, 1, 1), 7, -2),       # unknown type
+    ((64, 8, 1, 1), (4, 8, 1, 1), (64, 4, 1, 1), 9, -2),       # q8_1: not a src0 type
+    ((64, 8, 1, 1), (4, 8, 1, 1), (64, 4, 1, 1), 99, -2),      # unknown type
+    ((128, 8, 1, 1), (4, 8, 1, 1), (128, 4, 1, 1), 12, -3),    # q4_K M % 256
     ((64, -1, 1, 1), (4, -1, 1, 1), (64, 4, 1, 1), 0, -3),     # negative size
     ((64, 8, 0, 1), (4, 8, 0, 1), (64, 4, 0, 1), 0, -4),       # ne02 = 0
 ])

@@ -58,7 +58,8 @@ def test_host_buffer_holds_every_tensor(a_type, ne_a, ne_b):
     (F32, (256, 512, 1, 1), (8, 511, 1, 1)),       # K mismatch
     (Q8, (100, 64, 1, 1), (64, 64, 1, 1)),         # quantised M not a multiple of 32
     (F32, (256, 512, 3, 1), (8, 512, 4, 1)),       # no exact broadcast
-    (BF16, (256, 512, 1, 1), (8, 512, 1, 1)),      # src0 type not supported
+    (9, (256, 512, 1, 1), (8, 512, 1, 1)),         # q8_1: not a src0 type
+    (12, (128, 512, 1, 1), (8, 512, 1, 1)),        # q4_K needs M % 256
     (F32, (256, -1, 1, 1), (8, -1, 1, 1)),         # negative size
 ])
 def test_invalid_shapes_size_zero(a_type, ne_a, ne_b):
