@@ -90,6 +90,9 @@ def lib():
                                                   _i64p, _fp, _dp, _dp, ctypes.c_int]
             L.oracle_mul_mat_back.argtypes = [_vp, ctypes.c_int, _fp, _fp, _i64p, _i64p,
                                               _fp, _dp, _dp, _fp, _dp, _dp, ctypes.c_int]
+            L.oracle_mul_mat_id_weight_grad.argtypes = [_fp, ctypes.POINTER(ctypes.c_int32), _fp,
+                                                        _i64p, _i64p, ctypes.c_int64, _fp, _dp,
+                                                        _dp, ctypes.c_int]
             _lib = L
     return _lib
 
@@ -296,4 +299,25 @@ def mul_mat_back(W, w_type, x, dy, ne_w, nthreads=0):
         _ptr(out["dx"]["abs"], ctypes.c_double), nthreads)
     if rc:
         raise ValueError("oracle_mul_mat_back rejected its arguments")
+    return out
+
+
+def mul_mat_id_weight_grad(x, ids, dy, E, nthreads=0):
+    """Expert-weight gradient of MUL_MAT_ID.  x: float32 (n_tokens, n_x, K);
+    ids: int32 (n_tokens, n_used); dy: float32 (n_tokens, n_used, N).
+    Returns {"dst", "f64", "abs"}, each shaped (E, N, K) (ggml {K, N, E})."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    dy = np.ascontiguousarray(dy, dtype=np.float32)
+    T, n_x, K = x.shape
+    _, n_used, N = dy.shape
+    shape = (E, N, K)
+    out = {"dst": np.empty(shape, np.float32), "f64": np.empty(shape, np.float64),
+           "abs": np.empty(shape, np.float64)}
+    rc = lib().oracle_mul_mat_id_weight_grad(
+        _ptr(x, ctypes.c_float), _ptr(ids, ctypes.c_int32), _ptr(dy, ctypes.c_float),
+        _ne((K, n_x, T)), _ne((N, n_used, T)), int(E), _ptr(out["dst"], ctypes.c_float),
+        _ptr(out["f64"], ctypes.c_double), _ptr(out["abs"], ctypes.c_double), nthreads)
+    if rc:
+        raise ValueError("oracle_mul_mat_id_weight_grad rejected its arguments")
     return out

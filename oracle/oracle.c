@@ -634,9 +634,11 @@ static int check_mmid(int w_type, const int32_t *ids, const int64_t ne_w[3],
                       const int64_t ne_ids[2])
 {
     if (!ne_w || !ne_ids) return -1;
-    if (w_type != ORACLE_F32 && w_type != ORACLE_BF16 && w_type != ORACLE_F16)
-        return -1;
+    /* every expert type of "Metal kernel_mul_mat_id_back" (first bullet:
+     * out_prod's set); quantised blocks run along k */
+    if (oracle_block_elems(w_type) < 0) return -1;
     for (int i = 0; i < 3; ++i) if (ne_w[i] < 0) return -1;
+    if (ne_w[0] % oracle_block_elems(w_type)) return -1;
     if (ne_ids[0] < 0 || ne_ids[1] < 0) return -1;
     const int64_t nslot = ne_ids[0] * ne_ids[1];
     if (nslot > 0 && !ids) return -1;
@@ -645,14 +647,13 @@ static int check_mmid(int w_type, const int32_t *ids, const int64_t ne_w[3],
     return 0;
 }
 
+/* W[k, r, e]: element k of row (e, r), a row of K elements of w_type */
 static double w_at(const void *W, int w_type, const int64_t ne_w[3], int64_t e,
                    int64_t k, int64_t r)
 {
     const int64_t K = ne_w[0], N = ne_w[1];
-    const int64_t idx = (e * N + r) * K + k;
-    if (w_type == ORACLE_F32) return (double)((const float *)W)[idx];
-    uint16_t h = ((const uint16_t *)W)[idx];
-    return w_type == ORACLE_BF16 ? oracle_bf16_to_double(h) : oracle_half_to_double(h);
+    const uint8_t *row = (const uint8_t *)W + (e * N + r) * row_bytes(w_type, K);
+    return elem(w_type, row, k);
 }
 
 int oracle_mul_mat_id_back(const void *W, int w_type, const int32_t *ids,
@@ -717,6 +718,47 @@ int oracle_mul_mat_id_back_at(const void *W, int w_type, const int32_t *ids,
         }
         if (val) val[p] = acc;
         if (abssum) abssum[p] = sab;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* the expert-weight gradient of MUL_MAT_ID                           */
+/* ------------------------------------------------------------------ */
+
+int oracle_mul_mat_id_weight_grad(const float *x, const int32_t *ids, const float *dy,
+                                  const int64_t ne_x[3], const int64_t ne_dy[3], int64_t E,
+                                  float *dW, double *dW_f64, double *dW_abs, int nthreads)
+{
+    if (!ne_x || !ne_dy || E < 0) return -1;
+    const int64_t K = ne_x[0], n_x = ne_x[1], T = ne_x[2];
+    const int64_t N = ne_dy[0], n_used = ne_dy[1];
+    if (K < 0 || n_x < 1 || T < 0 || N < 0 || n_used < 0) return -1;
+    if (ne_dy[2] != T || n_used % n_x) return -1;
+    if (!dW && !dW_f64 && !dW_abs) return -1;
+    if (T * n_used > 0 && (!ids || !x || !dy)) return -1;
+    for (int64_t s = 0; s < T * n_used; ++s)
+        if (ids[s] < 0 || ids[s] >= E) return -1;
+    set_threads(nthreads);
+    /* one work item per (expert, r): a row of K results */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t w = 0; w < E * N; ++w) {
+        const int64_t e = w / N, r = w % N;
+        const int64_t base = (e * N + r) * K;
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0, sab = 0.0;
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t i = 0; i < n_used; ++i) {
+                    if (ids[t * n_used + i] != e) continue;
+                    const double p = (double)x[(t * n_x + i % n_x) * K + k] *
+                                     (double)dy[(t * n_used + i) * N + r];
+                    acc += p;
+                    sab += fabs(p);
+                }
+            if (dW) dW[base + k] = (float)acc;
+            if (dW_f64) dW_f64[base + k] = acc;
+            if (dW_abs) dW_abs[base + k] = sab;
+        }
     }
     return 0;
 }

@@ -81,7 +81,8 @@ int oracle_out_prod_fp16_staged(const void *a, int a_type, const float *b,
                                 const int64_t ne_a[4], const int64_t ne_b[4],
                                 float *dst, int nthreads);
 
-/* MUL_MAT_ID_BACK.  W: ne_w = {K, N, E} (k fastest), f32 or bf16;
+/* MUL_MAT_ID_BACK.  W: ne_w = {K, N, E} (k fastest), any type above (rows of
+ * K elements; quantised blocks run along k, K % block size == 0);
  * ids: int32 [n_tokens][n_used] (slot fastest), ids[t*n_used + i];
  * g: f32 {N, n_used, n_tokens}; dx: f32 {K, n_used, n_tokens}.
  *   dx[k,i,t] = sum_r W[k, r, ids[i,t]] * g[r, i, t]
@@ -121,6 +122,19 @@ int oracle_mul_mat_back(const void *W, int w_type, const float *x, const float *
                         const int64_t ne_w[4], const int64_t ne_x[4],
                         float *dW, double *dW_f64, double *dW_abs,
                         float *dx, double *dx_f64, double *dx_abs, int nthreads);
+
+/* The expert-weight gradient of MUL_MAT_ID (whose input gradient is
+ * MUL_MAT_ID_BACK).  Forward: y[r,i,t] = sum_k W[k,r,ids[i,t]] * x[k, i % n_x, t]
+ * with x {K, n_x, n_tokens} f32 (n_x = 1: one row per token for every slot;
+ * n_x = n_used: one row per slot), ids int32 [n_tokens][n_used], dy f32
+ * {N, n_used, n_tokens}.  Output dW {K, N, E} f32:
+ *   dW[k,r,e] = sum over slots (t ascending, then i ascending) with
+ *               ids[i,t] == e of x[k, i % n_x, t] * dy[r, i, t]
+ * (zero for an expert no slot is routed to).  An id outside [0, E) makes
+ * the call fail (-1) before anything is written. */
+int oracle_mul_mat_id_weight_grad(const float *x, const int32_t *ids, const float *dy,
+                                  const int64_t ne_x[3], const int64_t ne_dy[3], int64_t E,
+                                  float *dW, double *dW_f64, double *dW_abs, int nthreads);
 
 /* Forward MUL_MAT in fp64: W {K, R} (k fastest), x {K, T};
  * y[r,t] = sum_k W[k,r] * x[k,t], y {R, T} (r fastest). */

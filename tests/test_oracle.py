@@ -646,3 +646,88 @@ def test_plain_16bit_types_out_prod(orc, tid):
     r = orc.out_prod(bits, tid, b, ne_a, ne_b)
     ref = np.einsum("km,kn->nm", vals[0, 0], b[0, 0].astype(np.float64))
     assert np.all(np.abs(r["f64"][0, 0] - ref) <= 1e-13 * r["abs"][0, 0])
+
+
+@pytest.mark.parametrize("wt", [synth.TYPE_F16, synth.TYPE_Q8_0, synth.TYPE_Q4_1, synth.TYPE_Q5_0,
+                                synth.TYPE_Q2_K, synth.TYPE_Q4_K, synth.TYPE_Q6_K])
+def test_mmid_one_hot_equals_dense_every_weight_type(orc, wt):
+    """Expert weights of every type ("Metal kernel_mul_mat_id_back", first
+    bullet): with all slots routed to expert e, dx[:, i, :] equals OUT_PROD of
+    that expert's rows (the same bytes as a src0) and g^T, bit for bit."""
+    qk = synth.BLOCK.get(wt, (1, 2))[0]
+    K, N, E, n_used, T = (256 if qk == 256 else 64), 24, 4, 2, 6
+    x = synth.normal(22, K * N * E, std=0.1).reshape(E, N, K)
+    W = synth.quantize(wt, x)                       # rows (e, r) of K elements
+    W = W.reshape(E, N, -1).view(np.uint8) if wt == synth.TYPE_F16 else W.reshape(E, N, -1)
+    g = synth.normal(23, N * n_used * T).reshape(T, n_used, N)
+    for e in (0, 3):
+        ids = np.full((T, n_used), e, np.int32)
+        r = orc.mul_mat_id_back(W, wt, ids, g, (K, N, E))
+        for i in range(n_used):
+            bT = np.ascontiguousarray(g[:, i, :].T).reshape(1, 1, N, T)
+            op = orc.out_prod(W[e].reshape(1, 1, N, -1), wt, bT, (K, N, 1, 1), (T, N, 1, 1))
+            assert np.array_equal(op["f64"][0, 0], r["f64"][:, i, :])
+
+
+# --------------------------------------------------------------------------
+# the expert-weight gradient of MUL_MAT_ID (the op whose input gradient is
+# MUL_MAT_ID_BACK; "Metal kernel_mul_mat_id_back" is proven with the
+# gradient check of MUL_MAT_ID)
+# --------------------------------------------------------------------------
+
+def _moe_inputs(seed, K, N, E, n_used, n_x, T):
+    x = synth.normal(seed, T * n_x * K).reshape(T, n_x, K)
+    dy = synth.normal(seed + 1, T * n_used * N).reshape(T, n_used, N)
+    ids = synth.routing_ids(seed + 2, E, n_used, T)
+    return x, ids, dy
+
+
+@pytest.mark.parametrize("n_x", [1, 3])
+def test_expert_weight_grad_finite_differences(orc, n_x):
+    """L = sum(y * G) with y[r,i,t] = sum_k W[k,r,ids[i,t]] x[k, i % n_x, t] is
+    linear in W: central differences of a numpy forward give dW."""
+    K, N, E, n_used, T = 5, 4, 4, 3, 6
+    x, ids, G = _moe_inputs(180, K, N, E, n_used, n_x, T)
+    out = orc.mul_mat_id_weight_grad(x, ids, G, E)
+    W = np.random.default_rng(7).normal(size=(E, N, K))
+    xd, Gd = x.astype(np.float64), G.astype(np.float64)
+
+    def loss(Wm):
+        y = np.einsum("tirk,tik->tir", Wm[ids], xd[:, np.arange(n_used) % n_x, :])
+        return float((y * Gd).sum())
+
+    for idx in np.ndindex(W.shape):
+        Wp, Wm = W.copy(), W.copy()
+        Wp[idx] += 1.0
+        Wm[idx] -= 1.0
+        fd = (loss(Wp) - loss(Wm)) / 2.0
+        assert abs(fd - out["f64"][idx]) <= 1e-12 * (1 + abs(fd)), idx
+
+
+def test_expert_weight_grad_sums_to_dense(orc):
+    """Summed over experts, the gradient is the dense weight gradient over
+    every slot: OUT_PROD(x, dy) with all slots as one reduction."""
+    K, N, E, n_used, T = 40, 24, 6, 4, 30
+    x, ids, dy = _moe_inputs(182, K, N, E, n_used, n_used, T)
+    out = orc.mul_mat_id_weight_grad(x, ids, dy, E)
+    dense = orc.out_prod(x.reshape(1, 1, T * n_used, K), synth.TYPE_F32,
+                         dy.reshape(1, 1, T * n_used, N), (K, T * n_used, 1, 1),
+                         (N, T * n_used, 1, 1))
+    total = out["f64"].sum(axis=0)
+    assert np.all(np.abs(total - dense["f64"][0, 0]) <= 1e-12 * dense["abs"][0, 0])
+    assert np.allclose(out["abs"].sum(axis=0), dense["abs"][0, 0], rtol=1e-12, atol=0)
+
+
+def test_expert_weight_grad_one_hot(orc):
+    """All slots routed to expert e: dW[:, :, e] is OUT_PROD(x, dy) over all
+    slots, bit for bit; every other expert's gradient is zero."""
+    K, N, E, n_used, T = 32, 20, 3, 2, 9
+    x, _, dy = _moe_inputs(184, K, N, E, n_used, 1, T)
+    ids = np.full((T, n_used), 1, np.int32)
+    out = orc.mul_mat_id_weight_grad(x, ids, dy, E)
+    xs = np.repeat(x, n_used, axis=1)                        # every slot's row
+    dense = orc.out_prod(xs.reshape(1, 1, T * n_used, K), synth.TYPE_F32,
+                         dy.reshape(1, 1, T * n_used, N), (K, T * n_used, 1, 1),
+                         (N, T * n_used, 1, 1))
+    assert np.array_equal(out["f64"][1], dense["f64"][0, 0])
+    assert not out["f64"][0].any() and not out["f64"][2].any()
