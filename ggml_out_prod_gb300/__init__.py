@@ -81,6 +81,7 @@ EXPORTS = (
     "oop_last_launch_count", "oop_out_prod_host", "oop_out_prod_host_buffer_size",
     "oop_out_prod_plan", "oop_out_prod_strided", "oop_out_prod_strided_workspace_size",
     "oop_mul_mat_back", "oop_mul_mat_back_workspace_size",
+    "oop_mul_mat_id_weight_grad", "oop_mul_mat_id_weight_grad_workspace_size",
 )
 
 
@@ -169,6 +170,11 @@ def lib():
             L.oop_mul_mat_back.restype = ctypes.c_int
             L.oop_mul_mat_back.argtypes = [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _i64p, _i64p,
                                            _vp, ctypes.c_size_t, _vp]
+            L.oop_mul_mat_id_weight_grad_workspace_size.restype = ctypes.c_size_t
+            L.oop_mul_mat_id_weight_grad_workspace_size.argtypes = [_i64p, _i64p, ctypes.c_int64]
+            L.oop_mul_mat_id_weight_grad.restype = ctypes.c_int
+            L.oop_mul_mat_id_weight_grad.argtypes = [_vp, _vp, _vp, _vp, _i64p, _i64p,
+                                                     ctypes.c_int64, _vp, ctypes.c_size_t, _vp]
             _lib = L
     return _lib
 
@@ -274,6 +280,18 @@ def oop_mul_mat_back(W, w_type, x, dy, dW, dx, ne_w, ne_x, workspace, workspace_
                      stream) -> int:
     return int(lib().oop_mul_mat_back(W, int(w_type), x, dy, dW, dx, _ne(ne_w), _ne(ne_x),
                                       workspace, int(workspace_bytes), stream))
+
+
+def oop_mul_mat_id_weight_grad_workspace_size(ne_x, ne_dy, n_expert) -> int:
+    return int(lib().oop_mul_mat_id_weight_grad_workspace_size(_ne(ne_x), _ne(ne_dy),
+                                                               int(n_expert)))
+
+
+def oop_mul_mat_id_weight_grad(x, ids, dy, dW, ne_x, ne_dy, n_expert, workspace,
+                               workspace_bytes, stream) -> int:
+    return int(lib().oop_mul_mat_id_weight_grad(x, ids, dy, dW, _ne(ne_x), _ne(ne_dy),
+                                                int(n_expert), workspace, int(workspace_bytes),
+                                                stream))
 
 
 def oop_mul_mat_id_back_workspace_size(w_type, ne_w, ne_ids) -> int:
@@ -432,20 +450,24 @@ def mul_mat_back(W, x, dy, w_type=None, ne_w=None, want_dW=True, want_dx=True,
 
 
 def mul_mat_id_back(W, ids, g, w_type=None, out=None, workspace=None, stream=None,
-                    path=PATH_AUTO):
+                    path=PATH_AUTO, K=None):
     """dx = MUL_MAT_ID_BACK(W, ids, g).
 
-    W: float32 (E, N, K) or bf16 bits / torch.bfloat16 (E, N, K); ids: int32
-    (n_tokens, n_used); g: float32 (n_tokens, n_used, N).  Returns dx float32
-    (n_tokens, n_used, K)."""
+    W: float32 (E, N, K), 2-byte f16 / bf16 elements (E, N, K), or uint8
+    rows of quantised blocks (E, N, row bytes; give ``w_type``, K is derived
+    from the row bytes unless given); ids: int32 (n_tokens, n_used); g: float32
+    (n_tokens, n_used, N).  Returns dx float32 (n_tokens, n_used, K)."""
     torch = _torch()
     for t, n in ((W, "W"), (ids, "ids"), (g, "g")):
         _check_cuda(t, n)
     if w_type is None:
         w_type = TYPE_F32 if W.dtype == torch.float32 else TYPE_BF16
+    _check_src0(W, w_type, "W")
     if ids.dtype != torch.int32 or g.dtype != torch.float32:
         raise ValueError("ids must be int32 and g float32")
-    E, N, K = W.shape
+    E, N, K_row = W.shape
+    if K is None:
+        K = K_row // _BLOCKS[w_type][1] * _BLOCKS[w_type][0] if w_type in _BLOCKS else K_row
     n_tok, n_used = ids.shape
     if tuple(g.shape) != (n_tok, n_used, N):
         raise ValueError("g must be (n_tokens, n_used, N)")
@@ -460,6 +482,32 @@ def mul_mat_id_back(W, ids, g, w_type=None, out=None, workspace=None, stream=Non
                              _stream_ptr(stream), path)
     if rc != OK:
         raise OopError(rc, "oop_mul_mat_id_back")
+    return out
+
+
+def mul_mat_id_weight_grad(x, ids, dy, n_expert, out=None, workspace=None, stream=None):
+    """dW = the expert-weight gradient of MUL_MAT_ID.
+
+    x: float32 (n_tokens, n_x, K); ids: int32 (n_tokens, n_used); dy: float32
+    (n_tokens, n_used, N).  Returns dW float32 (n_expert, N, K)."""
+    torch = _torch()
+    for t, n in ((x, "x"), (ids, "ids"), (dy, "dy")):
+        _check_cuda(t, n)
+    if x.dtype != torch.float32 or dy.dtype != torch.float32 or ids.dtype != torch.int32:
+        raise ValueError("x and dy must be float32, ids int32")
+    n_tok, n_x, K = x.shape
+    _, n_used, N = dy.shape
+    ne_x, ne_dy = (K, n_x, n_tok), (N, n_used, n_tok)
+    if out is None:
+        out = torch.empty((n_expert, N, K), dtype=torch.float32, device=x.device)
+    _check_cuda(out, "out")
+    nws = oop_mul_mat_id_weight_grad_workspace_size(ne_x, ne_dy, n_expert)
+    ws = _workspace(nws, x.device, workspace)
+    rc = oop_mul_mat_id_weight_grad(_ptr(x), _ptr(ids), _ptr(dy), _ptr(out), ne_x, ne_dy,
+                                    n_expert, _ptr(ws), ws.numel() if ws is not None else 0,
+                                    _stream_ptr(stream))
+    if rc != OK:
+        raise OopError(rc, "oop_mul_mat_id_weight_grad")
     return out
 
 

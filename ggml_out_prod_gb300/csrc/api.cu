@@ -363,9 +363,10 @@ namespace {
 
 int check_mmid_shape(int w_type, const int64_t ne_w[3], const int64_t ne_ids[2], MmidShape *s) {
     if (!ne_w || !ne_ids) return OOP_ERR_NULL;
-    if (w_type != OOP_TYPE_F32 && w_type != OOP_TYPE_BF16) return OOP_ERR_TYPE;
+    if (type_block_elems(w_type) < 0) return OOP_ERR_TYPE;
     for (int i = 0; i < 3; ++i)
         if (ne_w[i] < 0) return OOP_ERR_SHAPE;
+    if (ne_w[0] % type_block_elems(w_type) != 0) return OOP_ERR_SHAPE;   // blocks run along k
     if (ne_ids[0] < 0 || ne_ids[1] < 0) return OOP_ERR_SHAPE;
     *s = MmidShape{ne_w[0], ne_w[1], ne_w[2], ne_ids[0], ne_ids[1], w_type};
     const double big = 9.0e18;
@@ -408,6 +409,7 @@ int oop_mul_mat_id_back_ex(const void *W, int w_type, const int32_t *ids, const 
         if (!W || !g) return OOP_ERR_NULL;
         if (!aligned(g, 4) || !aligned(W, w_type == OOP_TYPE_F32 ? 4 : 2)) return OOP_ERR_ALIGN;
     }
+    // (W's rows are then 2-byte aligned too: every block size is even)
     int *status = nullptr;
     rc = device_setup(&status);
     if (rc != OOP_OK) return rc;
@@ -433,6 +435,53 @@ int oop_mul_mat_id_back(const void *W, int w_type, const int32_t *ids, const flo
                         size_t workspace_bytes, void *stream) {
     return oop_mul_mat_id_back_ex(W, w_type, ids, g, dx, ne_w, ne_ids, workspace,
                                   workspace_bytes, stream, OOP_PATH_AUTO);
+}
+
+size_t oop_mul_mat_id_weight_grad_workspace_size(const int64_t ne_x[3], const int64_t ne_dy[3],
+                                                  int64_t n_expert) {
+    if (!ne_x || !ne_dy) return 0;
+    const oop::WgradShape s = {ne_x[0], ne_x[1], ne_dy[0], ne_dy[1], ne_x[2], n_expert};
+    if (s.K < 0 || s.n_x < 1 || s.N < 0 || s.n_used < 0 || s.n_tok < 0 || ne_dy[2] != s.n_tok ||
+        s.n_used % s.n_x != 0 || s.E < 1 || s.E > 6144)
+        return 0;
+    if (s.K == 0 || s.N == 0 || s.n_used * s.n_tok == 0) return 0;
+    return oop::tc_wgrad_workspace_bytes(s);
+}
+
+int oop_mul_mat_id_weight_grad(const float *x, const int32_t *ids, const float *dy, float *dW,
+                               const int64_t ne_x[3], const int64_t ne_dy[3], int64_t n_expert,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    oop::g_kernel_launches = 0;
+    if (!ne_x || !ne_dy) return OOP_ERR_NULL;
+    const oop::WgradShape s = {ne_x[0], ne_x[1], ne_dy[0], ne_dy[1], ne_x[2], n_expert};
+    if (s.K < 0 || s.n_x < 1 || s.N < 0 || s.n_used < 0 || s.n_tok < 0) return OOP_ERR_SHAPE;
+    if (ne_dy[2] != s.n_tok || s.n_used % s.n_x != 0) return OOP_ERR_SHAPE;
+    if (s.E < 1 || s.E > 6144) return OOP_ERR_SHAPE;          // counts are kept on chip
+    const double big = 9.0e18;
+    if (static_cast<double>(s.K) * s.N * s.E * 4.0 > big ||
+        static_cast<double>(s.K) * s.n_x * s.n_tok * 4.0 > big ||
+        static_cast<double>(s.N) * s.n_used * s.n_tok * 4.0 > big ||
+        s.n_used * s.n_tok > 0x3fffffffLL)
+        return OOP_ERR_SHAPE;
+    if (s.K == 0 || s.N == 0) return OOP_OK;                  // dW is empty
+    if (!dW) return OOP_ERR_NULL;
+    if (!aligned(dW, 4)) return OOP_ERR_ALIGN;
+    const int64_t slots = s.n_used * s.n_tok;
+    if (slots > 0) {
+        if (!x || !ids || !dy) return OOP_ERR_NULL;
+        if (!aligned(x, 4) || !aligned(ids, 4) || !aligned(dy, 4)) return OOP_ERR_ALIGN;
+    }
+    int *status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != OOP_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (slots == 0)   // no slot routed anywhere: every expert's gradient is zero
+        return cuda_rc(cudaMemsetAsync(dW, 0, static_cast<size_t>(s.K * s.N * s.E) * 4, st));
+    const size_t need = oop::tc_wgrad_workspace_bytes(s);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return OOP_ERR_WORKSPACE;
+    cudaError_t e = oop::launch_mmid_wgrad(x, ids, dy, dW, s, workspace, status, st);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_rc(e);
 }
 
 int oop_device_status(void *stream, int clear) {

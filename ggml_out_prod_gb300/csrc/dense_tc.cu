@@ -177,6 +177,12 @@ struct TcParams {
     const int *grp_rows;          // [slots] sorted slot -> dst row
     const int *grp_tiles;         // work list: (expert << 16) | n-tile
     const int *grp_ntiles;        // valid entries in grp_tiles
+    // segmented mode (MUL_MAT_ID's expert-weight gradient; data-parallel
+    // only): slice e reduces over its own k range, seg_nkb[e] k-blocks from
+    // row seg_off[e] of src0 (one src0 slice holding every segment) and
+    // column seg_off[e] of the split src1 (one slice, every segment)
+    const int *seg_off;
+    const int *seg_nkb;
 };
 
 // First iteration of stream-K CTA c, and the CTA that owns iteration x.
@@ -190,8 +196,9 @@ __host__ __device__ __forceinline__ int64_t sk_owner(int64_t iters, int ctas, in
 // Where tile t sits: m-tile, n-tile, dst slice, its valid src1 rows, and the
 // first src0 row (k = 0) of the src0 slice it reads.
 struct Tile {
-    int mt, nt;
+    int mt, nt, nkb;              // nkb: k-blocks of this tile
     int64_t slice, ncols, brow0, a_row0;
+    int64_t kofs, bslice;         // src1 k offset and slice coordinate
 };
 
 template <bool GROUPED>
@@ -217,6 +224,15 @@ __device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
     }
     const int64_t i2 = d.slice % p.ne12, i3 = d.slice / p.ne12;
     d.a_row0 = (i3 / p.dps3 * p.ne02 + i2 / p.dps2) * p.K;
+    d.nkb = p.num_kb;
+    d.kofs = 0;
+    d.bslice = d.slice;
+    if (!GROUPED && p.seg_off) {
+        d.kofs = p.seg_off[d.slice];
+        d.nkb = p.seg_nkb[d.slice];
+        d.a_row0 = d.kofs;
+        d.bslice = 0;
+    }
     return d;
 }
 
@@ -240,7 +256,7 @@ struct Walk {
     }
     __device__ __forceinline__ void next(const TcParams &p) {
         ++it;
-        if (++kb == p.num_kb) {
+        if (++kb == t.nkb) {
             kb = 0;
             tile += stride;
             if (it < end) t = decode_tile<GROUPED>(p, tile);
@@ -378,8 +394,14 @@ __global__ void __maxnreg__(MAX_REGS)
         if constexpr (GROUPED) {
             if (t >= static_cast<int64_t>(p.mtiles) * *p.grp_ntiles) return;   // no work left
         }
-        it0 = t * p.num_kb;
-        it1 = it0 + p.num_kb;
+        if (!GROUPED && p.seg_nkb) {
+            // segmented: this tile's k-block count is its slice's
+            it0 = 0;
+            it1 = p.seg_nkb[t / (static_cast<int64_t>(p.mtiles) * p.ntiles)];
+        } else {
+            it0 = t * p.num_kb;
+            it1 = it0 + p.num_kb;
+        }
         span = {it0, it1, t, 1, 0};
     }
     if (it0 >= it1) return;
@@ -452,10 +474,11 @@ __global__ void __maxnreg__(MAX_REGS)
                     ptx::tma_load_2d(st + B_IMG, &map_blo, &bars->rfull[r], w.kb * BK,
                                      static_cast<int>(t.brow0));
                 } else {
-                    ptx::tma_load_3d(st, &map_bhi, &bars->rfull[r], w.kb * BK, t.nt * BN,
-                                     static_cast<int>(t.slice));
-                    ptx::tma_load_3d(st + B_IMG, &map_blo, &bars->rfull[r], w.kb * BK,
-                                     t.nt * BN, static_cast<int>(t.slice));
+                    const int bk = static_cast<int>(t.kofs + static_cast<int64_t>(w.kb) * BK);
+                    ptx::tma_load_3d(st, &map_bhi, &bars->rfull[r], bk, t.nt * BN,
+                                     static_cast<int>(t.bslice));
+                    ptx::tma_load_3d(st + B_IMG, &map_blo, &bars->rfull[r], bk, t.nt * BN,
+                                     static_cast<int>(t.bslice));
                 }
                 last_ph[r] = static_cast<int>(rr.phase);
             }
@@ -488,7 +511,7 @@ __global__ void __maxnreg__(MAX_REGS)
                 seg_kb0 = w.kb;
             }
             const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
-            const bool chunk_last = in_chunk == CHUNK_KB - 1 || w.kb + 1 == p.num_kb ||
+            const bool chunk_last = in_chunk == CHUNK_KB - 1 || w.kb + 1 == w.t.nkb ||
                                     w.it + 1 == w.end;
             if (in_chunk == 0) ++q;
             const int buf = q & 1;
@@ -667,7 +690,7 @@ __global__ void __maxnreg__(MAX_REGS)
         for (Walk<GROUPED> w(p, span); w.it < w.end; w.next(p), ++g) {
             if (g == 0 || w.kb == 0) seg_kb0 = w.kb;
             const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
-            const bool last = w.kb + 1 == p.num_kb || w.it + 1 == w.end;   // segment ends
+            const bool last = w.kb + 1 == w.t.nkb || w.it + 1 == w.end;   // segment ends
             if (in_chunk == 0) ++q;
             if (in_chunk != CHUNK_KB - 1 && !last) continue;   // once per chunk
             const Tile &t = w.t;
@@ -683,7 +706,7 @@ __global__ void __maxnreg__(MAX_REGS)
             }
             // where a finished segment goes: dst, or a stream-K partial slot
             // (slot 0 for the CTA's first segment, 1 for its last)
-            const bool whole = seg_kb0 == 0 && w.kb + 1 == p.num_kb;
+            const bool whole = seg_kb0 == 0 && w.kb + 1 == w.t.nkb;
             const int64_t m = static_cast<int64_t>(t.mt) * BM + row;
             float *dst = GROUPED ? p.dst : p.dst + t.slice * p.N * p.M;
             float *part = nullptr;
@@ -1054,6 +1077,102 @@ __global__ void __launch_bounds__(256) mmid_gsplit_kernel(const float *__restric
     ptx::griddep_launch_dependents();   // as in bsplit_kernel
 }
 
+// ---- MUL_MAT_ID's expert-weight gradient as a segmented product ------------
+// dW_e = sum over the slots routed to e of x_slot (x) dy_slot: OUT_PROD per
+// expert whose reduction runs over that expert's slots.  The slots are sorted
+// by expert into segments rounded up to whole k-blocks (padding rows are zero
+// on both sides, and an expert with no slot gets one block of padding, so its
+// dW comes out zero); the tile kernel's segmented mode then gives slice e the
+// k range of segment e.  Segment starts are multiples of 32, which keeps every
+// TMA x coordinate of the split gradient 16-byte aligned.
+
+// Routing, one CTA: per-expert counts, segment offsets and k-block counts,
+// and the sorted-slot list (-1 at padding).  Slots with an id outside [0, E)
+// take part in no segment and set OOP_ERR_BAD_ID.
+__global__ void __launch_bounds__(1024) wgrad_route_kernel(const int32_t *__restrict__ ids,
+                                                           int64_t nslot, int E,
+                                                           int64_t rows_max, int *seg_off,
+                                                           int *seg_nkb, int *total, int *rows,
+                                                           int *status) {
+    extern __shared__ int sh[];                   // [E] counts, then [E] cursors
+    int *cnt = sh, *cur = sh + E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    for (int64_t j = threadIdx.x; j < rows_max; j += blockDim.x) rows[j] = -1;
+    __syncthreads();
+    for (int64_t s = threadIdx.x; s < nslot; s += blockDim.x) {
+        const int e = ids[s];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else record_status(status, OOP_ERR_BAD_ID);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int e = 0; e < E; ++e) {
+            const int nkb = cnt[e] > 0 ? (cnt[e] + BK - 1) / BK : 1;
+            seg_off[e] = acc;
+            seg_nkb[e] = nkb;
+            cur[e] = acc;
+            acc += nkb * BK;
+        }
+        *total = acc;
+    }
+    __syncthreads();
+    for (int64_t s = threadIdx.x; s < nslot; s += blockDim.x) {
+        const int e = ids[s];
+        if (e >= 0 && e < E) rows[atomicAdd(&cur[e], 1)] = static_cast<int>(s);
+    }
+}
+
+// Sorted slot j (one per CTA) -> xg[j][0..K) = x[., i % n_x, t] of slot
+// s = t * n_used + i, zero at padding.  Rows past the routed total are never
+// read and are left alone.
+__global__ void __launch_bounds__(256) wgrad_gather_kernel(const float *__restrict__ x,
+                                                           const int *__restrict__ rows,
+                                                           const int *__restrict__ total,
+                                                           float *__restrict__ xg, int64_t K,
+                                                           int64_t n_x, int64_t n_used) {
+    const int64_t j = blockIdx.x;
+    if (j >= *total) return;
+    const int s = rows[j];
+    float *dst = xg + j * K;
+    if (s < 0) {
+        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) dst[k] = 0.f;
+        return;
+    }
+    const float *src = x + ((s / n_used) * n_x + (s % n_used) % n_x) * K;
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) dst[k] = __ldg(src + k);
+}
+
+// bhi, blo [r][j] (j fastest, row length Kp) = TF32 split of dy[r] of sorted
+// slot j, zero at padding: 64 j x 64 r per CTA through shared memory, read
+// along r, written along j.
+__global__ void __launch_bounds__(256) wgrad_dysplit_kernel(const float *__restrict__ dy,
+                                                            const int *__restrict__ rows,
+                                                            const int *__restrict__ total,
+                                                            uint32_t *__restrict__ bhi,
+                                                            uint32_t *__restrict__ blo,
+                                                            int64_t N, int64_t Kp) {
+    __shared__ float tile[kSplitTile][kSplitTile + 1];      // [j][r]
+    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kSplitTile;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kSplitTile;
+    const int64_t tot = *total;
+    if (j0 >= tot) return;
+    const int tx = threadIdx.x, ty = threadIdx.y;           // 32 x 8
+    for (int i = ty; i < kSplitTile; i += 8) {
+        const int64_t j = j0 + i;
+        const int s = j < tot ? rows[j] : -1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t r = r0 + tx + 32 * h;
+            tile[i][tx + 32 * h] = (s >= 0 && r < N) ? __ldg(dy + static_cast<int64_t>(s) * N + r)
+                                                     : 0.f;
+        }
+    }
+    __syncthreads();
+    store_split_tile(tile, bhi, blo, 0, j0, r0, N, Kp);
+    ptx::griddep_launch_dependents();   // as in bsplit_kernel
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
 
 // bhi / blo: [slices][N][Kp] words, boxes of 32 k x 128 n, 128-byte swizzle.
@@ -1406,7 +1525,7 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     os.dps2 = 1;
     os.dps3 = 1;
     os.a_type = s.w_type;
-    os.a_row_bytes = s.K * (s.w_type == OOP_TYPE_F32 ? 4 : 2);
+    os.a_row_bytes = s.K / type_block_elems(s.w_type) * type_block_bytes(s.w_type);
 
     TcParams p = {};
     p.a = static_cast<const uint8_t *>(W);
@@ -1441,17 +1560,139 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     p.partial = reinterpret_cast<float *>(ws + t.off_part);
     const int64_t max_grid = t.mtiles * t.max_tiles;
     const dim3 grid(static_cast<unsigned>(p.ctas > 0 || p.persistent ? G : max_grid));
-    if (s.w_type == OOP_TYPE_F32)
-        e = launch_typed<OOP_TYPE_F32, true>(W, os, mhi, mlo, p, grid, stream);
-    else if (s.w_type == OOP_TYPE_BF16)
-        e = launch_typed<OOP_TYPE_BF16, true>(W, os, mhi, mlo, p, grid, stream);
-    else
+    switch (s.w_type) {
+#define OOP_TC_CASE(T) \
+    case T: e = launch_typed<T, true>(W, os, mhi, mlo, p, grid, stream); break;
+    OOP_TC_CASE(OOP_TYPE_F32)
+    OOP_TC_CASE(OOP_TYPE_F16)
+    OOP_TC_CASE(OOP_TYPE_BF16)
+    OOP_TC_CASE(OOP_TYPE_Q4_0)
+    OOP_TC_CASE(OOP_TYPE_Q4_1)
+    OOP_TC_CASE(OOP_TYPE_Q5_0)
+    OOP_TC_CASE(OOP_TYPE_Q5_1)
+    OOP_TC_CASE(OOP_TYPE_Q8_0)
+    OOP_TC_CASE(OOP_TYPE_Q2_K)
+    OOP_TC_CASE(OOP_TYPE_Q3_K)
+    OOP_TC_CASE(OOP_TYPE_Q4_K)
+    OOP_TC_CASE(OOP_TYPE_Q5_K)
+    OOP_TC_CASE(OOP_TYPE_Q6_K)
+#undef OOP_TC_CASE
+    default:
         return cudaErrorInvalidValue;
+    }
     if (e != cudaSuccess || p.ctas == 0) return e;
     launch_fixup<true>(p.partial, p, max_grid, stream);
     e = cudaGetLastError();
     if (e == cudaSuccess) ++g_kernel_launches;
     return e;
+}
+
+// ---- the expert-weight gradient launcher ------------------------------------
+
+namespace {
+
+struct WgradPlan {
+    int64_t nslot, rows_max, Kp;
+    size_t off_seg_off, off_seg_nkb, off_total, off_rows, off_xg, off_bhi, off_blo, total;
+};
+
+WgradPlan plan_wgrad(const WgradShape &s) {
+    WgradPlan t = {};
+    t.nslot = s.n_used * s.n_tok;
+    t.rows_max = t.nslot + static_cast<int64_t>(BK) * s.E;      // at most one block of padding each
+    t.Kp = padded_k(t.rows_max);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += align256(bytes);
+        return at;
+    };
+    t.off_seg_off = take(sizeof(int) * static_cast<size_t>(s.E));
+    t.off_seg_nkb = take(sizeof(int) * static_cast<size_t>(s.E));
+    t.off_total = take(sizeof(int));
+    t.off_rows = take(sizeof(int) * static_cast<size_t>(t.rows_max));
+    t.off_xg = take(4 * static_cast<size_t>(t.rows_max) * static_cast<size_t>(s.K));
+    t.off_bhi = take(4 * static_cast<size_t>(s.N) * static_cast<size_t>(t.Kp));
+    t.off_blo = take(4 * static_cast<size_t>(s.N) * static_cast<size_t>(t.Kp));
+    t.total = o;
+    return t;
+}
+
+}  // namespace
+
+size_t tc_wgrad_workspace_bytes(const WgradShape &s) { return plan_wgrad(s).total; }
+
+cudaError_t launch_mmid_wgrad(const float *x, const int32_t *ids, const float *dy, float *dW,
+                              const WgradShape &s, void *workspace, int *status,
+                              cudaStream_t stream) {
+    const WgradPlan t = plan_wgrad(s);
+    const int64_t mtiles = (s.K + BM - 1) / BM, ntiles = (s.N + BN - 1) / BN;
+    if (s.E < 1 || s.E > 65535 || t.rows_max > 0x7fffffffLL || mtiles * ntiles > 0x7fffffffLL ||
+        (t.Kp + kSplitTile - 1) / kSplitTile > 0x7fffffffLL || (s.N + kSplitTile - 1) / kSplitTile > 65535)
+        return cudaErrorInvalidConfiguration;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int *seg_off = reinterpret_cast<int *>(ws + t.off_seg_off);
+    int *seg_nkb = reinterpret_cast<int *>(ws + t.off_seg_nkb);
+    int *total = reinterpret_cast<int *>(ws + t.off_total);
+    int *rows = reinterpret_cast<int *>(ws + t.off_rows);
+    float *xg = reinterpret_cast<float *>(ws + t.off_xg);
+    uint32_t *bhi = reinterpret_cast<uint32_t *>(ws + t.off_bhi);
+    uint32_t *blo = reinterpret_cast<uint32_t *>(ws + t.off_blo);
+
+    const size_t route_smem = 2 * sizeof(int) * static_cast<size_t>(s.E);
+    if (route_smem > 48 * 1024) return cudaErrorInvalidConfiguration;
+    wgrad_route_kernel<<<1, 1024, route_smem, stream>>>(ids, t.nslot, static_cast<int>(s.E),
+                                                         t.rows_max, seg_off, seg_nkb, total,
+                                                         rows, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ++g_kernel_launches;
+    wgrad_gather_kernel<<<static_cast<unsigned>(t.rows_max), 256, 0, stream>>>(
+        x, rows, total, xg, s.K, s.n_x, s.n_used);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ++g_kernel_launches;
+    wgrad_dysplit_kernel<<<dim3(static_cast<unsigned>((t.Kp + kSplitTile - 1) / kSplitTile),
+                                static_cast<unsigned>((s.N + kSplitTile - 1) / kSplitTile)),
+                           dim3(32, 8), 0, stream>>>(dy, rows, total, bhi, blo, s.N, t.Kp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ++g_kernel_launches;
+
+    CUtensorMap mhi, mlo;
+    if (!make_b_map(&mhi, bhi, t.Kp, s.N, 1) || !make_b_map(&mlo, blo, t.Kp, s.N, 1))
+        return cudaErrorInvalidValue;
+
+    // the gathered rows xg [rows_max][K] are src0: M = K, one slice, read by
+    // every expert's segment
+    OutProdShape os = {};
+    os.M = s.K;
+    os.K = t.rows_max;
+    os.N = s.N;
+    os.ne02 = os.ne03 = os.ne13 = 1;
+    os.ne12 = s.E;
+    os.dps2 = s.E;
+    os.dps3 = 1;
+    os.a_type = OOP_TYPE_F32;
+    os.a_row_bytes = 4 * s.K;
+
+    TcParams p = {};
+    p.a = reinterpret_cast<const uint8_t *>(xg);
+    p.dst = dW;
+    p.status = status;
+    p.M = s.K;
+    p.K = t.rows_max;          // every row of a segment is data or zero padding
+    p.N = s.N;
+    p.ne02 = 1;
+    p.ne12 = s.E;
+    p.dps2 = s.E;
+    p.dps3 = 1;
+    p.a_row_bytes = os.a_row_bytes;
+    p.num_kb = 1;
+    p.mtiles = static_cast<int>(mtiles);
+    p.ntiles = static_cast<int>(ntiles);
+    p.seg_off = seg_off;
+    p.seg_nkb = seg_nkb;
+    const dim3 grid(static_cast<unsigned>(mtiles * ntiles), static_cast<unsigned>(s.E));
+    return launch_typed<OOP_TYPE_F32, false>(xg, os, mhi, mlo, p, grid, stream);
 }
 
 }  // namespace oop

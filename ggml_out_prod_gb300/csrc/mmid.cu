@@ -7,6 +7,7 @@
 // thread t accumulates k = t + 256*j (coalesced reads of each expert row r,
 // which is contiguous in k), g's slot column is staged in shared memory.
 #include "oop_internal.cuh"
+#include "quant.cuh"
 
 namespace oop {
 namespace {
@@ -14,20 +15,19 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kPer = 8;     // k columns per thread per pass
 
+// W[k, r, e]: element k of row (e, r), rows of `row_bytes` (any src0 type;
+// quantised blocks run along k)
 template <int TYPE>
-__device__ __forceinline__ float w_elem(const void *W, int64_t idx) {
-    if constexpr (TYPE == OOP_TYPE_F32) {
-        return __ldg(static_cast<const float *>(W) + idx);
-    } else {
-        return bf16_bits_to_float(__ldg(static_cast<const unsigned short *>(W) + idx));
-    }
+__device__ __forceinline__ float w_elem(const uint8_t *row, int64_t k) {
+    if constexpr (TYPE == OOP_TYPE_F32) return __ldg(reinterpret_cast<const float *>(row) + k);
+    else return decode_row<TYPE>(row, k);
 }
 
 template <int TYPE>
 __global__ void __launch_bounds__(kThreads) mmid_slot_kernel(const void *W, const int32_t *ids,
                                                               const float *g, float *dx,
                                                               int64_t K, int64_t N, int64_t E,
-                                                              int *status) {
+                                                              int64_t row_bytes, int *status) {
     extern __shared__ float gs[];
     const int64_t slot = blockIdx.x;               // t * n_used + i
     const int32_t e = __ldg(ids + slot);
@@ -39,18 +39,18 @@ __global__ void __launch_bounds__(kThreads) mmid_slot_kernel(const void *W, cons
     }
     for (int64_t r = threadIdx.x; r < N; r += kThreads) gs[r] = __ldg(g + slot * N + r);
     __syncthreads();
-    const int64_t wbase = static_cast<int64_t>(e) * N * K;
+    const uint8_t *wbase = static_cast<const uint8_t *>(W) + static_cast<int64_t>(e) * N * row_bytes;
     for (int64_t kb = 0; kb < K; kb += kThreads * kPer) {
         float acc[kPer];
 #pragma unroll
         for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
         for (int64_t r = 0; r < N; ++r) {
             const float gr = gs[r];
-            const int64_t rb = wbase + r * K;
+            const uint8_t *row = wbase + r * row_bytes;
 #pragma unroll
             for (int j = 0; j < kPer; ++j) {
                 const int64_t k = kb + threadIdx.x + j * kThreads;
-                if (k < K) acc[j] = fmaf(w_elem<TYPE>(W, rb + k), gr, acc[j]);
+                if (k < K) acc[j] = fmaf(w_elem<TYPE>(row, k), gr, acc[j]);
             }
         }
 #pragma unroll
@@ -69,16 +69,34 @@ cudaError_t launch_mmid_per_slot(const void *W, const int32_t *ids, const float 
     if (slots > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const size_t smem = sizeof(float) * static_cast<size_t>(s.N);
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
-    auto k32 = mmid_slot_kernel<OOP_TYPE_F32>;
-    auto kbf = mmid_slot_kernel<OOP_TYPE_BF16>;
-    auto kern = s.w_type == OOP_TYPE_F32 ? k32 : kbf;
+    decltype(&mmid_slot_kernel<OOP_TYPE_F32>) kern = nullptr;
+    switch (s.w_type) {
+#define OOP_MMID_CASE(T) \
+    case T: kern = mmid_slot_kernel<T>; break;
+    OOP_MMID_CASE(OOP_TYPE_F32)
+    OOP_MMID_CASE(OOP_TYPE_F16)
+    OOP_MMID_CASE(OOP_TYPE_BF16)
+    OOP_MMID_CASE(OOP_TYPE_Q4_0)
+    OOP_MMID_CASE(OOP_TYPE_Q4_1)
+    OOP_MMID_CASE(OOP_TYPE_Q5_0)
+    OOP_MMID_CASE(OOP_TYPE_Q5_1)
+    OOP_MMID_CASE(OOP_TYPE_Q8_0)
+    OOP_MMID_CASE(OOP_TYPE_Q2_K)
+    OOP_MMID_CASE(OOP_TYPE_Q3_K)
+    OOP_MMID_CASE(OOP_TYPE_Q4_K)
+    OOP_MMID_CASE(OOP_TYPE_Q5_K)
+    OOP_MMID_CASE(OOP_TYPE_Q6_K)
+#undef OOP_MMID_CASE
+    default: return cudaErrorInvalidValue;
+    }
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
+    const int64_t row_bytes = s.K / type_block_elems(s.w_type) * type_block_bytes(s.w_type);
     kern<<<static_cast<unsigned>(slots), kThreads, smem, stream>>>(W, ids, g, dx, s.K, s.N, s.E,
-                                                                   status);
+                                                                   row_bytes, status);
     return cudaGetLastError();
 }
 

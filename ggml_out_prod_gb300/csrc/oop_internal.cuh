@@ -68,6 +68,12 @@ struct MmidShape {
     int w_type;
 };
 
+// MUL_MAT_ID's expert-weight gradient: x {K, n_x, n_tok}, dy {N, n_used,
+// n_tok}, dW {K, N, E}.
+struct WgradShape {
+    int64_t K, n_x, N, n_used, n_tok, E;
+};
+
 __device__ __forceinline__ float half_bits_to_float(uint16_t h) {
     return __half2float(__ushort_as_half(h));
 }
@@ -157,6 +163,12 @@ size_t tc_mmid_workspace_bytes(const MmidShape &s);
 cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, float *dx,
                            const MmidShape &s, void *workspace, int *status,
                            cudaStream_t stream);
+
+// MUL_MAT_ID's expert-weight gradient as a segmented tensor-core product.
+size_t tc_wgrad_workspace_bytes(const WgradShape &s);
+cudaError_t launch_mmid_wgrad(const float *x, const int32_t *ids, const float *dy, float *dW,
+                              const WgradShape &s, void *workspace, int *status,
+                              cudaStream_t stream);
 
 // MUL_MAT_ID_BACK, one CTA per routed slot.
 cudaError_t launch_mmid_per_slot(const void *W, const int32_t *ids,

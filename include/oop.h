@@ -272,7 +272,9 @@ int oop_out_prod_noalloc(const void *a, int a_type, const float *b, float *dst,
  *
  *   dx[k, i, t] = sum_r W[k, r, e] * g[r, i, t]
  *
- *   ne_w   = {K, N, E}             W: f32 or bf16, k fastest
+ *   ne_w   = {K, N, E}             W: any oop_type (out_prod's set), k fastest;
+ *                                  rows (e, r) of K elements, quantised blocks
+ *                                  along k (K % 32, or % 256 for the K-quants)
  *   ne_ids = {n_used, n_tokens}    ids: int32, slot i fastest
  *   g:  f32 {N, n_used, n_tokens}
  *   dx: f32 {K, n_used, n_tokens}, OVERWRITTEN; one writer per element.
@@ -298,6 +300,37 @@ int oop_mul_mat_id_back_ex(const void *W, int w_type, const int32_t *ids,
                            const float *g, float *dx, const int64_t ne_w[3],
                            const int64_t ne_ids[2], void *workspace,
                            size_t workspace_bytes, void *stream, int path);
+
+/*
+ * The expert-weight gradient of MUL_MAT_ID, the op whose input gradient is
+ * MUL_MAT_ID_BACK ("Metal kernel_mul_mat_id_back": its proof is the gradient
+ * check of MUL_MAT_ID).  Forward, per routed slot (i, t):
+ *
+ *   y[r, i, t] = sum_k W[k, r, ids[i, t]] * x[k, i % n_x, t]
+ *
+ *   ne_x  = {K, n_x, n_tokens}      x: f32; n_x = 1 (one row per token, shared
+ *                                   by its slots) or n_used (one per slot),
+ *                                   any n_x dividing n_used
+ *   ids:  int32 {n_used, n_tokens}  slot i fastest
+ *   ne_dy = {N, n_used, n_tokens}   dy: f32, the gradient of y
+ *   dW:   f32 {K, N, n_expert}, OVERWRITTEN:
+ *
+ *   dW[k, r, e] = sum over the slots (i, t) with ids[i, t] == e of
+ *                 x[k, i % n_x, t] * dy[r, i, t]      (zero if no slot is routed to e)
+ *
+ * Per expert an OUT_PROD whose reduction runs over that expert's routed
+ * slots, on the tensor cores (same 3xTF32 scheme and bound as oop_out_prod).
+ * An id outside [0, n_expert) takes part in no sum and records OOP_ERR_BAD_ID
+ * in the device status word.  n_expert <= 6144.  workspace:
+ * oop_mul_mat_id_weight_grad_workspace_size(...) bytes, 256-byte aligned (0
+ * and NULL allowed for an empty call).
+ */
+size_t oop_mul_mat_id_weight_grad_workspace_size(const int64_t ne_x[3], const int64_t ne_dy[3],
+                                                  int64_t n_expert);
+
+int oop_mul_mat_id_weight_grad(const float *x, const int32_t *ids, const float *dy, float *dW,
+                               const int64_t ne_x[3], const int64_t ne_dy[3], int64_t n_expert,
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* Synchronises `stream`, then returns the current device's status word
  * (OOP_OK, or the first device-side error recorded since it was last

@@ -90,10 +90,14 @@ def test_host_checks_nulls(built):
     rc = L.oop_out_prod(None, 0, None, None, _ne((64, 8, 1, 1)), _ne((0, 8, 1, 1)),
                         _ne((64, 0, 1, 1)), None, 0, None)
     assert rc == 0
-    # MUL_MAT_ID_BACK: wrong type, negative size
-    rc = L.oop_mul_mat_id_back(None, 8, None, None, None, _ne((4, 3, 2)), _ne((1, 1)),
+    # MUL_MAT_ID_BACK: wrong type (q8_1 is no expert type), blocks that do not
+    # fill K, negative size
+    rc = L.oop_mul_mat_id_back(None, 9, None, None, None, _ne((4, 3, 2)), _ne((1, 1)),
                                None, 0, None)
     assert rc == -2
+    rc = L.oop_mul_mat_id_back(None, 8, None, None, None, _ne((48, 3, 2)), _ne((1, 1)),
+                               None, 0, None)
+    assert rc == -3
     rc = L.oop_mul_mat_id_back(None, 0, None, None, None, _ne((4, -3, 2)), _ne((1, 1)),
                                None, 0, None)
     assert rc == -3

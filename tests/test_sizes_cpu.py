@@ -74,7 +74,8 @@ def test_mul_mat_id_back_workspace():
         ws = op.oop_mul_mat_id_back_workspace_size(wt, ne_w, ne_ids)
         # at least the TF32 split (hi and lo) of every routed slot's g row
         assert ws >= 2 * 4 * 768 * 8 * 512
-    assert op.oop_mul_mat_id_back_workspace_size(Q8, ne_w, ne_ids) == 0
+    assert op.oop_mul_mat_id_back_workspace_size(9, ne_w, ne_ids) == 0      # q8_1: no
+    assert op.oop_mul_mat_id_back_workspace_size(Q8, ne_w, ne_ids) > 0     # every other type
     assert op.oop_mul_mat_id_back_workspace_size(F32, (2048, 768, 6145), ne_ids) == 0
     assert op.oop_mul_mat_id_back_workspace_size(F32, ne_w, (0, 512)) == 0
 
@@ -91,3 +92,15 @@ def test_host_buffer_empty_sum(a_type, ne_a, ne_b):
     _, _, dst = _bytes(a_type, ne_a, ne_b)
     total = op.oop_out_prod_host_buffer_size(a_type, ne_a, ne_b)
     assert dst <= total <= dst + 4 * 255
+
+
+def test_expert_weight_grad_workspace():
+    ne_x, ne_dy = (2048, 8, 512), (768, 8, 512)
+    ws = op.oop_mul_mat_id_weight_grad_workspace_size(ne_x, ne_dy, 32)
+    # the gathered x rows and the split of dy for every routed slot, with up
+    # to one k-block of padding per expert
+    rows = 8 * 512 + 32 * 32
+    assert ws >= 4 * rows * 2048 + 2 * 4 * 768 * rows
+    assert op.oop_mul_mat_id_weight_grad_workspace_size(ne_x, ne_dy, 0) == 0
+    assert op.oop_mul_mat_id_weight_grad_workspace_size((2048, 3, 512), ne_dy, 32) == 0  # 8 % 3
+    assert op.oop_mul_mat_id_weight_grad_workspace_size(ne_x, (768, 8, 511), 32) == 0
