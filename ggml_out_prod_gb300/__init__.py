@@ -82,7 +82,14 @@ EXPORTS = (
     "oop_out_prod_plan", "oop_out_prod_strided", "oop_out_prod_strided_workspace_size",
     "oop_mul_mat_back", "oop_mul_mat_back_workspace_size",
     "oop_mul_mat_id_weight_grad", "oop_mul_mat_id_weight_grad_workspace_size",
+    "oop_out_prod_batch", "oop_out_prod_batch_max", "oop_lora_backward",
 )
+
+
+class OopProblem(ctypes.Structure):
+    """oop_out_prod_problem: one narrow single-slice OUT_PROD of a batch."""
+    _fields_ = [("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("dst", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("K", ctypes.c_int64), ("dst_transposed", ctypes.c_int)]
 
 
 class OopError(RuntimeError):
@@ -175,6 +182,14 @@ def lib():
             L.oop_mul_mat_id_weight_grad.restype = ctypes.c_int
             L.oop_mul_mat_id_weight_grad.argtypes = [_vp, _vp, _vp, _vp, _i64p, _i64p,
                                                      ctypes.c_int64, _vp, ctypes.c_size_t, _vp]
+            L.oop_out_prod_batch_max.restype = ctypes.c_int
+            L.oop_out_prod_batch_max.argtypes = []
+            L.oop_out_prod_batch.restype = ctypes.c_int
+            L.oop_out_prod_batch.argtypes = [ctypes.POINTER(OopProblem), ctypes.c_int,
+                                             ctypes.c_int64, _vp]
+            L.oop_lora_backward.restype = ctypes.c_int
+            L.oop_lora_backward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _vp]
             _lib = L
     return _lib
 
@@ -509,6 +524,63 @@ def mul_mat_id_weight_grad(x, ids, dy, n_expert, out=None, workspace=None, strea
     if rc != OK:
         raise OopError(rc, "oop_mul_mat_id_weight_grad")
     return out
+
+
+def oop_out_prod_batch(problems, N, stream) -> int:
+    """problems: a sequence of OopProblem (or (a, b, dst, M, K, transposed) tuples of
+    device pointers and sizes)."""
+    arr = (OopProblem * max(len(problems), 1))()
+    for i, q in enumerate(problems):
+        arr[i] = q if isinstance(q, OopProblem) else OopProblem(*q)
+    return int(lib().oop_out_prod_batch(arr, len(problems), int(N), stream))
+
+
+def out_prod_batch(problems, stream=None):
+    """Narrow OUT_PRODs in one call: ``problems`` is a list of (a, b, dst) or
+    (a, b, dst, transposed) torch float32 CUDA tensors with a (K, M), b (K, N)
+    and dst (N, M) -- or (M, N) when transposed -- and one N for all."""
+    if not problems:
+        return
+    Ns = {q[1].shape[-1] for q in problems}
+    if len(Ns) != 1:
+        raise ValueError("every problem of a batch has the same N")
+    N = Ns.pop()
+    items = []
+    for q in problems:
+        a, b, dst = q[0], q[1], q[2]
+        tr = bool(q[3]) if len(q) > 3 else False
+        for t, n in ((a, "a"), (b, "b"), (dst, "dst")):
+            _check_cuda(t, n)
+        K, M = a.shape[-2], a.shape[-1]
+        if b.shape[-2] != K or tuple(dst.shape[-2:]) != ((M, N) if tr else (N, M)):
+            raise ValueError("shapes do not match")
+        items.append(OopProblem(a.data_ptr() if a.numel() else None,
+                                b.data_ptr() if b.numel() else None, dst.data_ptr(), M, K,
+                                1 if tr else 0))
+    rc = oop_out_prod_batch(items, N, _stream_ptr(stream))
+    if rc != OK:
+        raise OopError(rc, "oop_out_prod_batch")
+
+
+def lora_backward(x, h, dz, dh, stream=None):
+    """Both LoRA adapter gradients of one projection in one launch.
+
+    x (T, K_in), h (T, r), dz (T, N_out), dh (T, r): float32 CUDA tensors
+    (ggml {K_in, T}, {r, T}, {N_out, T}, {r, T}).  Returns (dA, dB): dA
+    (r, K_in) = ggml {K_in, r}, dB (N_out, r) = ggml {r, N_out}."""
+    torch = _torch()
+    for t, n in ((x, "x"), (h, "h"), (dz, "dz"), (dh, "dh")):
+        _check_cuda(t, n)
+    T, K_in = x.shape
+    r = h.shape[1]
+    N_out = dz.shape[1]
+    dA = torch.empty((r, K_in), dtype=torch.float32, device=x.device)
+    dB = torch.empty((N_out, r), dtype=torch.float32, device=x.device)
+    rc = int(lib().oop_lora_backward(_ptr(x), _ptr(h), _ptr(dz), _ptr(dh), _ptr(dA), _ptr(dB),
+                                     K_in, N_out, T, r, _stream_ptr(stream)))
+    if rc != OK:
+        raise OopError(rc, "oop_lora_backward")
+    return dA, dB
 
 
 def profile_main_kernel(before, after) -> None:

@@ -135,6 +135,8 @@ thread_local cudaError_t g_last_cuda = cudaSuccess;
 
 }  // namespace
 
+int device_status_word(int **status) { return device_setup(status); }
+
 int out_prod_check_shape(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
     OutProdShape s = {};
     return check_out_prod_shape(a_type, ne_a, ne_b, &s);
@@ -186,6 +188,8 @@ size_t workspace_need(const OutProdShape &s, int path) {
 }
 
 }  // namespace
+
+int cuda_status(cudaError_t e) { return cuda_rc(e); }
 
 int run_out_prod(const void *a, int a_type, const float *b, const int64_t nb_b[4], float *dst,
                  const int64_t ne_a[4], const int64_t ne_b[4], const int64_t ne_dst[4],

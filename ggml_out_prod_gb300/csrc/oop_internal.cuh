@@ -106,6 +106,14 @@ int64_t skinny_tma_tile_m(const OutProdShape &s, int sms);
 cudaError_t launch_skinny_tma(const float *a, const float *b, float *dst,
                               const OutProdShape &s, int *status, cudaStream_t stream);
 
+// A list of single-slice f32 problems with the same N in one persistent
+// launch (at most skinny_batch_max() per launch; each must pass
+// skinny_batch_ok).
+bool skinny_batch_ok(const oop_out_prod_problem &q, int64_t N);
+int skinny_batch_max();
+cudaError_t launch_skinny_batch(const oop_out_prod_problem *probs, int count, int64_t N,
+                                int *status, cudaStream_t stream);
+
 // CUDA-core tiled OUT_PROD, any src0 type.
 cudaError_t launch_dense_simt(const void *a, const float *b, float *dst,
                               const OutProdShape &s, cudaStream_t stream);
@@ -113,6 +121,13 @@ cudaError_t launch_dense_simt(const void *a, const float *b, float *dst,
 // Kernels enqueued by the current API call on this thread (each launcher
 // adds its own).
 extern thread_local int g_kernel_launches;
+
+// The current device's status-word address, after checking it is sm_103
+// (OOP_OK or the status the entry points return).
+int device_status_word(int **status);
+// OOP_OK for cudaSuccess; otherwise OOP_ERR_CUDA, recording the error for
+// oop_last_cuda_error.
+int cuda_status(cudaError_t e);
 
 // SM count of the current device, queried once per device (0 on failure).
 // Safe to call from several host threads at once.

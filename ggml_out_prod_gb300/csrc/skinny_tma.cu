@@ -32,6 +32,7 @@
 // Waits are bounded like the tensor-core kernel's: running out records
 // OOP_ERR_DEVICE_TIMEOUT, every role stops, the TMA warp drains its copies.
 #include <algorithm>
+#include <cstring>
 
 #include "oop_internal.cuh"
 #include "tc_ptx.cuh"
@@ -55,6 +56,22 @@ struct TmaArgs {
     int64_t mtiles, items;      // items = slices * mtiles
     int kstages;                // ceil(K / kTK)
 };
+
+// Problems per batch launch (their tensor maps sit in the kernel parameters).
+constexpr int kMaxBatch = 48;
+
+struct BatchArgs {
+    CUtensorMap maps[kMaxBatch];
+    const float *b[kMaxBatch];
+    float *dst[kMaxBatch];
+    int64_t M[kMaxBatch], K[kMaxBatch];
+    int64_t item_off[kMaxBatch + 1];
+    int dst_t[kMaxBatch];
+    int64_t items;
+    int count;
+    int *status;
+};
+static_assert(sizeof(BatchArgs) < 30000, "kernel parameter space");
 
 template <int NP, int VW>
 struct Layout {
@@ -156,10 +173,22 @@ __device__ __forceinline__ void add_partial(const float *r, uint64_t (&acc)[NP /
     }
 }
 
-// N == NP here (the launcher takes this kernel only for N % 4 == 0).
-template <int NP, int VW>
-__global__ void __launch_bounds__(kThreads, 1)
-    skinny_tma_kernel(const __grid_constant__ CUtensorMap map_a, const TmaArgs p) {
+// What one work item reads and writes: src0 through `map` from row `arow0`
+// (k = 0) at m-tile `mt`, src1 rows of NP words from `b`, dst rows of `M`
+// floats at `dst`, K rows in `kstages` stages.
+struct ItemRef {
+    const CUtensorMap *map;
+    int64_t arow0, M, K;
+    const float *b;
+    float *dst;
+    int mt, kstages;
+    bool dst_t;                   // dst stored transposed: element (m, n) at m * NP + n
+};
+
+// The body shared by both kernels: `resolve(item)` gives an item's ItemRef.
+// N == NP here (the launchers take this form only for N % 4 == 0).
+template <int NP, int VW, class Resolve>
+__device__ __forceinline__ void skinny_body(int64_t items, int *status, const Resolve &resolve) {
     using L = Layout<NP, VW>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -186,19 +215,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kConsumerWarps) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            ptx::prefetch_tmap(&map_a);
             int last_ph[L::STAGES];
             for (int s = 0; s < L::STAGES; ++s) last_ph[s] = -1;
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int64_t item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
-                const int64_t slice = item / p.mtiles;
-                const int mt = static_cast<int>(item % p.mtiles);
-                const int64_t i2 = slice % p.ne12, i3 = slice / p.ne12;
-                const int64_t arow0 = (i3 / p.dps3 * p.ne02 + i2 / p.dps2) * p.K;
-                const float *bs = p.b + slice * p.K * p.N;
-                for (int ks = 0; ks < p.kstages; ++ks) {
+            for (int64_t item = blockIdx.x; item < items && ok; item += gridDim.x) {
+                const ItemRef it = resolve(item);
+                if (item == blockIdx.x) ptx::prefetch_tmap(it.map);
+                for (int ks = 0; ks < it.kstages; ++ks) {
                     if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1, abort, true, kWaitNs,
                                                 &timed_out)) {
                         ok = false;
@@ -206,12 +231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int64_t k0 = static_cast<int64_t>(ks) * kTK;
                     const uint32_t bbytes =
-                        static_cast<uint32_t>(std::min<int64_t>(kTK, p.K - k0) * p.N * 4);
+                        static_cast<uint32_t>(std::min<int64_t>(kTK, it.K - k0) * NP * 4);
                     uint8_t *st = smem + s * L::STAGE;
                     ptx::mbar_arrive_expect_tx(&full[s], L::A_BYTES + bbytes);
-                    ptx::tma_load_2d(st, &map_a, &full[s], mt * L::TM,
-                                     static_cast<int>(arow0 + k0));
-                    ptx::bulk_load(st + L::A_BYTES, bs + k0 * p.N, bbytes, &full[s]);
+                    ptx::tma_load_2d(st, it.map, &full[s], it.mt * L::TM,
+                                     static_cast<int>(it.arow0 + k0));
+                    ptx::bulk_load(st + L::A_BYTES, it.b + k0 * NP, bbytes, &full[s]);
                     last_ph[s] = static_cast<int>(ph);
                     if (++s == L::STAGES) {
                         s = 0;
@@ -233,15 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int64_t item = blockIdx.x; item < p.items; item += gridDim.x) {
-            const int64_t slice = item / p.mtiles;
-            const int mt = static_cast<int>(item % p.mtiles);
+        for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+            const ItemRef it = resolve(item);
             uint64_t acc[NP / 2][VW];
 #pragma unroll
             for (int j = 0; j < NP / 2; ++j)
 #pragma unroll
                 for (int v = 0; v < VW; ++v) acc[j][v] = 0;   // +0.0f in both halves
-            for (int ks = 0; ks < p.kstages; ++ks) {
+            for (int ks = 0; ks < it.kstages; ++ks) {
                 if (ok) {
                     const bool got = ptx::mbar_wait_bounded(&full[s], ph, abort, true, kWaitNs,
                                                             &timed_out);
@@ -253,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         reinterpret_cast<const float *>(smem + s * L::STAGE + L::A_BYTES);
                     const int64_t k0 = static_cast<int64_t>(ks) * kTK;
                     const int row0 = warp * kRowsPerWarp;
-                    if (k0 + kTK <= p.K) {
+                    if (k0 + kTK <= it.K) {
                         if constexpr (L::PREFETCH) {
                             // row j + 1's loads go out before row j's FMAs
                             Row<NP, VW> cur, nxt;
@@ -277,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the last stage of a slice: rows past K belong to the
                         // next slice (src0) or were not copied (src1)
                         for (int j = 0; j < kRowsPerWarp; ++j) {
-                            if (k0 + row0 + j < p.K) {
+                            if (k0 + row0 + j < it.K) {
                                 Row<NP, VW> cur;
                                 load_row<NP, VW>(sa, sb, row0 + j, lane, cur);
                                 fma_row<NP, VW>(cur, acc);
@@ -307,20 +331,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
             if (ok) {
-                float *dst = p.dst + slice * p.N * p.M;
                 for (int o = threadIdx.x; o < NP * L::TM; o += kConsumers) {
                     const int n = o / L::TM, mm = o % L::TM;
                     float sum = 0.f;
 #pragma unroll
                     for (int w = 0; w < 4; ++w) sum += red[(w * NP + n) * L::TM + mm];
-                    const int64_t m = static_cast<int64_t>(mt) * L::TM + mm;
-                    if (m < p.M) dst[static_cast<int64_t>(n) * p.M + m] = sum;
+                    const int64_t m = static_cast<int64_t>(it.mt) * L::TM + mm;
+                    if (m < it.M)
+                        it.dst[it.dst_t ? m * NP + n : static_cast<int64_t>(n) * it.M + m] = sum;
                 }
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
         }
     }
-    if (timed_out) record_status(p.status, OOP_ERR_DEVICE_TIMEOUT);
+    if (timed_out) record_status(status, OOP_ERR_DEVICE_TIMEOUT);
+}
+
+template <int NP, int VW>
+__global__ void __launch_bounds__(kThreads, 1)
+    skinny_tma_kernel(const __grid_constant__ CUtensorMap map_a, const TmaArgs p) {
+    skinny_body<NP, VW>(p.items, p.status, [&](int64_t item) {
+        const int64_t slice = item / p.mtiles;
+        const int64_t i2 = slice % p.ne12, i3 = slice / p.ne12;
+        ItemRef r;
+        r.map = &map_a;
+        r.arow0 = (i3 / p.dps3 * p.ne02 + i2 / p.dps2) * p.K;
+        r.M = p.M;
+        r.K = p.K;
+        r.b = p.b + slice * p.K * NP;
+        r.dst = p.dst + slice * NP * p.M;
+        r.mt = static_cast<int>(item % p.mtiles);
+        r.kstages = p.kstages;
+        r.dst_t = false;
+        return r;
+    });
+}
+
+// A list of independent single-slice problems in one launch: problem i owns
+// items [item_off[i], item_off[i + 1]), one per m-tile, its src0 read through
+// its own tensor map (kept in the kernel parameters).
+template <int NP, int VW>
+__global__ void __launch_bounds__(kThreads, 1)
+    skinny_batch_kernel(const __grid_constant__ BatchArgs pb) {
+    skinny_body<NP, VW>(pb.items, pb.status, [&](int64_t item) {
+        int i = 0;
+        while (i + 1 < pb.count && item >= pb.item_off[i + 1]) ++i;
+        ItemRef r;
+        r.map = &pb.maps[i];
+        r.arow0 = 0;
+        r.M = pb.M[i];
+        r.K = pb.K[i];
+        r.b = pb.b[i];
+        r.dst = pb.dst[i];
+        r.mt = static_cast<int>(item - pb.item_off[i]);
+        r.kstages = static_cast<int>((pb.K[i] + kTK - 1) / kTK);
+        r.dst_t = pb.dst_t[i] != 0;
+        return r;
+    });
 }
 
 template <int NP, int VW>
@@ -363,7 +430,73 @@ cudaError_t launch_tma(const float *a, const float *b, float *dst, const OutProd
     return cudaGetLastError();
 }
 
+template <int NP, int VW>
+cudaError_t launch_batch_typed(const oop_out_prod_problem *probs, int count, int *status, int sms,
+                               cudaStream_t stream) {
+    using L = Layout<NP, VW>;
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    BatchArgs pb;
+    memset(&pb, 0, sizeof pb);
+    int64_t items = 0;
+    for (int i = 0; i < count; ++i) {
+        const oop_out_prod_problem &q = probs[i];
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(q.M), static_cast<cuuint64_t>(q.K)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.M * 4)};
+        cuuint32_t box[2] = {static_cast<cuuint32_t>(L::TM), kTK};
+        cuuint32_t estr[2] = {1, 1};
+        if (enc(&pb.maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(q.a), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        pb.b[i] = q.b;
+        pb.dst[i] = q.dst;
+        pb.M[i] = q.M;
+        pb.K[i] = q.K;
+        pb.dst_t[i] = q.dst_transposed;
+        pb.item_off[i] = items;
+        items += (q.M + L::TM - 1) / L::TM;
+    }
+    pb.item_off[count] = items;
+    pb.items = items;
+    pb.count = count;
+    pb.status = status;
+    auto kern = skinny_batch_kernel<NP, VW>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L::SMEM));
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::min<int64_t>(items, sms);
+    kern<<<static_cast<unsigned>(grid), kThreads, L::SMEM, stream>>>(pb);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+bool skinny_batch_ok(const oop_out_prod_problem &q, int64_t N) {
+    return N % 4 == 0 && N >= 4 && N <= 32 && q.M % 4 == 0 && q.M > 0 && q.K > 0 &&
+           q.K < (1LL << 31) && reinterpret_cast<uintptr_t>(q.a) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(q.b) % 16 == 0;
+}
+
+int skinny_batch_max() { return kMaxBatch; }
+
+cudaError_t launch_skinny_batch(const oop_out_prod_problem *probs, int count, int64_t N,
+                                int *status, cudaStream_t stream) {
+    const int sms = device_sm_count();
+    if (count < 1 || count > kMaxBatch || sms <= 0) return cudaErrorInvalidValue;
+    switch (N) {
+    case 4: return launch_batch_typed<4, 4>(probs, count, status, sms, stream);
+    case 8: return launch_batch_typed<8, 4>(probs, count, status, sms, stream);
+    case 12: return launch_batch_typed<12, 4>(probs, count, status, sms, stream);
+    case 16: return launch_batch_typed<16, 4>(probs, count, status, sms, stream);
+    case 20: return launch_batch_typed<20, 4>(probs, count, status, sms, stream);
+    case 24: return launch_batch_typed<24, 4>(probs, count, status, sms, stream);
+    case 28: return launch_batch_typed<28, 2>(probs, count, status, sms, stream);
+    case 32: return launch_batch_typed<32, 2>(probs, count, status, sms, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
 
 // Items of 128 m (four m per lane) up to N = 24, of 64 m above; N = 20 and
 // 24 fall back to 64 when 128-wide items would leave fewer than two per SM.

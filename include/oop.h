@@ -206,6 +206,52 @@ int oop_mul_mat_back(const void *W, int w_type, const float *x, const float *dy,
                      size_t workspace_bytes, void *stream);
 
 /*
+ * A list of narrow OUT_PRODs in as few launches as possible (no counterpart
+ * on the pages' API; the workload is theirs: "metal: OUT_PROD runs batched,
+ * broadcast and narrow shapes on the GPU", opening list item 2 -- the rank-r
+ * gradients of LoRA fine-tuning).  Each problem is one slice:
+ *
+ *   dst[m, n] = sum_k a[m, k] * b[n, k]     a {M, K} f32, b {N, K} f32
+ *
+ * with dst {M, N} f32 OVERWRITTEN, or, with dst_transposed != 0, stored as
+ * {N, M} (element (m, n) at m * N + n).  N (1..32) is the
+ * same for every problem of the call.  Problems whose a and b are 16-byte
+ * aligned with M % 4 == 0, N % 4 == 0 and K > 0 are streamed together by one
+ * persistent kernel, up to oop_out_prod_batch_max() per launch (each with its
+ * own tensor map); any other problem runs as its own skinny-N launch.  No
+ * workspace.  Precision and errors as oop_out_prod; every problem is checked
+ * before anything is enqueued.  K == 0 zero-fills that dst.
+ */
+typedef struct {
+    const float *a;       /* {M, K}: device, f32 */
+    const float *b;       /* {N, K}: device, f32 */
+    float *dst;           /* {M, N}, or {N, M} when dst_transposed: device, f32 */
+    int64_t M, K;
+    int dst_transposed;
+} oop_out_prod_problem;
+
+int oop_out_prod_batch_max(void);
+
+int oop_out_prod_batch(const oop_out_prod_problem *problems, int count, int64_t N, void *stream);
+
+/*
+ * Both LoRA adapter gradients of one projection in one launch.  With the
+ * adapter y += B (A x) (ggml: A {K_in, r}, B {r, N_out}), the forward's
+ * h = A x {r, T} and the backward's dh = B^T dz {r, T} for the output
+ * gradient dz {N_out, T} and input x {K_in, T}:
+ *
+ *   dA = OUT_PROD(x, dh)   {K_in, r}      dA[k, j] = sum_t x[k, t] * dh[j, t]
+ *   dB = OUT_PROD(h, dz)   {r, N_out}     dB[j, o] = sum_t h[j, t] * dz[o, t]
+ *
+ * (dB as the narrow product OUT_PROD(dz, h) written transposed.)  All f32,
+ * device pointers, dense; r in 1..32; dA and dB OVERWRITTEN.  Errors and
+ * precision as oop_out_prod_batch.
+ */
+int oop_lora_backward(const float *x, const float *h, const float *dz, const float *dh, float *dA,
+                      float *dB, int64_t K_in, int64_t N_out, int64_t T, int64_t r,
+                      void *stream);
+
+/*
  * OUT_PROD from HOST buffers (no counterpart on the pages; the benchmark's
  * end-to-end figure goes through it): enqueues on `stream` the copies of a
  * and b into `device_buffer`, the product, and the copy of dst back into
