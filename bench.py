@@ -430,7 +430,77 @@ def gpu_arm(args):
             "roofline": dense_roofline(fl, us, tf32_peak)}
         del ta, tb, o
 
-    # every dense shape, q8_0 and q4_0: whole call and tile kernel alone
+    # the rank-r LoRA gradients of one 4B layer in one launch: dA and dB of the
+    # seven adapted projections (14 narrow OUT_PRODs over 512 tokens), against
+    # one launch per gradient
+    T, r = 512, 8
+    lay = [(K_in, N_out) for K_in, N_out in synth.LAYER_4B_PROJ]
+    ms = [k for k, _ in lay] + [n for _, n in lay]
+    byts = sum(4.0 * (m * T + r * T + m * r) for m in ms)
+    sets = rotation_sets(byts)
+    lists = []
+    for si in range(sets):
+        probs = []
+        for j, m in enumerate(ms):
+            ta = torch.from_numpy(synth.make_a(synth.TYPE_F32, (m, T, 1, 1), 400 + j)[0, 0]).to(device)
+            tb = torch.from_numpy(synth.make_b((r, T, 1, 1), 430 + j, std=100.0,
+                                               outliers=True)[0, 0]).to(device)
+            probs.append((ta, tb, torch.empty((r, m), device=device)))
+        lists.append(probs)
+    us_b = statistics.mean(time_rotating(
+        torch, [(lambda pr=pr: op.out_prod_batch(pr)) for pr in lists], psteps, 3)) * 1e3
+    us_l = statistics.mean(time_rotating(
+        torch, [(lambda pr=pr: [op.out_prod(a_, b_, out=d_, path=op.PATH_SKINNY)
+                                for a_, b_, d_ in pr]) for pr in lists], psteps, 3)) * 1e3
+    parts["lora_layer_r8_batched"] = {
+        "workload": "dA and dB of the 4B's 7 adapted projections at rank 8 over 512 tokens "
+                    "(14 narrow OUT_PRODs, a [M, 512] f32, M from 1024 to 9728)",
+        "us_one_launch": round(us_b, 3), "us_one_launch_per_gradient": round(us_l, 3),
+        "bytes": byts, "rotation_sets": sets, "roofline": hbm_roofline(byts, us_b, hbm)}
+    del lists
+
+    # both adapter gradients of one projection (the 4B's q: 2560 -> 4096) in one launch
+    K_in, N_out = 2560, 4096
+    byts = 4.0 * ((K_in + N_out) * T + 2 * r * T + (K_in + N_out) * r)
+    sets = rotation_sets(byts)
+    ins = []
+    for si in range(sets):
+        ins.append(tuple(torch.from_numpy(v).to(device) for v in (
+            synth.make_a(synth.TYPE_F32, (K_in, T, 1, 1), 460)[0, 0],
+            synth.make_b((r, T, 1, 1), 461)[0, 0],
+            synth.make_b((N_out, T, 1, 1), 462, std=100.0, outliers=True)[0, 0],
+            synth.make_b((r, T, 1, 1), 463, std=100.0, outliers=True)[0, 0])))
+    us = statistics.mean(time_rotating(
+        torch, [(lambda v=v: op.lora_backward(*v)) for v in ins], psteps, 3)) * 1e3
+    parts["lora_backward_q_proj_r8"] = {
+        "workload": "dA {2560, 8} and dB {8, 4096} of one projection over 512 tokens, one launch",
+        "us": round(us, 3), "bytes": byts, "rotation_sets": sets,
+        "roofline": hbm_roofline(byts, us, hbm)}
+    del ins
+
+    # dx of a MUL_MAT backward through the transposed gradient view (no copy
+    # of dy^T): W q8_0 [5120, 5120], dy [5120, 1024]
+    Kw, R, T2 = 5120, 5120, 1024
+    Wq = torch.from_numpy(synth.make_a(synth.TYPE_Q8_0, (Kw, R, 1, 1), 470, std=0.02)).to(device)
+    dyv = torch.from_numpy(synth.make_b((R, T2, 1, 1), 471, std=1e3, outliers=True)).to(device)
+    dyT = dyv.transpose(2, 3)
+    o = torch.empty((1, 1, T2, Kw), dtype=torch.float32, device=device)
+    wsz = op.oop_out_prod_strided_workspace_size(op.TYPE_Q8_0, (Kw, R, 1, 1), (T2, R, 1, 1),
+                                                 op.nb_of(dyT))
+    wsb = torch.empty(max(wsz, 1), dtype=torch.uint8, device=device)
+    us = statistics.mean(time_rotating(torch, [lambda: op.out_prod(
+        Wq, dyT, a_type=op.TYPE_Q8_0, ne_a=(Kw, R, 1, 1), out=o, workspace=wsb)],
+        max(args.steps, 10), 3)) * 1e3
+    fl = 2.0 * Kw * R * T2
+    parts["dx_transposed_view_q8_0_m5120_k5120_n1024"] = {
+        "workload": "dx = OUT_PROD(W, dy^T) with dy^T read in place: W q8_0 [5120, 5120], "
+                    "dy [5120, 1024]", "us_call": round(us, 2),
+        "TFLOP/s_call": round(fl / (us * 1e-6) / 1e12, 2), "rotation_sets": 1,
+        "inputs": "W 27.9 MB + dy 21 MB; each call also writes and reads its 42 MB split"}
+    del Wq, dyv, dyT, o, wsb
+
+    # every dense shape, q8_0 and q4_0 (and q4_K, the pages' perf weight):
+    # whole call and tile kernel alone
     for m, k in synth.DENSE_MK:
         x = synth.normal(synth.tensor_seed(30), m * k, std=0.02).reshape(1, 1, k, m)
         bn = synth.make_b((DENSE_N, k, 1, 1), 31, std=1e3, outliers=True)
@@ -438,7 +508,8 @@ def gpu_arm(args):
         wsz = op.oop_out_prod_workspace_size(op.TYPE_Q8_0, (m, k, 1, 1), (DENSE_N, k, 1, 1))
         wsb = torch.empty(max(wsz, 1), dtype=torch.uint8, device=device)
         for tid, tname, quant in ((synth.TYPE_Q8_0, "q8_0", synth.quantize_q8_0),
-                                  (synth.TYPE_Q4_0, "q4_0", synth.quantize_q4_0)):
+                                  (synth.TYPE_Q4_0, "q4_0", synth.quantize_q4_0),
+                                  (synth.TYPE_Q4_K, "q4_K", synth.quantize_q4_k)):
             an = quant(x)
             byts = an.nbytes + bn.nbytes + 4 * m * DENSE_N
             sets = rotation_sets(byts)
@@ -505,6 +576,30 @@ def gpu_arm(args):
                             "roofline_frac": round(roof_us / us, 4)}
         parts[f"mul_mat_id_back_{nm}"] = entry
         del tW, tids, tg, o, wsb
+
+    # MUL_MAT_ID's expert-weight gradient at the same shapes: 32 experts
+    # [2048, 768], x one row per slot, 8 of 32 experts per token, 512 tokens
+    W, ids, g = synth.moe_back(synth.TYPE_F32)
+    x = synth.normal(synth.tensor_seed(480), 512 * 8 * 2048).reshape(512, 8, 2048)
+    fl = 2.0 * 2048 * 768 * 8 * 512
+    byts = x.nbytes + g.nbytes + ids.nbytes + 4.0 * 2048 * 768 * 32
+    sets = rotation_sets(byts)
+    tx = [torch.from_numpy(x).to(device) for _ in range(sets)]
+    tids = [torch.from_numpy(ids).to(device) for _ in range(sets)]
+    tg = [torch.from_numpy(g).to(device) for _ in range(sets)]
+    o = [torch.empty((32, 768, 2048), dtype=torch.float32, device=device) for _ in range(sets)]
+    wsz = op.oop_mul_mat_id_weight_grad_workspace_size((2048, 8, 512), (768, 8, 512), 32)
+    wsb = torch.empty(max(wsz, 1), dtype=torch.uint8, device=device)
+    us = statistics.mean(time_rotating(torch, [(lambda i=i: op.mul_mat_id_weight_grad(
+        tx[i], tids[i], tg[i], 32, out=o[i], workspace=wsb)) for i in range(sets)],
+        psteps, 2)) * 1e3
+    roof_us = max(byts / (hbm * 1e9), 3 * fl / (tf32_peak * 1e12)) * 1e6
+    parts["mul_mat_id_expert_weight_grad_f32"] = {
+        "workload": "dW [2048, 768, 32] from x [2048, 8, 512], dy [768, 8, 512], 8 of 32 "
+                    "experts per token", "us": round(us, 3),
+        "TFLOP/s": round(fl / (us * 1e-6) / 1e12, 3), "bytes": byts, "rotation_sets": sets,
+        "roof_us": round(roof_us, 2), "roofline_frac": round(roof_us / us, 4)}
+    del tx, tids, tg, o, wsb, x, W, g
 
     clk = clocks.stop()
     assert op.device_status() == 0, "device status word set"

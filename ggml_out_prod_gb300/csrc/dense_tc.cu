@@ -195,14 +195,24 @@ __host__ __device__ __forceinline__ int64_t sk_owner(int64_t iters, int ctas, in
 
 // Where tile t sits: m-tile, n-tile, dst slice, its valid src1 rows, and the
 // first src0 row (k = 0) of the src0 slice it reads.
+// The tile kernel's modes: plain OUT_PROD (every head x batch slice in one
+// grid), grouped (MUL_MAT_ID_BACK: slices are experts, src1 rows are the
+// routed slots sorted by expert, dst rows scattered back to slots) and
+// segmented (MUL_MAT_ID's expert-weight gradient: slice e reduces over its
+// own k range).  A compile-time parameter, so that the plain and grouped
+// kernels carry none of the segmented mode's state.
+constexpr int kModePlain = 0, kModeGrouped = 1, kModeSegmented = 2;
+
 struct Tile {
-    int mt, nt, nkb;              // nkb: k-blocks of this tile
+    int mt, nt;
     int64_t slice, ncols, brow0, a_row0;
-    int64_t kofs, bslice;         // src1 k offset and slice coordinate
+    int nkb;                      // segmented mode: this tile's k-blocks
+    int64_t kofs;                 // segmented mode: src1 k offset
 };
 
-template <bool GROUPED>
+template <int MODE>
 __device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
+    constexpr bool GROUPED = MODE == kModeGrouped;
     Tile d;
     if constexpr (GROUPED) {
         // work-list entries innermost: an expert's n-tiles of one m-tile are
@@ -224,16 +234,19 @@ __device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
     }
     const int64_t i2 = d.slice % p.ne12, i3 = d.slice / p.ne12;
     d.a_row0 = (i3 / p.dps3 * p.ne02 + i2 / p.dps2) * p.K;
-    d.nkb = p.num_kb;
-    d.kofs = 0;
-    d.bslice = d.slice;
-    if (!GROUPED && p.seg_off) {
+    if constexpr (MODE == kModeSegmented) {
         d.kofs = p.seg_off[d.slice];
         d.nkb = p.seg_nkb[d.slice];
         d.a_row0 = d.kofs;
-        d.bslice = 0;
     }
     return d;
+}
+
+// k-blocks of tile t
+template <int MODE>
+__device__ __forceinline__ int tile_nkb(const TcParams &p, const Tile &t) {
+    if constexpr (MODE == kModeSegmented) return t.nkb;
+    else return p.num_kb;
 }
 
 // A CTA's share of the iterations: it0 .. it1 - 1, starting at k-block kb0
@@ -245,21 +258,21 @@ struct Span {
 };
 
 // Walks a CTA's iterations in order; every role keeps its own copy.
-template <bool GROUPED>
+template <int MODE>
 struct Walk {
     int64_t it, end, tile, stride;
     int kb;
     Tile t;
     __device__ __forceinline__ Walk(const TcParams &p, const Span &sp)
         : it(sp.it0), end(sp.it1), tile(sp.tile0), stride(sp.stride), kb(sp.kb0) {
-        if (it < end) t = decode_tile<GROUPED>(p, tile);
+        if (it < end) t = decode_tile<MODE>(p, tile);
     }
     __device__ __forceinline__ void next(const TcParams &p) {
         ++it;
-        if (++kb == t.nkb) {
+        if (++kb == tile_nkb<MODE>(p, t)) {
             kb = 0;
             tile += stride;
-            if (it < end) t = decode_tile<GROUPED>(p, tile);
+            if (it < end) t = decode_tile<MODE>(p, tile);
         }
     }
 };
@@ -349,11 +362,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int TYPE, bool TMA_A, bool GROUPED>
+template <int TYPE, bool TMA_A, int MODE>
 __global__ void __maxnreg__(MAX_REGS)
     tc_out_prod_kernel(const __grid_constant__ CUtensorMap map_bhi,
                        const __grid_constant__ CUtensorMap map_blo,
                        const __grid_constant__ CUtensorMap map_a, const TcParams p) {
+    constexpr bool GROUPED = MODE == kModeGrouped;
     using Raw = RawA<TYPE>;
     constexpr bool HAS_ALO = !is_tf32_exact<TYPE>();   // bf16 / f16 values are TF32 values
     extern __shared__ uint8_t smem_raw[];
@@ -394,8 +408,8 @@ __global__ void __maxnreg__(MAX_REGS)
         if constexpr (GROUPED) {
             if (t >= static_cast<int64_t>(p.mtiles) * *p.grp_ntiles) return;   // no work left
         }
-        if (!GROUPED && p.seg_nkb) {
-            // segmented: this tile's k-block count is its slice's
+        if constexpr (MODE == kModeSegmented) {
+            // this tile's k-block count is its slice's
             it0 = 0;
             it1 = p.seg_nkb[t / (static_cast<int64_t>(p.mtiles) * p.ntiles)];
         } else {
@@ -446,7 +460,7 @@ __global__ void __maxnreg__(MAX_REGS)
             Ring<Raw::RSTAGES> rr;
             Ring<B_STAGES> bb;
             int g = 0;
-            for (Walk<GROUPED> w(p, span); w.it < w.end; w.next(p), rr.next(), bb.next(), ++g) {
+            for (Walk<MODE> w(p, span); w.it < w.end; w.next(p), rr.next(), bb.next(), ++g) {
                 const Tile &t = w.t;
                 // ring slot free (producers done with g - RSTAGES), B stage
                 // free (MMAs of g - B_STAGES completed)
@@ -474,11 +488,13 @@ __global__ void __maxnreg__(MAX_REGS)
                     ptx::tma_load_2d(st + B_IMG, &map_blo, &bars->rfull[r], w.kb * BK,
                                      static_cast<int>(t.brow0));
                 } else {
-                    const int bk = static_cast<int>(t.kofs + static_cast<int64_t>(w.kb) * BK);
-                    ptx::tma_load_3d(st, &map_bhi, &bars->rfull[r], bk, t.nt * BN,
-                                     static_cast<int>(t.bslice));
-                    ptx::tma_load_3d(st + B_IMG, &map_blo, &bars->rfull[r], bk, t.nt * BN,
-                                     static_cast<int>(t.bslice));
+                    // segmented: one src1 slice, each expert's segment at its k offset
+                    const int bk = MODE == kModeSegmented
+                                       ? static_cast<int>(t.kofs + static_cast<int64_t>(w.kb) * BK)
+                                       : w.kb * BK;
+                    const int bs = MODE == kModeSegmented ? 0 : static_cast<int>(t.slice);
+                    ptx::tma_load_3d(st, &map_bhi, &bars->rfull[r], bk, t.nt * BN, bs);
+                    ptx::tma_load_3d(st + B_IMG, &map_blo, &bars->rfull[r], bk, t.nt * BN, bs);
                 }
                 last_ph[r] = static_cast<int>(rr.phase);
             }
@@ -504,14 +520,14 @@ __global__ void __maxnreg__(MAX_REGS)
         // the MMAs of g are being issued; the full wait runs only when such
         // an early test came back negative.
         bool early_a = false, early_e = false;
-        for (Walk<GROUPED> w(p, span); w.it < w.end; w.next(p), aa.next(), bb.next(), ++g) {
+        for (Walk<MODE> w(p, span); w.it < w.end; w.next(p), aa.next(), bb.next(), ++g) {
             const bool seg_first = g == 0 || w.kb == 0;
             if (seg_first) {
                 ++seg;
                 seg_kb0 = w.kb;
             }
             const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
-            const bool chunk_last = in_chunk == CHUNK_KB - 1 || w.kb + 1 == w.t.nkb ||
+            const bool chunk_last = in_chunk == CHUNK_KB - 1 || w.kb + 1 == tile_nkb<MODE>(p, w.t) ||
                                     w.it + 1 == w.end;
             if (in_chunk == 0) ++q;
             const int buf = q & 1;
@@ -590,7 +606,7 @@ __global__ void __maxnreg__(MAX_REGS)
         Ring<Raw::RSTAGES> rr;
         Ring<A_STAGES> aa;
         Ring<B_STAGES> eb;                               // bempty of iteration g - A_STAGES
-        for (Walk<GROUPED> w(p, span); w.it < w.end; w.next(p), rr.next(), aa.next(), ++g) {
+        for (Walk<MODE> w(p, span); w.it < w.end; w.next(p), rr.next(), aa.next(), ++g) {
             const Tile &t = w.t;
             const int64_t m = static_cast<int64_t>(t.mt) * BM + r;
             const bool mok = m < p.M;
@@ -687,10 +703,10 @@ __global__ void __maxnreg__(MAX_REGS)
         uint32_t cmp[FOLD_COLS / 2];
         int seg_kb0 = 0;
         int g = 0, q = -1;
-        for (Walk<GROUPED> w(p, span); w.it < w.end; w.next(p), ++g) {
+        for (Walk<MODE> w(p, span); w.it < w.end; w.next(p), ++g) {
             if (g == 0 || w.kb == 0) seg_kb0 = w.kb;
             const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
-            const bool last = w.kb + 1 == w.t.nkb || w.it + 1 == w.end;   // segment ends
+            const bool last = w.kb + 1 == tile_nkb<MODE>(p, w.t) || w.it + 1 == w.end;   // segment ends
             if (in_chunk == 0) ++q;
             if (in_chunk != CHUNK_KB - 1 && !last) continue;   // once per chunk
             const Tile &t = w.t;
@@ -706,7 +722,7 @@ __global__ void __maxnreg__(MAX_REGS)
             }
             // where a finished segment goes: dst, or a stream-K partial slot
             // (slot 0 for the CTA's first segment, 1 for its last)
-            const bool whole = seg_kb0 == 0 && w.kb + 1 == w.t.nkb;
+            const bool whole = seg_kb0 == 0 && w.kb + 1 == tile_nkb<MODE>(p, w.t);
             const int64_t m = static_cast<int64_t>(t.mt) * BM + row;
             float *dst = GROUPED ? p.dst : p.dst + t.slice * p.N * p.M;
             float *part = nullptr;
@@ -870,7 +886,7 @@ __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__re
             }
         }
     }
-    const Tile d = decode_tile<GROUPED>(p, t);
+    const Tile d = decode_tile<GROUPED ? kModeGrouped : kModePlain>(p, t);
     const int64_t tile_cols = d.ncols - static_cast<int64_t>(d.nt) * BN;
     float *out = GROUPED ? p.dst : p.dst + d.slice * p.N * p.M;
 #pragma unroll
@@ -1265,7 +1281,7 @@ int plan_ctas(int64_t tiles, int num_kb, int sms, size_t partial_room) {
     return 10 * sk < 9 * dp ? G : 0;
 }
 
-template <int TYPE, bool GROUPED>
+template <int TYPE, int MODE>
 cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap &mhi,
                          const CUtensorMap &mlo, const TcParams &p, dim3 grid,
                          cudaStream_t stream) {
@@ -1306,8 +1322,8 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
         if (after && (e = cudaEventRecord(after, stream)) != cudaSuccess) return e;
         return cudaSuccess;
     };
-    return tma_a ? run(tc_out_prod_kernel<TYPE, true, GROUPED>)
-                 : run(tc_out_prod_kernel<TYPE, false, GROUPED>);
+    return tma_a ? run(tc_out_prod_kernel<TYPE, true, MODE>)
+                 : run(tc_out_prod_kernel<TYPE, false, MODE>);
 }
 
 size_t split_bytes(const OutProdShape &s) {
@@ -1414,7 +1430,7 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
 
     switch (s.a_type) {
 #define OOP_TC_CASE(T) \
-    case T: e = launch_typed<T, false>(a, s, mhi, mlo, p, grid, stream); break;
+    case T: e = launch_typed<T, kModePlain>(a, s, mhi, mlo, p, grid, stream); break;
     OOP_TC_CASE(OOP_TYPE_F32)
     OOP_TC_CASE(OOP_TYPE_F16)
     OOP_TC_CASE(OOP_TYPE_BF16)
@@ -1562,7 +1578,7 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     const dim3 grid(static_cast<unsigned>(p.ctas > 0 || p.persistent ? G : max_grid));
     switch (s.w_type) {
 #define OOP_TC_CASE(T) \
-    case T: e = launch_typed<T, true>(W, os, mhi, mlo, p, grid, stream); break;
+    case T: e = launch_typed<T, kModeGrouped>(W, os, mhi, mlo, p, grid, stream); break;
     OOP_TC_CASE(OOP_TYPE_F32)
     OOP_TC_CASE(OOP_TYPE_F16)
     OOP_TC_CASE(OOP_TYPE_BF16)
@@ -1692,7 +1708,7 @@ cudaError_t launch_mmid_wgrad(const float *x, const int32_t *ids, const float *d
     p.seg_off = seg_off;
     p.seg_nkb = seg_nkb;
     const dim3 grid(static_cast<unsigned>(mtiles * ntiles), static_cast<unsigned>(s.E));
-    return launch_typed<OOP_TYPE_F32, false>(xg, os, mhi, mlo, p, grid, stream);
+    return launch_typed<OOP_TYPE_F32, kModeSegmented>(xg, os, mhi, mlo, p, grid, stream);
 }
 
 }  // namespace oop

@@ -485,6 +485,12 @@ def make_b(ne: tuple, tensor_id: int, std: float = 1.0, outliers: bool = False,
 
 # The five workloads, by what they are.
 LORA_RANKS = (4, 8, 24)
+# (in, out) widths of a 4B layer's seven adapted projections (q, k, v, o,
+# gate, up, down): hidden width 2560 as in the rank-r workload, the other
+# widths those of a published 4B decoder with 32 query and 8 key-value heads
+# of 128 and an MLP of 9728
+LAYER_4B_PROJ = ((2560, 4096), (2560, 1024), (2560, 1024), (4096, 2560), (2560, 9728),
+                 (2560, 9728), (9728, 2560))
 DENSE_MK = ((1536, 1536), (5120, 5120), (5120, 17408), (17408, 5120))
 
 
