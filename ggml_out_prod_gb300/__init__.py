@@ -102,7 +102,9 @@ class OopError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.SO
+    """The library file: the in-tree build, or the file named by the
+    environment variable GGML_OUT_PROD_GB300_LIBRARY (e.g. a sanitizer build)."""
+    return os.environ.get("GGML_OUT_PROD_GB300_LIBRARY") or _build.SO
 
 
 def build(force: bool = False) -> str:

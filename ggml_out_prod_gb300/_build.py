@@ -47,14 +47,26 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+# Host code built with AddressSanitizer and UndefinedBehaviorSanitizer (device
+# code unchanged), into its own folder: for the CPU tests of the host-side
+# checks, loaded with the sanitizer runtimes preloaded.
+SANITIZE = ["-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined",
+            "-Xcompiler", "-fno-omit-frame-pointer", "-Xcompiler", "-fno-sanitize-recover=all"]
+
+
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          sanitize: bool = False) -> str:
+    build_dir = os.path.join(BUILD, "sanitize") if sanitize else BUILD
+    so = os.path.join(build_dir, "liboop.so")
+    if sanitize:
+        extra = list(extra or []) + SANITIZE
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     hdrs = _deps()
     objs = []
     jobs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs + [__file__]):
             cmd = [cc, *ARCH, *NVCC_FLAGS, *(extra or []), "-c", src, "-o", obj]
@@ -70,13 +82,13 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _stale(SO, objs):
-        tmp = SO + f".{os.getpid()}.tmp"
+    if force or jobs or _stale(so, objs):
+        tmp = so + f".{os.getpid()}.tmp"
         cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-               "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
+               "-Xlinker", "-rpath,/usr/local/cuda/lib64", *(SANITIZE if sanitize else [])]
         run(cmd)
-        os.replace(tmp, SO)
-    return SO
+        os.replace(tmp, so)
+    return so
 
 
 if __name__ == "__main__":
