@@ -296,6 +296,104 @@ __device__ __forceinline__ float load_a(const uint8_t *row, int64_t m) {
     return decode_row<TYPE>(row, m);
 }
 
+// The scale and offset of one k row's group of elements, for the
+// cooperative decode of staged_half: `blk` is the row's block (32-element
+// types) or super-block (K-quants); `grp` the warp's group (the 32-block in
+// the tile, or the K-quant's 32-element group in its half `h`); `hl` the lane
+// half for types with a scale per 16 elements.  x = fmaf(sc, code, of)
+// reproduces decode() exactly (of = -0.0 keeps the sign of a zero product).
+template <int TYPE>
+__device__ __forceinline__ void block_scale(const uint8_t *blk, int grp, int h, int hl, float &sc,
+                                            float &of, uint32_t &xw) {
+    using namespace qdec;
+    if constexpr (TYPE == OOP_TYPE_Q4_1 || TYPE == OOP_TYPE_Q5_1) {
+        sc = f16(blk);
+        of = f16(blk + 2);
+        if constexpr (TYPE == OOP_TYPE_Q5_1) xw = u32(blk + 4);
+    } else if constexpr (TYPE == OOP_TYPE_Q5_0) {
+        sc = f16(blk);
+        of = -0.0f;
+        xw = u32(blk + 2);
+    } else if constexpr (TYPE == OOP_TYPE_Q4_K || TYPE == OOP_TYPE_Q5_K) {
+        uint32_t s6, m6;
+        scale_min_k4(blk + 4, 4 * h + grp, s6, m6);
+        sc = f16(blk) * static_cast<float>(s6);
+        of = -(f16(blk + 2) * static_cast<float>(m6));
+    } else if constexpr (TYPE == OOP_TYPE_Q6_K) {
+        sc = f16(blk + 208) * static_cast<float>(static_cast<int8_t>(blk[192 + 8 * h + hl + 2 * grp]));
+        of = -0.0f;
+    } else if constexpr (TYPE == OOP_TYPE_Q2_K) {
+        const uint32_t s = blk[8 * h + 2 * grp + hl];
+        sc = f16(blk + 80) * static_cast<float>(s & 0xFu);
+        of = -(f16(blk + 82) * static_cast<float>(s >> 4));
+    } else if constexpr (TYPE == OOP_TYPE_Q3_K) {
+        sc = f16(blk + 108) * static_cast<float>(scale_q3k(blk + 96, 8 * h + 2 * grp + hl));
+        of = -0.0f;
+    }
+}
+
+// The code of element `lane` of the group (see block_scale) in row `blk`.
+template <int TYPE>
+__device__ __forceinline__ int block_code(const uint8_t *blk, int grp, int h, int lane,
+                                          uint32_t xw) {
+    if constexpr (TYPE == OOP_TYPE_Q4_1) {
+        const uint32_t byte = blk[4 + (lane & 15)];
+        return static_cast<int>(lane < 16 ? (byte & 0xFu) : (byte >> 4));
+    } else if constexpr (TYPE == OOP_TYPE_Q5_0 || TYPE == OOP_TYPE_Q5_1) {
+        constexpr int QS = TYPE == OOP_TYPE_Q5_0 ? 6 : 8;
+        const uint32_t byte = blk[QS + (lane & 15)];
+        const uint32_t lo = lane < 16 ? (byte & 0xFu) : (byte >> 4);
+        const int v = static_cast<int>(lo | (((xw >> lane) & 1u) << 4));
+        return TYPE == OOP_TYPE_Q5_0 ? v - 16 : v;
+    } else if constexpr (TYPE == OOP_TYPE_Q4_K || TYPE == OOP_TYPE_Q5_K) {
+        constexpr int QS = TYPE == OOP_TYPE_Q4_K ? 16 : 48;
+        const int sb = 4 * h + grp;
+        uint32_t q = (blk[QS + 32 * (sb >> 1) + lane] >> (4 * (sb & 1))) & 0xFu;
+        if constexpr (TYPE == OOP_TYPE_Q5_K) q |= ((blk[16 + lane] >> sb) & 1u) << 4;
+        return static_cast<int>(q);
+    } else if constexpr (TYPE == OOP_TYPE_Q6_K) {
+        const uint32_t byte = blk[64 * h + lane + 32 * (grp & 1)];
+        const uint32_t lo = grp >= 2 ? (byte >> 4) : (byte & 0xFu);
+        const uint32_t hi = (blk[128 + 32 * h + lane] >> (2 * grp)) & 3u;
+        return static_cast<int>(lo | (hi << 4)) - 32;
+    } else if constexpr (TYPE == OOP_TYPE_Q2_K) {
+        return static_cast<int>((blk[16 + 32 * h + lane] >> (2 * grp)) & 3u);
+    } else if constexpr (TYPE == OOP_TYPE_Q3_K) {
+        const int q2 = static_cast<int>((blk[32 + 32 * h + lane] >> (2 * grp)) & 3u);
+        return q2 - (((blk[lane] >> (4 * h + grp)) & 1u) ? 0 : 4);
+    } else {
+        return 0;
+    }
+}
+
+// The cooperative decode of staged_half straight from global memory, for
+// src0 rows TMA cannot stage (row bytes not a multiple of 16): `row0` is this
+// warp's group in the first of the 16 k rows, `stride` the row bytes; rows
+// nk.. (past K, or all of them for a group past M) are neither read nor used.
+template <int TYPE>
+__device__ __forceinline__ void global_half(const uint8_t *row0, int64_t stride, int nk,
+                                            int quad, int h, int lane, float (&x)[KH]) {
+    const int jr = lane & (KH - 1), hl = lane >> 4;
+    float sc = 0.f, of = 0.f;
+    uint32_t xw = 0;
+    if (jr < nk) block_scale<TYPE>(row0 + jr * stride, quad, h, hl, sc, of, xw);
+    constexpr bool HALVES = TYPE == OOP_TYPE_Q6_K || TYPE == OOP_TYPE_Q2_K ||
+                            TYPE == OOP_TYPE_Q3_K;
+    const int src_add = HALVES ? 16 * (lane >> 4) : 0;
+#pragma unroll
+    for (int j = 0; j < KH; ++j) {
+        const float sj = __shfl_sync(0xffffffffu, sc, j + src_add);
+        const float oj = __shfl_sync(0xffffffffu, of, j + src_add);
+        uint32_t xj = 0;
+        if constexpr (TYPE == OOP_TYPE_Q5_0 || TYPE == OOP_TYPE_Q5_1)
+            xj = __shfl_sync(0xffffffffu, xw, j);
+        x[j] = j < nk ? fmaf(sj, static_cast<float>(block_code<TYPE>(row0 + j * stride, quad, h,
+                                                                        lane, xj)),
+                             oj)
+                      : 0.f;
+    }
+}
+
 // The 16 src0 values (k rows 16*kh .. 16*kh+15 of a staged k-block) of row
 // r of the m-tile.  Lane l of the warp owns row r = 32 * (warp % 4) + l, so a
 // warp covers one quantisation block: its 16 scales are read once (lane j
@@ -313,17 +411,32 @@ __device__ __forceinline__ void staged_half(const uint8_t *slot, int r, int off0
 #pragma unroll
         for (int j = 0; j < KH; ++j) x[j] = decode<TYPE>(rows + j * Raw::ROW_BYTES + 2 * r, 0);
     } else if constexpr (TYPE != OOP_TYPE_Q8_0 && TYPE != OOP_TYPE_Q4_0) {
-        // the other block types: each thread decodes its own element of
-        // every row (the block header reads are warp-wide broadcasts)
-        if constexpr (QFormat<TYPE>::QK == 32) {
-            const uint8_t *blk = rows + off0 + (r >> 5) * Raw::BLOCK;
+        // The other block types.  Every element is scale * code + offset,
+        // where scale and offset depend only on the k row and on which
+        // 32 (or 16) elements of the block the element is in -- and the 32
+        // lanes of a warp are one such group (or two halves of one).  So lane
+        // L works out the scale and offset of row L % 16 for lane half L / 16
+        // once; each lane then takes its row's pair by shuffle and adds its
+        // own code: one fused multiply-add, the same rounding as decode().
+        const int quad = r >> 5;
+        const uint8_t *base = rows + off0 + (QFormat<TYPE>::QK == 32 ? quad * Raw::BLOCK : 0);
+        const int h = mt & 1;                               // K-quants: half of the super-block
+        const int jr = lane & (KH - 1), hl = lane >> 4;
+        float sc, of;
+        uint32_t xw = 0;                                    // q5_0 / q5_1: the fifth bits
+        block_scale<TYPE>(base + jr * Raw::ROW_BYTES, quad, h, hl, sc, of, xw);
+        constexpr bool HALVES = TYPE == OOP_TYPE_Q6_K || TYPE == OOP_TYPE_Q2_K ||
+                                TYPE == OOP_TYPE_Q3_K;      // a scale per 16 elements
+        const int src_add = HALVES ? 16 * (lane >> 4) : 0;
 #pragma unroll
-            for (int j = 0; j < KH; ++j) x[j] = decode<TYPE>(blk + j * Raw::ROW_BYTES, lane);
-        } else {
-            const uint8_t *blk = rows + off0;
-            const int e = (mt & 1) * BM + r;                 // element in the super-block
-#pragma unroll
-            for (int j = 0; j < KH; ++j) x[j] = decode<TYPE>(blk + j * Raw::ROW_BYTES, e);
+        for (int j = 0; j < KH; ++j) {
+            const float sj = __shfl_sync(0xffffffffu, sc, j + src_add);
+            const float oj = __shfl_sync(0xffffffffu, of, j + src_add);
+            uint32_t xj = 0;
+            if constexpr (TYPE == OOP_TYPE_Q5_0 || TYPE == OOP_TYPE_Q5_1)
+                xj = __shfl_sync(0xffffffffu, xw, j);
+            const int q = block_code<TYPE>(base + j * Raw::ROW_BYTES, quad, h, lane, xj);
+            x[j] = fmaf(sj, static_cast<float>(q), oj);
         }
     } else {
         const uint8_t *blk = rows + off0 + (r >> 5) * Raw::BLOCK;
@@ -640,10 +753,22 @@ __global__ void __maxnreg__(MAX_REGS)
                 }
             } else {
                 const uint8_t *a_slice = p.a + t.a_row0 * p.a_row_bytes;
+                if constexpr (!Raw::PLAIN && TYPE != OOP_TYPE_Q8_0 && TYPE != OOP_TYPE_Q4_0) {
+                    // blocks hold whole 32-element groups, so mok is the same
+                    // in every lane: a group past M is neither read nor used
+                    const uint8_t *row0 = a_slice + k0 * p.a_row_bytes +
+                                          raw_tile_byte0<TYPE>(t.mt) +
+                                          (QFormat<TYPE>::QK == 32 ? (r >> 5) * Raw::BLOCK : 0);
+                    const int nk = static_cast<int>(
+                        mok ? std::min<int64_t>(KH, std::max<int64_t>(0, p.K - k0)) : 0);
+                    global_half<TYPE>(row0, p.a_row_bytes, nk, r >> 5, t.mt & 1, lane, x);
+                } else {
 #pragma unroll
-                for (int j = 0; j < KH; ++j) {
-                    const int64_t k = k0 + j;
-                    x[j] = (mok && k < p.K) ? load_a<TYPE>(a_slice + k * p.a_row_bytes, m) : 0.f;
+                    for (int j = 0; j < KH; ++j) {
+                        const int64_t k = k0 + j;
+                        x[j] = (mok && k < p.K) ? load_a<TYPE>(a_slice + k * p.a_row_bytes, m)
+                                                : 0.f;
+                    }
                 }
             }
             __syncwarp();
