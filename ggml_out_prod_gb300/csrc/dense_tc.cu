@@ -512,9 +512,17 @@ __global__ void __maxnreg__(MAX_REGS)
     } else if (p.persistent) {
         const int64_t tiles =
             GROUPED ? static_cast<int64_t>(p.mtiles) * *p.grp_ntiles : p.iters / p.num_kb;
-        const int64_t mine = tiles > blockIdx.x ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
         it0 = 0;
-        it1 = mine * p.num_kb;
+        if constexpr (MODE == kModeSegmented) {
+            // the k-blocks of this CTA's tiles c, c + G, ... (p.iters holds the tile count)
+            it1 = 0;
+            const int64_t per = static_cast<int64_t>(p.mtiles) * p.ntiles;
+            for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) it1 += p.seg_nkb[t / per];
+        } else {
+            const int64_t mine =
+                tiles > blockIdx.x ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+            it1 = mine * p.num_kb;
+        }
         span = {it0, it1, static_cast<int64_t>(blockIdx.x), static_cast<int64_t>(gridDim.x), 0};
     } else {
         const int64_t t = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
@@ -1832,7 +1840,16 @@ cudaError_t launch_mmid_wgrad(const float *x, const int32_t *ids, const float *d
     p.ntiles = static_cast<int>(ntiles);
     p.seg_off = seg_off;
     p.seg_nkb = seg_nkb;
-    const dim3 grid(static_cast<unsigned>(mtiles * ntiles), static_cast<unsigned>(s.E));
+    // persistent by default: one CTA per SM takes whole tiles round-robin, so
+    // the short tiles (a few k-blocks each) flow into one another; the test
+    // hook's data-parallel schedule gives each tile its own CTA
+    const int64_t tiles = mtiles * ntiles * s.E;
+    const int G = std::min(device_sms(), kSkMaxCtas);
+    p.persistent = (g_schedule != 1 && G > 0) ? 1 : 0;
+    p.iters = tiles;
+    const dim3 grid = p.persistent
+                          ? dim3(static_cast<unsigned>(std::min<int64_t>(G, tiles)))
+                          : dim3(static_cast<unsigned>(mtiles * ntiles), static_cast<unsigned>(s.E));
     return launch_typed<OOP_TYPE_F32, kModeSegmented>(xg, os, mhi, mlo, p, grid, stream);
 }
 

@@ -180,11 +180,17 @@ def _wgrad(op, x, ids, dy, E):
     (128, 50, 40, 2, 2, 9),      # most experts with no slot: their gradient is zero
 ])
 def test_expert_weight_grad_whole(op, orc, K, N, E, n_used, n_x, T):
+    """Both schedules: persistent (the default) and one CTA per tile."""
     x, ids, dy = _wgrad_inputs(190 + E, K, N, E, n_used, n_x, T)
     ref = orc.mul_mat_id_weight_grad(x, ids, dy, E)
-    got = _wgrad(op, x, ids, dy, E).cpu().numpy()
-    assert op.device_status() == 0
-    assert_parity(got, ref["f64"], ref["abs"], f"expert weight grad {K}x{N}x{E}")
+    for sched in (op.SCHEDULE_AUTO, op.SCHEDULE_DATA_PARALLEL):
+        op.set_tc_schedule(sched)
+        try:
+            got = _wgrad(op, x, ids, dy, E).cpu().numpy()
+        finally:
+            op.set_tc_schedule(op.SCHEDULE_AUTO)
+        assert op.device_status() == 0
+        assert_parity(got, ref["f64"], ref["abs"], f"expert weight grad {K}x{N}x{E} {sched}")
 
 
 def test_expert_weight_grad_skewed(op, orc):
