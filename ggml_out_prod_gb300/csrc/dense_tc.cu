@@ -12,7 +12,7 @@
 // Launches per call:
 //  1. bsplit: b[slice][k][n] -> bhi, blo [slice][n][Kp] (K-major TF32 words,
 //     Kp = K rounded up to 4) in the caller's workspace;
-//  2. the tile kernel over 128 (m) x 96 (n) dst tiles of every head x batch
+//  2. the tile kernel over 128 (m) x 128 (n) dst tiles of every head x batch
 //     slice in one grid (src0 slice i2/dps2, i3/dps3 -- the broadcast map of
 //     "metal: OUT_PROD runs batched, broadcast and narrow shapes on the GPU");
 //  3. (stream-K schedule only) the fix-up that adds the k-partials of tiles
@@ -20,23 +20,29 @@
 //
 // Work is a list of (tile, k-block) iterations, tile-major.  Data-parallel
 // schedule: CTA c takes the num_kb iterations of tile c.  Stream-K schedule:
-// one CTA per SM, CTA c takes iterations [I*c/G, I*(c+1)/G) of the I in the
-// problem, so the last wave is not left a tenth full; a tile split between
-// CTAs is written as fp32 partials (at most two per CTA: its first and last
-// tile) and summed in k order by the fix-up.  Both are deterministic.
+// one CTA per SM; the full waves of tiles are taken whole, round-robin (so the
+// CTAs run in step along k and share the src0 and src1 rows they read in L2),
+// and the iterations of the last, partial wave's tiles are split evenly, CTA
+// c taking [I*c/G, I*(c+1)/G) of them, so that wave is not left a tenth full;
+// a tile split between CTAs is written as fp32 partials (at most two per CTA:
+// its first and last tile of the split range) and summed in k order by the
+// fix-up.  Both are deterministic.
 //
-// Tile kernel roles (576 threads = 18 warps at 96 registers, which is what
-// one SM sub-partition's register file holds for the five warps it gets):
-//  warp 0      TMA: raw src0 rows (32 k x one m-tile of f32 / bf16 words or
-//              q8_0 / q4_0 blocks) into a ring, bhi/blo tiles (32 k x 96 n,
-//              128-byte swizzle) into the B stages
-//  warp 1      TMEM allocation; the MMA loop (M128 N96 K8, A from tensor
+// Tile kernel roles (640 threads = 20 warps = 5 warpgroups, launched at 96
+// registers a thread, which one SM sub-partition holds for its five warps;
+// then traded between warpgroups with setmaxnreg):
+//  warpgroup 0 (48 registers)
+//    warp 0    TMA: raw src0 rows (32 k x one m-tile of the src0 type) into a
+//              ring, bhi/blo tiles (32 k x 128 n, 128-byte swizzle) into the
+//              B stages
+//    warp 1    TMEM allocation; the MMA loop (M128 N128 K8, A from tensor
 //              memory, B from shared memory), one elected lane issuing
-//  warps 2-9   src0 producer, thread = row of the m-tile = TMEM lane, two
-//              warps per lane quarter each taking 16 of the block's 32 k:
-//              raw ring -> dequantise -> split -> a_hi / a_lo columns of an
-//              A stage in tensor memory (tcgen05.st)
-//  warps 10-17 fold + epilogue: TMEM -> registers -> dst
+//    warps 2-3 idle
+//  warpgroups 1-2 (72 registers): src0 producer, thread = row of the m-tile
+//              = TMEM lane, two warps per lane quarter each taking 16 of the
+//              block's 32 k: raw ring -> dequantise -> split -> a_hi / a_lo
+//              columns of an A stage in tensor memory (tcgen05.st)
+//  warpgroups 3-4 (144 registers): fold + epilogue, TMEM -> registers -> dst
 // When src0's rows are not 16-byte aligned (TMA's rule), the producer loads
 // src0 from global memory itself instead of from the ring.
 //
@@ -50,13 +56,15 @@
 //    of a tile (all of K in the data-parallel schedule);
 //  * the big term a_hi*b_hi goes to D1, restarted every CHUNK_KB k-blocks
 //    (so at most 8 MMAs accumulate into it);
-//  * the fold warps add each finished D1 chunk into a Kahan pair: the sum S
-//    lives in TMEM, the compensation C in registers (48 columns per thread,
-//    kept as bfloat16 pairs).
-// TMEM columns: [0,96) D1 buffer 0, [96,192) D1 buffer 1, [192,288) D2,
-// [288,384) S, [384,448) and [448,512) the two A stages (a_hi in the first
-// 32 columns, a_lo in the next 32).  The MMA fills one D1 buffer while the
-// fold drains the other.
+//  * the fold warps add each finished D1 chunk into a Kahan pair kept in
+//    registers: each fold thread owns one row's 64 columns, their sums S and
+//    their compensations C (as bfloat16 pairs).
+// TMEM columns: [0,128) D1 buffer 0, [128,256) D1 buffer 1, [256,384) D2,
+// [384,448) and [448,512) the two A stages (a_hi in the first 32 columns,
+// a_lo in the next 32).  The MMA fills one D1 buffer while the fold drains
+// the other.  With S out of tensor memory the tile is 128 columns wide: every
+// producer instruction (dequantise, split) and every B byte feeds a third more
+// MMA work than at 96, the widest tile with S in tensor memory as well.
 //
 // Every wait is bounded (1 s of globaltimer); running out records
 // OOP_ERR_DEVICE_TIMEOUT, sets a CTA-wide abort flag, drains the copies and
@@ -75,25 +83,37 @@ namespace oop {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 96;
+constexpr int BN = kTcTileN;                 // 128
+static_assert(BN == 128, "the fold's layout and the TMEM map assume 128 columns");
 constexpr int BK = 32;                      // tf32 per 128-byte swizzle row
 constexpr int CHUNK_KB = 2;                 // k-blocks per D1 chunk
-constexpr int B_STAGES = 6;                 // bhi + blo stages in shared memory
+constexpr int MAX_BSTAGES = 6;              // bhi + blo stages in shared memory
 constexpr int A_STAGES = 2;                 // a_hi + a_lo stages in tensor memory
-constexpr int THREADS = 576;                // 18 warps, 96 registers each
-constexpr int MAX_REGS = 96;                // 5 warps x 32 lanes x 96 fill one SMSP
+constexpr int THREADS = 640;                // 20 warps = 5 warpgroups
+constexpr int MAX_REGS = 96;                // at launch: 5 warps x 32 lanes x 96 fill one SMSP
+// Warp roles: warpgroup 0 = TMA (warp 0), MMA (warp 1) and two idle warps;
+// warpgroups 1-2 the src0 producer; warpgroups 3-4 the fold.  Once set up,
+// the warpgroups trade registers (setmaxnreg): 48 for warpgroup 0, 72 for the
+// producer, 144 for the fold, which keeps its 64 running sums and their
+// compensations in registers.  The split uses exactly what the block was
+// launched with, and each sub-partition's share fits its register file.
+constexpr int WARP_PROD0 = 4, WARP_FOLD0 = 12;
+constexpr int REGS_CTRL = 48, REGS_PROD = 72, REGS_FOLD = 144;
+static_assert(4 * REGS_CTRL + 8 * REGS_PROD + 8 * REGS_FOLD == THREADS / 32 * MAX_REGS,
+              "register split must equal the launch allocation");
+static_assert(REGS_CTRL + 2 * REGS_PROD + 2 * REGS_FOLD <= 512, "registers per sub-partition");
 constexpr int PRODUCER_THREADS = 256;
 constexpr int KH = BK / 2;                  // k per producer thread and block
 constexpr int FOLD_THREADS = 256;
 constexpr int FOLD_COLS = BN / 2;           // columns per fold thread
-constexpr int B_IMG = BN * BK * 4;          // 12 KB
+constexpr int B_IMG = BN * BK * 4;          // 16 KB
 constexpr int STAGE_BYTES = 2 * B_IMG;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_D2 = 2 * BN;
-constexpr uint32_t COL_S = 3 * BN;
 constexpr uint32_t COL_A = 384;
 constexpr uint32_t A_COLS = 2 * BK;         // a_hi then a_lo, one column per k
-static_assert(4 * BN <= COL_A && COL_A + A_STAGES * A_COLS == TMEM_COLS, "tensor memory map");
+static_assert(3 * BN <= COL_A && COL_A + A_STAGES * A_COLS == TMEM_COLS, "tensor memory map");
+constexpr size_t SMEM_LIMIT = 232448;       // dynamic shared memory per CTA
 static_assert(BN % 16 == 0 && FOLD_COLS % 16 == 0, "MMA N and fold pieces");
 constexpr uint64_t WAIT_NS = 1000000000ull;
 constexpr int MAX_RSTAGES = 4;
@@ -119,7 +139,7 @@ struct RawA {
     static constexpr int ROW_BYTES = (SPAN + MAXOFF + 15) / 16 * 16;   // bytes per staged k row
     static constexpr int BOX_X = PLAIN ? BM : ROW_BYTES;              // in map elements
     static constexpr int SLOT = (ROW_BYTES * BK + 1023) / 1024 * 1024;
-    static constexpr int RSTAGES = TYPE == OOP_TYPE_F32 ? 3 : 4;
+    static constexpr int RSTAGES = TYPE == OOP_TYPE_F32 ? 2 : 4;   // f32: room for 3 B stages
 };
 
 // Byte offset, in a src0 row, of the first byte m-tile `mt` needs.
@@ -133,11 +153,11 @@ __host__ __device__ __forceinline__ int64_t raw_tile_byte0(int64_t mt) {
 
 struct Bars {
     // Iteration g (one k-block of one tile) uses ring slot g % RSTAGES, B
-    // stage g % B_STAGES and A stage g % A_STAGES.
+    // stage g % b_stages and A stage g % A_STAGES.
     uint64_t rfull[MAX_RSTAGES];  // every TMA copy of the iteration landed (raw src0, B)
     uint64_t rempty[MAX_RSTAGES]; // the producers are done with ring slot r
     uint64_t afull[A_STAGES];     // the producers wrote A stage s (and saw its B land)
-    uint64_t bempty[B_STAGES];    // the iteration's MMAs completed: its B stage and
+    uint64_t bempty[MAX_BSTAGES]; // the iteration's MMAs completed: its B stage and
                                   // its A stage are free
     uint64_t accf[2];             // D1 buffer b holds a finished chunk
     uint64_t acce[2];             // D1 buffer b was drained by the fold
@@ -150,9 +170,20 @@ struct Bars {
 template <int TYPE>
 constexpr bool elementwise_type() { return is_plain_type<TYPE>(); }
 
+// Shared memory: [B stages][raw src0 ring][barriers], from a 1024-byte
+// boundary (the 128-byte swizzle's); as many B stages as fit, up to six.
+template <int TYPE>
+constexpr size_t smem_fixed_bytes() {
+    return RawA<TYPE>::RSTAGES * RawA<TYPE>::SLOT + sizeof(Bars) + 1024;
+}
+template <int TYPE>
+constexpr int b_stages() {
+    return static_cast<int>(std::min<size_t>(MAX_BSTAGES,
+                                             (SMEM_LIMIT - smem_fixed_bytes<TYPE>()) / STAGE_BYTES));
+}
 template <int TYPE>
 constexpr size_t smem_bytes() {
-    return B_STAGES * STAGE_BYTES + RawA<TYPE>::RSTAGES * RawA<TYPE>::SLOT + sizeof(Bars) + 1024;
+    return b_stages<TYPE>() * STAGE_BYTES + smem_fixed_bytes<TYPE>();
 }
 
 struct TcParams {
@@ -249,30 +280,52 @@ __device__ __forceinline__ int tile_nkb(const TcParams &p, const Tile &t) {
     else return p.num_kb;
 }
 
-// A CTA's share of the iterations: it0 .. it1 - 1, starting at k-block kb0
-// of tile tile0; after a tile's last k-block the walk moves `stride` tiles on
-// (1 for a contiguous range, the grid size for whole tiles taken round-robin).
+// A CTA's share of the iterations, in up to two phases: first it0 .. it1 - 1
+// (a local count), starting at k-block kb0 of tile tile0, moving `stride`
+// tiles on after a tile's last k-block (1 for a contiguous range, the grid
+// size for whole tiles taken round-robin); then the global iterations
+// b0 .. b1 - 1 (a stream-K range, tile-major), if b0 < b1.
 struct Span {
     int64_t it0, it1, tile0, stride;
     int kb0;
+    int64_t b0, b1;
 };
 
-// Walks a CTA's iterations in order; every role keeps its own copy.
+// Walks a CTA's iterations in order; every role keeps its own copy.  `fresh`
+// marks the first iteration of each phase (a new segment, whatever its kb),
+// `split` the stream-K phase.
 template <int MODE>
 struct Walk {
-    int64_t it, end, tile, stride;
-    int kb;
+    int64_t it, end, nb0, nb1;
+    int tile, stride, kb;
+    bool fresh, split;
     Tile t;
     __device__ __forceinline__ Walk(const TcParams &p, const Span &sp)
-        : it(sp.it0), end(sp.it1), tile(sp.tile0), stride(sp.stride), kb(sp.kb0) {
+        : it(sp.it0), end(sp.it1), nb0(sp.b0), nb1(sp.b1), tile(static_cast<int>(sp.tile0)),
+          stride(static_cast<int>(sp.stride)), kb(sp.kb0), fresh(true), split(false) {
         if (it < end) t = decode_tile<MODE>(p, tile);
+        else second(p);
+    }
+    // switch to the stream-K range, if any
+    __device__ __forceinline__ void second(const TcParams &p) {
+        if (nb0 >= nb1) return;
+        it = nb0;
+        end = nb1;
+        nb0 = nb1;
+        tile = static_cast<int>(it / p.num_kb);
+        kb = static_cast<int>(it % p.num_kb);
+        stride = 1;
+        fresh = split = true;
+        t = decode_tile<MODE>(p, tile);
     }
     __device__ __forceinline__ void next(const TcParams &p) {
         ++it;
+        fresh = false;
         if (++kb == tile_nkb<MODE>(p, t)) {
             kb = 0;
             tile += stride;
             if (it < end) t = decode_tile<MODE>(p, tile);
+            else second(p);
         }
     }
 };
@@ -486,7 +539,8 @@ __global__ void __maxnreg__(MAX_REGS)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *ring = smem + B_STAGES * STAGE_BYTES;
+    constexpr int BST = b_stages<TYPE>();
+    uint8_t *ring = smem + BST * STAGE_BYTES;
     Bars *bars = reinterpret_cast<Bars *>(ring + Raw::RSTAGES * Raw::SLOT);
     volatile int *abort = &bars->abort;
 
@@ -503,12 +557,20 @@ __global__ void __maxnreg__(MAX_REGS)
     int64_t it0, it1;
     Span span = {};
     if (p.ctas > 0) {
-        // grouped: the tile count is known on the device only
-        const int64_t iters =
-            GROUPED ? static_cast<int64_t>(p.mtiles) * *p.grp_ntiles * p.num_kb : p.iters;
-        it0 = sk_begin(iters, p.ctas, blockIdx.x);
-        it1 = sk_begin(iters, p.ctas, blockIdx.x + 1);
-        span = {it0, it1, it0 / p.num_kb, 1, static_cast<int>(it0 % p.num_kb)};
+        // stream-K: the full waves of whole tiles first, round-robin (all CTAs
+        // at the same k, so the src0 and src1 rows they read are shared in
+        // L2), then the tail tiles' iterations split evenly; every CTA gets
+        // the same number of iterations to within one.  Grouped: the tile
+        // count is known on the device only.
+        const int64_t tiles =
+            GROUPED ? static_cast<int64_t>(p.mtiles) * *p.grp_ntiles : p.iters / p.num_kb;
+        const int64_t dp_tiles = tiles / p.ctas * p.ctas;
+        const int64_t tail = (tiles - dp_tiles) * p.num_kb, base = dp_tiles * p.num_kb;
+        span = {0, dp_tiles / p.ctas * p.num_kb, static_cast<int64_t>(blockIdx.x), p.ctas, 0,
+                base + sk_begin(tail, p.ctas, blockIdx.x),
+                base + sk_begin(tail, p.ctas, blockIdx.x + 1)};
+        it0 = 0;
+        it1 = span.it1 + (span.b1 - span.b0);
     } else if (p.persistent) {
         const int64_t tiles =
             GROUPED ? static_cast<int64_t>(p.mtiles) * *p.grp_ntiles : p.iters / p.num_kb;
@@ -542,7 +604,7 @@ __global__ void __maxnreg__(MAX_REGS)
     if (it0 >= it1) return;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < B_STAGES; ++s) ptx::mbar_init(&bars->bempty[s], 1);
+        for (int s = 0; s < BST; ++s) ptx::mbar_init(&bars->bempty[s], 1);
         for (int s = 0; s < A_STAGES; ++s) ptx::mbar_init(&bars->afull[s], PRODUCER_THREADS);
         for (int r = 0; r < Raw::RSTAGES; ++r) {
             ptx::mbar_init(&bars->rfull[r], 1);
@@ -572,161 +634,180 @@ __global__ void __maxnreg__(MAX_REGS)
     if constexpr (!GROUPED) ptx::griddep_wait();   // the split of src1 is complete
     const uint32_t tmem = bars->tmem_base;
     bool timed_out = false;
-
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            int last_ph[MAX_RSTAGES];           // parity of each slot's last copy, -1: none
-            for (int r = 0; r < MAX_RSTAGES; ++r) last_ph[r] = -1;
-            Ring<Raw::RSTAGES> rr;
-            Ring<B_STAGES> bb;
-            int g = 0;
-            for (Walk<MODE> w(p, span); w.it < w.end; w.next(p), rr.next(), bb.next(), ++g) {
-                const Tile &t = w.t;
-                // ring slot free (producers done with g - RSTAGES), B stage
-                // free (MMAs of g - B_STAGES completed)
-                const int r = rr.slot, s = bb.slot;
-                if (!ptx::mbar_wait_bounded(&bars->rempty[r], rr.phase ^ 1, abort, true, WAIT_NS,
-                                            &timed_out) ||
-                    !ptx::mbar_wait_bounded(&bars->bempty[s], bb.phase ^ 1, abort, true, WAIT_NS,
-                                            &timed_out))
+    // The register split: one setmaxnreg per warpgroup, executed by all its
+    // warps at the head of the warpgroup's branch, before any wait, so the
+    // fold's request is met once the others have given theirs back.
+    if (warp < WARP_PROD0) {
+        ptx::setmaxnreg_dec<REGS_CTRL>();
+        if (warp == 0) {
+            // ---------------- TMA producer ----------------
+            if (lane == 0) {
+                int last_ph[MAX_RSTAGES];           // parity of each slot's last copy, -1: none
+                for (int r = 0; r < MAX_RSTAGES; ++r) last_ph[r] = -1;
+                Ring<Raw::RSTAGES> rr;
+                Ring<BST> bb;
+                int g = 0;
+                for (Walk<MODE> w(p, span); w.it < w.end; w.next(p), rr.next(), bb.next(), ++g) {
+                    const Tile &t = w.t;
+                    // ring slot free (producers done with g - RSTAGES), B stage
+                    // free (MMAs of g - BST completed)
+                    const int r = rr.slot, s = bb.slot;
+                    if (!ptx::mbar_wait_bounded(&bars->rempty[r], rr.phase ^ 1, abort, true, WAIT_NS,
+                                                &timed_out) ||
+                        !ptx::mbar_wait_bounded(&bars->bempty[s], bb.phase ^ 1, abort, true, WAIT_NS,
+                                                &timed_out))
+                        break;
+                    if (p.inject == 1 && g == 0) continue;   // test hook: drop one iteration
+                    uint8_t *st = smem + s * STAGE_BYTES;
+                    ptx::mbar_arrive_expect_tx(
+                        &bars->rfull[r],
+                        static_cast<uint32_t>(2 * B_IMG + (TMA_A ? Raw::ROW_BYTES * BK : 0)));
+                    if constexpr (TMA_A) {
+                        const int box_x = elementwise_type<TYPE>()
+                                              ? t.mt * BM
+                                              : static_cast<int>(raw_tile_byte0<TYPE>(t.mt) & ~15);
+                        ptx::tma_load_2d(ring + r * Raw::SLOT, &map_a, &bars->rfull[r], box_x,
+                                         static_cast<int>(t.a_row0 + static_cast<int64_t>(w.kb) * BK));
+                    }
+                    if constexpr (GROUPED) {
+                        ptx::tma_load_2d(st, &map_bhi, &bars->rfull[r], w.kb * BK,
+                                         static_cast<int>(t.brow0));
+                        ptx::tma_load_2d(st + B_IMG, &map_blo, &bars->rfull[r], w.kb * BK,
+                                         static_cast<int>(t.brow0));
+                    } else {
+                        // segmented: one src1 slice, each expert's segment at its k offset
+                        const int bk = MODE == kModeSegmented
+                                           ? static_cast<int>(t.kofs + static_cast<int64_t>(w.kb) * BK)
+                                           : w.kb * BK;
+                        const int bs = MODE == kModeSegmented ? 0 : static_cast<int>(t.slice);
+                        ptx::tma_load_3d(st, &map_bhi, &bars->rfull[r], bk, t.nt * BN, bs);
+                        ptx::tma_load_3d(st + B_IMG, &map_blo, &bars->rfull[r], bk, t.nt * BN, bs);
+                    }
+                    last_ph[r] = static_cast<int>(rr.phase);
+                }
+                // copies in flight must land before the CTA's smem is released
+                for (int r = 0; r < Raw::RSTAGES; ++r)
+                    if (last_ph[r] >= 0)
+                        ptx::mbar_wait_bounded(&bars->rfull[r], static_cast<uint32_t>(last_ph[r]),
+                                               abort, false, WAIT_NS, &timed_out);
+            }
+        } else if (warp == 1) {
+            // ---------------- MMA issuer ----------------
+            // The whole warp runs the loop, so its control flow and operands are
+            // warp-uniform (kept in uniform registers); one elected lane issues.
+            constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
+            const uint32_t d2 = tmem + COL_D2;
+            const uint64_t desc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(smem));
+            int g = 0, q = -1, seg = -1;         // iteration, chunk, segment counters
+            int seg_kb0 = 0;
+            Ring<A_STAGES> aa;
+            Ring<BST> bb;
+            // A test of a barrier costs ~100 cycles even when its phase is long
+            // complete, the warp issues nothing while a test's result is
+            // outstanding, and the tensor core queues only about two MMAs beyond
+            // the one executing.  So every barrier iteration g+1 needs is tested
+            // right after the MMAs of g are issued, all at once (one barrier per
+            // lane); the blocking waits run only when that test came back
+            // negative.
+            bool ready = false;
+            for (Walk<MODE> w(p, span); w.it < w.end; ++g) {
+                const bool seg_first = w.fresh || w.kb == 0;
+                if (seg_first) {
+                    ++seg;
+                    seg_kb0 = w.kb;
+                }
+                const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
+                const bool seg_last = w.kb + 1 == tile_nkb<MODE>(p, w.t) || w.it + 1 == w.end;
+                const bool chunk_last = in_chunk == CHUNK_KB - 1 || seg_last;
+                if (in_chunk == 0) ++q;
+                const int buf = q & 1;
+                const int s = bb.slot, sa = aa.slot;
+                // D1 buffer drained by the fold; D2 read at the previous segment's
+                // end; this block's A stage written (its producers also saw its B
+                // stage land)
+                // D2 is first written at a segment's second block (its first
+                // block keeps every product in the fresh D1 chunk), so the wait for
+                // the fold to have read the previous segment's D2 sits there
+                const int seg_pos = w.kb - seg_kb0;
+                if (!ready &&
+                    ((in_chunk == 0 &&
+                      !warp_wait(&bars->acce[buf], (static_cast<uint32_t>(q >> 1) & 1) ^ 1, abort,
+                                 &timed_out)) ||
+                     (seg_pos == 1 && seg > 0 &&
+                      !warp_wait(&bars->d2free, static_cast<uint32_t>(seg - 1) & 1, abort,
+                                 &timed_out)) ||
+                     !warp_wait(&bars->afull[sa], aa.phase, abort, &timed_out)))
                     break;
-                if (p.inject == 1 && g == 0) continue;   // test hook: drop one iteration
-                uint8_t *st = smem + s * STAGE_BYTES;
-                ptx::mbar_arrive_expect_tx(
-                    &bars->rfull[r],
-                    static_cast<uint32_t>(2 * B_IMG + (TMA_A ? Raw::ROW_BYTES * BK : 0)));
-                if constexpr (TMA_A) {
-                    const int box_x = elementwise_type<TYPE>()
-                                          ? t.mt * BM
-                                          : static_cast<int>(raw_tile_byte0<TYPE>(t.mt) & ~15);
-                    ptx::tma_load_2d(ring + r * Raw::SLOT, &map_a, &bars->rfull[r], box_x,
-                                     static_cast<int>(t.a_row0 + static_cast<int64_t>(w.kb) * BK));
+                ptx::tc_fence_after();
+                const uint32_t d1 = tmem + static_cast<uint32_t>(buf * BN);
+                const uint32_t ahi = tmem + COL_A + static_cast<uint32_t>(sa) * A_COLS;
+                const uint32_t alo = ahi + BK;
+                // descriptor start addresses count 16-byte units
+                const uint64_t dhi = desc0 + static_cast<uint64_t>((s * STAGE_BYTES) >> 4);
+                const uint64_t dlo = dhi + (B_IMG >> 4);
+                // the barrier each lane tests for iteration g+1 while g's MMAs are
+                // issued: its A stage (lane 0), its D1 buffer if it starts a chunk
+                // (lane 1), D2 if it is its segment's second block (lane 2)
+                uint64_t *tbar;
+                uint32_t tpar;
+                {
+                    Ring<A_STAGES> an = aa;
+                    an.next();
+                    tbar = &bars->afull[an.slot];
+                    tpar = an.phase;
                 }
-                if constexpr (GROUPED) {
-                    ptx::tma_load_2d(st, &map_bhi, &bars->rfull[r], w.kb * BK,
-                                     static_cast<int>(t.brow0));
-                    ptx::tma_load_2d(st + B_IMG, &map_blo, &bars->rfull[r], w.kb * BK,
-                                     static_cast<int>(t.brow0));
-                } else {
-                    // segmented: one src1 slice, each expert's segment at its k offset
-                    const int bk = MODE == kModeSegmented
-                                       ? static_cast<int>(t.kofs + static_cast<int64_t>(w.kb) * BK)
-                                       : w.kb * BK;
-                    const int bs = MODE == kModeSegmented ? 0 : static_cast<int>(t.slice);
-                    ptx::tma_load_3d(st, &map_bhi, &bars->rfull[r], bk, t.nt * BN, bs);
-                    ptx::tma_load_3d(st + B_IMG, &map_blo, &bars->rfull[r], bk, t.nt * BN, bs);
+                if (lane == 1 && chunk_last) {
+                    tbar = &bars->acce[(q + 1) & 1];
+                    tpar = (static_cast<uint32_t>((q + 1) >> 1) & 1) ^ 1;
                 }
-                last_ph[r] = static_cast<int>(rr.phase);
-            }
-            // copies in flight must land before the CTA's smem is released
-            for (int r = 0; r < Raw::RSTAGES; ++r)
-                if (last_ph[r] >= 0)
-                    ptx::mbar_wait_bounded(&bars->rfull[r], static_cast<uint32_t>(last_ph[r]),
-                                           abort, false, WAIT_NS, &timed_out);
-        }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        // The whole warp runs the loop, so its control flow and operands are
-        // warp-uniform (kept in uniform registers); one elected lane issues.
-        constexpr uint32_t idesc = ptx::idesc_tf32(BM, BN);
-        const uint32_t d2 = tmem + COL_D2;
-        const uint64_t desc0 = ptx::sw128_kmajor_desc(ptx::smem_u32(smem));
-        int g = 0, q = -1, seg = -1;         // iteration, chunk, segment counters
-        int seg_kb0 = 0;
-        Ring<A_STAGES> aa;
-        Ring<B_STAGES> bb;
-        // A test of a barrier costs ~100 cycles even when its phase is long
-        // complete, so the barriers of iteration g+1 are tested early, while
-        // the MMAs of g are being issued; the full wait runs only when such
-        // an early test came back negative.
-        bool early_a = false, early_e = false;
-        for (Walk<MODE> w(p, span); w.it < w.end; w.next(p), aa.next(), bb.next(), ++g) {
-            const bool seg_first = g == 0 || w.kb == 0;
-            if (seg_first) {
-                ++seg;
-                seg_kb0 = w.kb;
-            }
-            const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
-            const bool chunk_last = in_chunk == CHUNK_KB - 1 || w.kb + 1 == tile_nkb<MODE>(p, w.t) ||
-                                    w.it + 1 == w.end;
-            if (in_chunk == 0) ++q;
-            const int buf = q & 1;
-            const int s = bb.slot, sa = aa.slot;
-            // D1 buffer drained by the fold; D2 read at the previous segment's
-            // end; this block's A stage written (its producers also saw its B
-            // stage land)
-            // D2 is first written at a segment's second block (its first
-            // block keeps every product in the fresh D1 chunk), so the wait for
-            // the fold to have read the previous segment's D2 sits there
-            const int seg_pos = w.kb - seg_kb0;
-            if ((in_chunk == 0 && !__all_sync(0xffffffffu, early_e) &&
-                 !warp_wait(&bars->acce[buf], (static_cast<uint32_t>(q >> 1) & 1) ^ 1, abort,
-                            &timed_out)) ||
-                (seg_pos == 1 && seg > 0 &&
-                 !warp_wait(&bars->d2free, static_cast<uint32_t>(seg - 1) & 1, abort,
-                            &timed_out)) ||
-                (!__all_sync(0xffffffffu, early_a) &&
-                 !warp_wait(&bars->afull[sa], aa.phase, abort, &timed_out)))
-                break;
-            // early tests for g+1 (its A stage; its D1 buffer if it starts a chunk)
-            {
-                Ring<A_STAGES> an = aa;
-                an.next();
-                early_a = ptx::mbar_test_wait(&bars->afull[an.slot], an.phase);
-            }
-            early_e = chunk_last &&
-                      ptx::mbar_test_wait(&bars->acce[(q + 1) & 1],
-                                          (static_cast<uint32_t>((q + 1) >> 1) & 1) ^ 1);
-            ptx::tc_fence_after();
-            const uint32_t d1 = tmem + static_cast<uint32_t>(buf * BN);
-            const uint32_t ahi = tmem + COL_A + static_cast<uint32_t>(sa) * A_COLS;
-            const uint32_t alo = ahi + BK;
-            // descriptor start addresses count 16-byte units
-            const uint64_t dhi = desc0 + static_cast<uint64_t>((s * STAGE_BYTES) >> 4);
-            const uint64_t dlo = dhi + (B_IMG >> 4);
-            if (ptx::elect_one()) {
+                if (lane == 2 && seg_pos == 0 && !seg_last && seg > 0) {
+                    tbar = &bars->d2free;
+                    tpar = static_cast<uint32_t>(seg - 1) & 1;
+                }
+                const uint32_t lead = ptx::elect_one() ? 1u : 0u;
+                uint32_t ok;
                 if constexpr (HAS_ALO) {
                     if (seg_pos == 0)   // every product into the fresh D1, small ones first
-                        ptx::mma_block_3xtf32_one(d1, ahi, alo, dhi, dlo, idesc);
+                        ok = ptx::mma_block_3xtf32_one_test(d1, ahi, alo, dhi, dlo, idesc, lead, tbar,
+                                                            tpar);
                     else                // cross terms into D2, the big term into D1
-                        ptx::mma_block_3xtf32(d1, d2, ahi, alo, dhi, dlo, idesc, in_chunk == 0,
-                                              seg_pos == 1);
+                        ok = ptx::mma_block_3xtf32_test(d1, d2, ahi, alo, dhi, dlo, idesc,
+                                                        in_chunk == 0, seg_pos == 1, lead, tbar, tpar);
                 } else {
-                    // bf16 src0: a_lo is zero, one cross term
-#pragma unroll
-                    for (int kk = 0; kk < BK / 8; ++kk) {
-                        const uint64_t off = kk * 2;    // 8 tf32 = 32 bytes along k
-                        ptx::mma_tf32_ta(seg_pos == 0 ? d1 : d2, ahi + kk * 8, dlo + off, idesc,
-                                         (seg_pos <= 1 && kk == 0) ? 0u : 1u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < BK / 8; ++kk)
-                        ptx::mma_tf32_ta(d1, ahi + kk * 8, dhi + kk * 2, idesc,
-                                         (in_chunk == 0 && kk == 0 && seg_pos != 0) ? 0u : 1u);
+                    // bf16 / f16 src0: a_lo is zero, one cross term
+                    ok = ptx::mma_block_1xlo_test(seg_pos == 0 ? d1 : d2, d1, ahi, dhi, dlo, idesc,
+                                                  seg_pos <= 1, in_chunk == 0 && seg_pos != 0, lead,
+                                                  tbar, tpar);
                 }
-                ptx::mma_commit(&bars->bempty[s]);
-                if (chunk_last) ptx::mma_commit(&bars->accf[buf]);
+                if (lead) {
+                    ptx::mma_commit(&bars->bempty[s]);
+                    if (chunk_last) ptx::mma_commit(&bars->accf[buf]);
+                }
+                __syncwarp();
+                ready = __all_sync(0xffffffffu, ok != 0);
+                w.next(p);
+                aa.next();
+                bb.next();
+            }
+            // every MMA issued must finish before TMEM is released
+            if (ptx::elect_one()) {
+                ptx::mma_commit(&bars->mma_done);
+                ptx::mbar_wait_bounded(&bars->mma_done, 0, abort, false, WAIT_NS, &timed_out);
             }
             __syncwarp();
-        }
-        // every MMA issued must finish before TMEM is released
-        if (ptx::elect_one()) {
-            ptx::mma_commit(&bars->mma_done);
-            ptx::mbar_wait_bounded(&bars->mma_done, 0, abort, false, WAIT_NS, &timed_out);
-        }
-        __syncwarp();
-    } else if (warp < 10) {
+        }                                                  // warps 2 and 3: idle
+    } else if (warp < WARP_FOLD0) {
         // ---------------- src0 producer ----------------
+        ptx::setmaxnreg_dec<REGS_PROD>();
         const int quad = warp & 3;                       // TMEM lanes 32*quad ..
-        const int kh = (warp - 2) >> 2;                  // k rows KH*kh .. of each block
+        const int kh = (warp - WARP_PROD0) >> 2;         // k rows KH*kh .. of each block
         const int r = 32 * quad + lane;                  // row of the m-tile
         const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
         int g = 0;
         bool early_r = false;
         Ring<Raw::RSTAGES> rr;
         Ring<A_STAGES> aa;
-        Ring<B_STAGES> eb;                               // bempty of iteration g - A_STAGES
+        Ring<BST> eb;                                    // bempty of iteration g - A_STAGES
         for (Walk<MODE> w(p, span); w.it < w.end; w.next(p), rr.next(), aa.next(), ++g) {
             const Tile &t = w.t;
             const int64_t m = static_cast<int64_t>(t.mt) * BM + r;
@@ -825,19 +906,26 @@ __global__ void __maxnreg__(MAX_REGS)
         }
     } else {
         // ---------------- fold + epilogue ----------------
+        ptx::setmaxnreg_inc<REGS_FOLD>();
         const int quad = warp & 3;                          // TMEM lanes 32*quad ..
-        const int half = (warp - 10) >> 2;                  // columns FOLD_COLS*half ..
+        const int half = (warp - WARP_FOLD0) >> 2;          // columns FOLD_COLS*half ..
         const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
         const uint32_t col0 = static_cast<uint32_t>(FOLD_COLS * half);
         const int row = 32 * quad + lane;
-        // Kahan compensations, two columns per register as bfloat16: C is at
-        // most about half an ulp of S, so rounding it to 8 bits costs ~2^-9
-        // ulp of S per fold
-        uint32_t cmp[FOLD_COLS / 2];
+        // this thread's running sums S of its 64 columns, and their Kahan
+        // compensations C, two columns per register as bfloat16 (C is at most
+        // about half an ulp of S, so rounding it to 8 bits costs ~2^-9 ulp of
+        // S per fold)
+        float sreg[FOLD_COLS];
+        uint32_t creg[FOLD_COLS / 2];
         int seg_kb0 = 0;
-        int g = 0, q = -1;
-        for (Walk<MODE> w(p, span); w.it < w.end; w.next(p), ++g) {
-            if (g == 0 || w.kb == 0) seg_kb0 = w.kb;
+        bool seg_split0 = false;        // the segment starts the stream-K range
+        int q = -1;
+        for (Walk<MODE> w(p, span); w.it < w.end; w.next(p)) {
+            if (w.fresh || w.kb == 0) {
+                seg_kb0 = w.kb;
+                seg_split0 = w.fresh && w.split;
+            }
             const int in_chunk = (w.kb - seg_kb0) % CHUNK_KB;
             const bool last = w.kb + 1 == tile_nkb<MODE>(p, w.t) || w.it + 1 == w.end;   // segment ends
             if (in_chunk == 0) ++q;
@@ -849,96 +937,91 @@ __global__ void __maxnreg__(MAX_REGS)
                 break;
             ptx::tc_fence_after();
             const bool first = w.kb - seg_kb0 < CHUNK_KB;       // segment's first chunk
-            if (first) {
-#pragma unroll
-                for (int j = 0; j < FOLD_COLS / 2; ++j) cmp[j] = 0;
-            }
-            // where a finished segment goes: dst, or a stream-K partial slot
-            // (slot 0 for the CTA's first segment, 1 for its last)
-            const bool whole = seg_kb0 == 0 && w.kb + 1 == tile_nkb<MODE>(p, w.t);
-            const int64_t m = static_cast<int64_t>(t.mt) * BM + row;
-            float *dst = GROUPED ? p.dst : p.dst + t.slice * p.N * p.M;
-            float *part = nullptr;
-            if (last && !whole)
-                part = p.partial + (static_cast<int64_t>(blockIdx.x) * 2 +
-                                    (w.it - w.kb + seg_kb0 == it0 ? 0 : 1)) *
-                                       (BM * BN);
-            const int64_t tile_cols = t.ncols - static_cast<int64_t>(t.nt) * BN;
+            // the chunk into (S, C)
 #pragma unroll
             for (int pc = 0; pc < FOLD_COLS / 16; ++pc) {
                 const uint32_t col = col0 + pc * 16;
-                // tcgen05.ld/st are warp-collective (.sync.aligned): the lanes
-                // must be converged after the divergent stores of the last piece
-                __syncwarp();
-                uint32_t xv[16], sv[16];
-                if (first)
-                    ptx::tmem_ld16_wait(tmem + lane_off + buf * BN + col, xv);
-                else
-                    ptx::tmem_ld16x2_wait(tmem + lane_off + buf * BN + col, xv,
-                                          tmem + lane_off + COL_S + col, sv);
-                if (!first) {
+                uint32_t xv[16];
+                ptx::tmem_ld16_wait(tmem + lane_off + buf * BN + col, xv);
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        // Kahan on two columns at once: the running sum is S - C
-                        uint32_t &cb = cmp[pc * 8 + j / 2];
-                        const uint64_t c2 = ptx::unpack_bf16x2(cb);
-                        const uint64_t s2 = ptx::pack2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1]));
-                        const uint64_t x2 = ptx::pack2(__uint_as_float(xv[j]), __uint_as_float(xv[j + 1]));
-                        const uint64_t y2 = ptx::sub2(x2, c2);
-                        const uint64_t t2 = ptx::add2(s2, y2);
-                        float t0, t1, n0, n1;
-                        ptx::unpack2(ptx::sub2(ptx::sub2(t2, s2), y2), n0, n1);
-                        cb = ptx::pack_bf16x2(n0, n1);
-                        ptx::unpack2(t2, t0, t1);
-                        xv[j] = __float_as_uint(t0);
-                        xv[j + 1] = __float_as_uint(t1);
+                for (int j = 0; j < 16; j += 2) {
+                    float &s0 = sreg[pc * 16 + j], &s1 = sreg[pc * 16 + j + 1];
+                    uint32_t &cb = creg[pc * 8 + j / 2];
+                    if (first) {            // S = the first chunk, C = 0
+                        s0 = __uint_as_float(xv[j]);
+                        s1 = __uint_as_float(xv[j + 1]);
+                        cb = 0;
+                        continue;
                     }
-                }
-                // xv now holds S for these 16 columns
-                if (last) {
-                    uint32_t (&dv)[16] = sv;                // D2, the cross terms
-                    __syncwarp();
-                    if (w.kb > seg_kb0) {
-                        ptx::tmem_ld16_wait(tmem + lane_off + COL_D2 + col, dv);
-                    } else {                                // a one-block segment: none
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) dv[j] = 0;
-                    }
-                    if (m < p.M) {
-#pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            float c0, c1;
-                            ptx::unpack2(ptx::unpack_bf16x2(cmp[pc * 8 + j / 2]), c0, c1);
-                            const float v0 = __uint_as_float(xv[j]) + (__uint_as_float(dv[j]) - c0);
-                            const float v1 =
-                                __uint_as_float(xv[j + 1]) + (__uint_as_float(dv[j + 1]) - c1);
-                            const int64_t jc = static_cast<int64_t>(col) + j;   // column in tile
-                            if (part) {
-                                part[jc * BM + row] = v0;
-                                part[(jc + 1) * BM + row] = v1;
-                                continue;
-                            }
-                            int64_t r0 = -1, r1 = -1;                            // dst rows
-                            if constexpr (GROUPED) {
-                                if (jc < tile_cols) r0 = p.grp_rows[t.brow0 + jc];
-                                if (jc + 1 < tile_cols) r1 = p.grp_rows[t.brow0 + jc + 1];
-                            } else {
-                                if (jc < tile_cols) r0 = static_cast<int64_t>(t.nt) * BN + jc;
-                                if (jc + 1 < tile_cols) r1 = static_cast<int64_t>(t.nt) * BN + jc + 1;
-                            }
-                            if (r0 >= 0) dst[r0 * p.M + m] = v0;
-                            if (r1 >= 0) dst[r1 * p.M + m] = v1;
-                        }
-                    }
-                } else {
-                    ptx::tmem_st16(tmem + lane_off + COL_S + col, xv);
+                    // Kahan on two columns at once: the running sum is S - C
+                    const uint64_t c2 = ptx::unpack_bf16x2(cb);
+                    const uint64_t s2 = ptx::pack2(s0, s1);
+                    const uint64_t x2 = ptx::pack2(__uint_as_float(xv[j]), __uint_as_float(xv[j + 1]));
+                    const uint64_t y2 = ptx::sub2(x2, c2);
+                    const uint64_t t2 = ptx::add2(s2, y2);
+                    float n0, n1;
+                    ptx::unpack2(ptx::sub2(ptx::sub2(t2, s2), y2), n0, n1);
+                    cb = ptx::pack_bf16x2(n0, n1);
+                    ptx::unpack2(t2, s0, s1);
                 }
             }
-            __syncwarp();
-            ptx::tmem_wait_st();
+            // the D1 buffer is drained: the MMA may refill it during the epilogue
             ptx::tc_fence_before();
-            if (last) ptx::mbar_arrive(&bars->d2free);
             ptx::mbar_arrive(&bars->acce[buf]);
+            if (!last) continue;
+            // The segment's result S - C + D2 (the cross terms): to dst, or, for
+            // a segment that is not the whole tile, to a stream-K partial slot
+            // (slot 0 for the CTA's first segment of the split range, 1 for its
+            // last).  Each thread writes its row's 64 columns: a warp writes 32
+            // consecutive m of one dst row per column.
+            const bool whole = seg_kb0 == 0 && w.kb + 1 == tile_nkb<MODE>(p, w.t);
+            const bool has_d2 = w.kb > seg_kb0;
+            const int64_t m = static_cast<int64_t>(t.mt) * BM + row;
+            const int tile_cols = static_cast<int>(
+                std::min<int64_t>(BN, t.ncols - static_cast<int64_t>(t.nt) * BN));
+            float *part = whole ? nullptr
+                                : p.partial + (static_cast<int64_t>(blockIdx.x) * 2 +
+                                               (seg_split0 ? 0 : 1)) * (BM * BN) + row;
+            // plain: column jc of the tile is dst row nt * BN + jc
+            float *dcol = (GROUPED ? p.dst : p.dst + t.slice * p.N * p.M) + m;
+            if constexpr (!GROUPED) dcol += static_cast<int64_t>(t.nt) * BN * p.M;
+            // S - C first: the compensations' registers are free for the loads
+#pragma unroll
+            for (int j = 0; j < FOLD_COLS; j += 2) {
+                float c0, c1;
+                ptx::unpack2(ptx::unpack_bf16x2(creg[j / 2]), c0, c1);
+                sreg[j] -= c0;
+                sreg[j + 1] -= c1;
+            }
+#pragma unroll
+            for (int pc = 0; pc < FOLD_COLS / 16; ++pc) {
+                const int col = static_cast<int>(col0) + pc * 16;
+                uint32_t dv[16];
+                __syncwarp();                               // converged for tcgen05.ld
+                ptx::tmem_ld16_wait(tmem + lane_off + COL_D2 + col, dv);
+                if (m >= p.M) continue;
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    // a one-block segment wrote no D2 (it holds an older one)
+                    const float v[2] = {sreg[pc * 16 + j] + (has_d2 ? __uint_as_float(dv[j]) : 0.f),
+                                        sreg[pc * 16 + j + 1] +
+                                            (has_d2 ? __uint_as_float(dv[j + 1]) : 0.f)};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int jc = col + j + e;         // column in the tile
+                        if (part) {
+                            part[jc * BM] = v[e];
+                        } else if (jc < tile_cols) {
+                            if constexpr (GROUPED)
+                                dcol[static_cast<int64_t>(p.grp_rows[t.brow0 + jc]) * p.M] = v[e];
+                            else
+                                dcol[static_cast<int64_t>(jc) * p.M] = v[e];
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bars->d2free);
         }
     }
 
@@ -971,13 +1054,16 @@ static_assert(BM * BN % FIX_THREADS == 0, "fix-up tiling");
 
 template <bool GROUPED, int EPT, int BATCH>
 __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__restrict__ partial,
-                                                               const TcParams p) {
-    const int64_t t = blockIdx.x;
+                                                               const TcParams p, int64_t t_first) {
+    const int64_t t = t_first + blockIdx.x;
     const int64_t tiles = GROUPED ? static_cast<int64_t>(p.mtiles) * *p.grp_ntiles
                                   : p.iters / p.num_kb;
-    if (t >= tiles) return;
-    const int64_t iters = tiles * p.num_kb;
-    const int64_t x0 = t * p.num_kb, x1 = x0 + p.num_kb - 1;
+    // the full waves are whole tiles, written by their CTAs; only the tail
+    // tiles' iterations were split (the tile kernel's stream-K span)
+    const int64_t dp_tiles = tiles / p.ctas * p.ctas;
+    if (t >= tiles || t < dp_tiles) return;
+    const int64_t iters = (tiles - dp_tiles) * p.num_kb;
+    const int64_t x0 = (t - dp_tiles) * p.num_kb, x1 = x0 + p.num_kb - 1;
     const int64_t c0 = sk_owner(iters, p.ctas, x0), c1 = sk_owner(iters, p.ctas, x1);
     if (c0 == c1) return;
     // this thread's elements of the tile: e0 + j * FIX_THREADS, j < EPT
@@ -1034,17 +1120,21 @@ __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const float *__re
     }
 }
 
-// The fix-up for `tiles` tiles (an upper bound for the grouped product)
-// shared out among p.ctas CTAs: the per-element form once a tile has about
-// four partials or more.
+// The fix-up for tiles t_first .. t_first + count - 1: the tail after the
+// full waves (an upper bound, from 0, for the grouped product, whose tile
+// count is on the device); the per-element form once a tile has about four
+// partials or more.
 template <bool GROUPED>
-void launch_fixup(const float *partial, const TcParams &p, int64_t tiles, cudaStream_t stream) {
-    if (p.ctas >= 4 * tiles)
+void launch_fixup(const float *partial, const TcParams &p, int64_t t_first, int64_t count,
+                  cudaStream_t stream) {
+    if (count <= 0) return;
+    if (p.ctas >= 4 * count)
         sk_fixup_kernel<GROUPED, 1, FIX_BATCH>
-            <<<dim3(static_cast<unsigned>(tiles), FIX_CHUNKS), FIX_THREADS, 0, stream>>>(partial, p);
+            <<<dim3(static_cast<unsigned>(count), FIX_CHUNKS), FIX_THREADS, 0, stream>>>(partial, p,
+                                                                                       t_first);
     else
         sk_fixup_kernel<GROUPED, FIX_CHUNKS, 1>
-            <<<static_cast<unsigned>(tiles), FIX_THREADS, 0, stream>>>(partial, p);
+            <<<static_cast<unsigned>(count), FIX_THREADS, 0, stream>>>(partial, p, t_first);
 }
 
 // b[slice][k][n] (n fastest) -> bhi, blo [slice][n][Kp] (k fastest), TF32
@@ -1404,14 +1494,18 @@ int device_sms() { return device_sm_count(); }
 int plan_ctas(int64_t tiles, int num_kb, int sms, size_t partial_room) {
     const int64_t iters = tiles * num_kb;
     const int G = static_cast<int>(std::min<int64_t>(std::min(sms, kSkMaxCtas), iters));
-    if (G <= 0 || g_schedule == 1 || partial_room < static_cast<size_t>(G) * 2 * kSlotBytes)
+    // whole waves only: the stream-K span would be the data-parallel schedule
+    if (G <= 0 || g_schedule == 1 || tiles % G == 0 ||
+        partial_room < static_cast<size_t>(G) * 2 * kSlotBytes)
         return 0;
     if (g_schedule == 2) return G;
     // in k-block times: data-parallel waves x the k-blocks of a tile, against
-    // an even share of the iterations plus the partials and the fix-up (~12)
+    // an even share of the iterations plus the fix-up launch (~8) and the
+    // partials of the split tail tiles (~6 per two of them a CTA)
     const int64_t dp = (tiles + G - 1) / G * num_kb;
-    const int64_t sk = (iters + G - 1) / G + 12;
-    return 10 * sk < 9 * dp ? G : 0;
+    const int64_t tail = tiles % G;
+    const int64_t sk = (iters + G - 1) / G + 8 + 6 * ((2 * tail + G - 1) / G);
+    return sk < dp ? G : 0;
 }
 
 template <int TYPE, int MODE>
@@ -1433,6 +1527,11 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
+        // the kernel's register split hands out exactly what a block of
+        // MAX_REGS-register threads holds: any other launch count is refused
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+        if (fa.numRegs != MAX_REGS) return cudaErrorInvalidConfiguration;
         cudaEvent_t before = g_ev_before, after = g_ev_after;
         g_ev_before = g_ev_after = nullptr;
         if (before && (e = cudaEventRecord(before, stream)) != cudaSuccess) return e;
@@ -1583,7 +1682,7 @@ cudaError_t launch_dense_tc(const void *a, const float *b, float *dst, const Out
     }
     if (e != cudaSuccess || p.ctas == 0) return e;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    launch_fixup<false>(partial, p, tiles, stream);
+    launch_fixup<false>(partial, p, tiles / p.ctas * p.ctas, tiles % p.ctas, stream);
     e = cudaGetLastError();
     if (e == cudaSuccess) ++g_kernel_launches;
     return e;
@@ -1730,7 +1829,7 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
         return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess || p.ctas == 0) return e;
-    launch_fixup<true>(p.partial, p, max_grid, stream);
+    launch_fixup<true>(p.partial, p, 0, max_grid, stream);
     e = cudaGetLastError();
     if (e == cudaSuccess) ++g_kernel_launches;
     return e;

@@ -2,7 +2,7 @@
 // of dst out, enqueued as one call.
 //
 // For a single slice with N wide enough, the work is pipelined over up to four
-// chunks of dst columns n (boundaries on 96-column tile edges): src0 and the
+// chunks of dst columns n (boundaries on tile edges): src0 and the
 // first chunk's src1 columns go in, then each product runs while the next
 // chunk's src1 columns are copied in and the previous chunk of dst is copied
 // out.  The copies run on a library-owned copy stream (one per
@@ -124,8 +124,8 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
 
     const int64_t M = ne_a[0], K = ne_a[1], N = ne_b[0];
     const bool single = ne_b[2] * ne_b[3] == 1 && ne_a[2] * ne_a[3] == 1;
-    // chunks of at least two 96-column tiles, boundaries on tile edges
-    const int64_t tiles_n = (N + 95) / 96;
+    // chunks of at least two tiles, boundaries on tile edges
+    const int64_t tiles_n = (N + oop::kTcTileN - 1) / oop::kTcTileN;
     const int chunks = single && K > 0 ? static_cast<int>(std::min<int64_t>(kMaxChunks, tiles_n / 2)) : 1;
     if (chunks < 2) {
         rc = rc_of(cudaMemcpyAsync(a_dev, a_host, L.a_bytes, cudaMemcpyHostToDevice, st));
@@ -147,7 +147,7 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
     cudaEvent_t *ev = pp->ev;
     int64_t nb[kMaxChunks + 1];                                // chunk c: columns [nb[c], nb[c+1])
     for (int c = 0; c <= chunks; ++c)
-        nb[c] = std::min<int64_t>(N, (tiles_n * c + chunks - 1) / chunks * 96);
+        nb[c] = std::min<int64_t>(N, (tiles_n * c + chunks - 1) / chunks * oop::kTcTileN);
     cudaError_t e = cudaEventRecord(ev[0], st);                // after the caller's prior work
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[0], 0);
     if (e == cudaSuccess) e = cudaMemcpyAsync(a_dev, a_host, L.a_bytes, cudaMemcpyHostToDevice, cs);

@@ -12,6 +12,8 @@
 
 namespace oop {
 
+// dst columns (src1 rows n) per tile of the tensor-core kernel
+constexpr int kTcTileN = 128;
 
 // Elements and bytes per block of a src0 type (1 and the element size for the
 // plain types), -1 for an unknown type.  Host and device.

@@ -88,6 +88,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// Per-warpgroup register budget (every thread of the warpgroup executes the
+// same call): give back down to N registers a thread, or wait for registers
+// given back by other warpgroups until N are available.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // True in exactly one active lane of the warp (all lanes must call it).
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred = 0;
@@ -160,85 +172,111 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::tf32, one CTA.  A occupies
-// lanes 0..M-1 (row i in lane i) and 8 consecutive 32-bit columns (k).
-__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+// One 32-k block of the 3xTF32 product, A from tensor memory (lanes 0..127 =
+// rows, one 32-bit column per k), B from shared memory (descriptors; +2 is
+// 32 bytes along the swizzled k row, i.e. 8 tf32), issued as MMAs of 8 k:
+//   for kk = 0..3:  d2 (+)= a_lo * b_hi ; d2 += a_hi * b_lo ; d1 (+)= a_hi * b_hi
+// (d2 restarted at kk = 0 when `fresh2`, d1 when `fresh1`).  The "one" form
+// puts every product into d, restarted: the eight small cross terms first,
+// while d is still ~2^-11 of its final size, then the four big terms.
+// The blocks are issued by the lanes with `lead` set (one lane) while every
+// lane tests one barrier phase (`tbar` / `tpar`, per lane) in the same
+// statement; they return that lane's outcome.  The test sits after the eighth
+// MMA (the fifth of the bf16 block): by then the issuing lane is held by the
+// tensor core's full queue anyway, and the test's ~100-cycle latency passes
+// while the last MMAs are issued, instead of stalling the warp before them.
+#define OOP_MMA_PROLOGUE                                                        \
+    "{\n\t.reg .pred pl, pok, p1, p2, pt;\n\t"                                  \
+    ".reg .b32 a0, a1, a2, a3, l0, l1, l2, l3, okr;\n\t"                         \
+    ".reg .b64 h0, h1, h2, h3, o0, o1, o2, o3;\n\t"                             \
+    "setp.ne.b32 pl, %1, 0;\n\t"                                                \
+    "setp.eq.b32 pt, 0, 0;\n\t"                                                 \
+    "mov.b32 a0, %4;\n\tadd.u32 a1, %4, 8;\n\tadd.u32 a2, %4, 16;\n\tadd.u32 a3, %4, 24;\n\t" \
+    "mov.b32 l0, %5;\n\tadd.u32 l1, %5, 8;\n\tadd.u32 l2, %5, 16;\n\tadd.u32 l3, %5, 24;\n\t" \
+    "mov.b64 h0, %6;\n\tadd.u64 h1, %6, 2;\n\tadd.u64 h2, %6, 4;\n\tadd.u64 h3, %6, 6;\n\t" \
+    "mov.b64 o0, %7;\n\tadd.u64 o1, %7, 2;\n\tadd.u64 o2, %7, 4;\n\tadd.u64 o3, %7, 6;\n\t"
+#define OOP_MMA_TEST "mbarrier.test_wait.parity.shared::cta.b64 pok, [%2], %3;\n\t"
+#define OOP_MMA_EPILOGUE "selp.u32 %0, 1, 0, pok;\n\t}"
+#define OOP_MMA(d, a, b, acc) "@pl tcgen05.mma.cta_group::1.kind::tf32 [" d "], [" a "], " b ", %8, " acc ";\n\t"
+
+// the 3xTF32 block (d1 = %9, d2 = %10, fresh1 = %11, fresh2 = %12)
+__device__ __forceinline__ uint32_t mma_block_3xtf32_test(uint32_t d1, uint32_t d2, uint32_t ahi,
+                                                          uint32_t alo, uint64_t bhi, uint64_t blo,
+                                                          uint32_t idesc, uint32_t fresh1,
+                                                          uint32_t fresh2, uint32_t lead,
+                                                          uint64_t *tbar, uint32_t tpar) {
+    uint32_t ok;
+    asm volatile(OOP_MMA_PROLOGUE
+                 "setp.eq.b32 p1, %11, 0;\n\t"
+                 "setp.eq.b32 p2, %12, 0;\n\t"
+                 OOP_MMA("%10", "l0", "h0", "p2") OOP_MMA("%10", "a0", "o0", "pt")
+                 OOP_MMA("%9", "a0", "h0", "p1") OOP_MMA("%10", "l1", "h1", "pt")
+                 OOP_MMA("%10", "a1", "o1", "pt") OOP_MMA("%9", "a1", "h1", "pt")
+                 OOP_MMA("%10", "l2", "h2", "pt") OOP_MMA("%10", "a2", "o2", "pt")
+                 OOP_MMA_TEST
+                 OOP_MMA("%9", "a2", "h2", "pt") OOP_MMA("%10", "l3", "h3", "pt")
+                 OOP_MMA("%10", "a3", "o3", "pt") OOP_MMA("%9", "a3", "h3", "pt")
+                 OOP_MMA_EPILOGUE
+                 : "=r"(ok)
+                 : "r"(lead), "r"(smem_u32(tbar)), "r"(tpar), "r"(ahi), "r"(alo), "l"(bhi),
+                   "l"(blo), "r"(idesc), "r"(d1), "r"(d2), "r"(fresh1), "r"(fresh2)
+                 : "memory");
+    return ok;
 }
 
-// One 32-k block of the 3xTF32 product, A from tensor memory, in one
-// statement (the accumulate predicates are set once, not per MMA):
-//   for kk = 0..3 (8 k each; A columns +8*kk, B descriptors +2*kk, i.e. 32
-//   bytes along the swizzled k row):
-//     d2 (+)= a_lo * b_hi ; d2 += a_hi * b_lo ; d1 (+)= a_hi * b_hi
-// d2 starts fresh at kk = 0 when `fresh2`, d1 when `fresh1`.
-__device__ __forceinline__ void mma_block_3xtf32(uint32_t d1, uint32_t d2, uint32_t ahi,
-                                                 uint32_t alo, uint64_t bhi, uint64_t blo,
-                                                 uint32_t idesc, uint32_t fresh1,
-                                                 uint32_t fresh2) {
-    asm volatile(
-        "{\n\t.reg .pred p1, p2, pt;\n\t"
-        "setp.eq.b32 p1, %7, 0;\n\t"
-        "setp.eq.b32 p2, %8, 0;\n\t"
-        "setp.eq.b32 pt, 0, 0;\n\t"
-        ".reg .b32 a0, a1, a2, a3, l0, l1, l2, l3;\n\t"
-        ".reg .b64 h0, h1, h2, h3, o0, o1, o2, o3;\n\t"
-        "mov.b32 a0, %2;\n\tadd.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
-        "mov.b32 l0, %3;\n\tadd.u32 l1, %3, 8;\n\tadd.u32 l2, %3, 16;\n\tadd.u32 l3, %3, 24;\n\t"
-        "mov.b64 h0, %4;\n\tadd.u64 h1, %4, 2;\n\tadd.u64 h2, %4, 4;\n\tadd.u64 h3, %4, 6;\n\t"
-        "mov.b64 o0, %5;\n\tadd.u64 o1, %5, 2;\n\tadd.u64 o2, %5, 4;\n\tadd.u64 o3, %5, 6;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [l0], h0, %6, p2;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [a0], o0, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a0], h0, %6, p1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [l1], h1, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [a1], o1, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a1], h1, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [l2], h2, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [a2], o2, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a2], h2, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [l3], h3, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%1], [a3], o3, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a3], h3, %6, pt;\n\t}" ::"r"(d1),
-        "r"(d2), "r"(ahi), "r"(alo), "l"(bhi), "l"(blo), "r"(idesc), "r"(fresh1), "r"(fresh2)
-        : "memory");
+// the "one" form (d = %9)
+__device__ __forceinline__ uint32_t mma_block_3xtf32_one_test(uint32_t d, uint32_t ahi,
+                                                              uint32_t alo, uint64_t bhi,
+                                                              uint64_t blo, uint32_t idesc,
+                                                              uint32_t lead, uint64_t *tbar,
+                                                              uint32_t tpar) {
+    uint32_t ok;
+    asm volatile(OOP_MMA_PROLOGUE
+                 "setp.ne.b32 p1, 0, 0;\n\t"
+                 OOP_MMA("%9", "l0", "h0", "p1") OOP_MMA("%9", "a0", "o0", "pt")
+                 OOP_MMA("%9", "l1", "h1", "pt") OOP_MMA("%9", "a1", "o1", "pt")
+                 OOP_MMA("%9", "l2", "h2", "pt") OOP_MMA("%9", "a2", "o2", "pt")
+                 OOP_MMA("%9", "l3", "h3", "pt") OOP_MMA("%9", "a3", "o3", "pt")
+                 OOP_MMA_TEST
+                 OOP_MMA("%9", "a0", "h0", "pt") OOP_MMA("%9", "a1", "h1", "pt")
+                 OOP_MMA("%9", "a2", "h2", "pt") OOP_MMA("%9", "a3", "h3", "pt")
+                 OOP_MMA_EPILOGUE
+                 : "=r"(ok)
+                 : "r"(lead), "r"(smem_u32(tbar)), "r"(tpar), "r"(ahi), "r"(alo), "l"(bhi),
+                   "l"(blo), "r"(idesc), "r"(d)
+                 : "memory");
+    return ok;
 }
 
-// The same 32-k block with every product in d (restarted): the eight small
-// cross terms first, while d is still ~2^-11 of its final size, then the four
-// big terms.
-__device__ __forceinline__ void mma_block_3xtf32_one(uint32_t d, uint32_t ahi, uint32_t alo,
-                                                     uint64_t bhi, uint64_t blo, uint32_t idesc) {
-    asm volatile(
-        "{\n\t.reg .pred pf, pt;\n\t"
-        "setp.ne.b32 pf, 0, 0;\n\t"
-        "setp.eq.b32 pt, 0, 0;\n\t"
-        ".reg .b32 a0, a1, a2, a3, l0, l1, l2, l3;\n\t"
-        ".reg .b64 h0, h1, h2, h3, o0, o1, o2, o3;\n\t"
-        "mov.b32 a0, %1;\n\tadd.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
-        "mov.b32 l0, %2;\n\tadd.u32 l1, %2, 8;\n\tadd.u32 l2, %2, 16;\n\tadd.u32 l3, %2, 24;\n\t"
-        "mov.b64 h0, %3;\n\tadd.u64 h1, %3, 2;\n\tadd.u64 h2, %3, 4;\n\tadd.u64 h3, %3, 6;\n\t"
-        "mov.b64 o0, %4;\n\tadd.u64 o1, %4, 2;\n\tadd.u64 o2, %4, 4;\n\tadd.u64 o3, %4, 6;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [l0], h0, %5, pf;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a0], o0, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [l1], h1, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a1], o1, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [l2], h2, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a2], o2, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [l3], h3, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a3], o3, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a0], h0, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a1], h1, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a2], h2, %5, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [a3], h3, %5, pt;\n\t}" ::"r"(d),
-        "r"(ahi), "r"(alo), "l"(bhi), "l"(blo), "r"(idesc)
-        : "memory");
+// A block whose a_lo is zero (bf16 / f16 src0): the cross term a_hi * b_lo
+// into dx (restarted at its first MMA when `freshx`), then a_hi * b_hi into
+// d1 (restarted when `fresh1`).  (dx = %9, d1 = %10, freshx = %11, fresh1 = %12)
+__device__ __forceinline__ uint32_t mma_block_1xlo_test(uint32_t dx, uint32_t d1, uint32_t ahi,
+                                                        uint64_t bhi, uint64_t blo, uint32_t idesc,
+                                                        uint32_t freshx, uint32_t fresh1,
+                                                        uint32_t lead, uint64_t *tbar,
+                                                        uint32_t tpar) {
+    uint32_t ok;
+    asm volatile(OOP_MMA_PROLOGUE
+                 "setp.eq.b32 p1, %11, 0;\n\t"
+                 "setp.eq.b32 p2, %12, 0;\n\t"
+                 OOP_MMA("%9", "a0", "o0", "p1") OOP_MMA("%9", "a1", "o1", "pt")
+                 OOP_MMA("%9", "a2", "o2", "pt") OOP_MMA("%9", "a3", "o3", "pt")
+                 OOP_MMA("%10", "a0", "h0", "p2")
+                 OOP_MMA_TEST
+                 OOP_MMA("%10", "a1", "h1", "pt") OOP_MMA("%10", "a2", "h2", "pt")
+                 OOP_MMA("%10", "a3", "h3", "pt")
+                 OOP_MMA_EPILOGUE
+                 : "=r"(ok)
+                 : "r"(lead), "r"(smem_u32(tbar)), "r"(tpar), "r"(ahi), "r"(ahi), "l"(bhi),
+                   "l"(blo), "r"(idesc), "r"(dx), "r"(d1), "r"(freshx), "r"(fresh1)
+                 : "memory");
+    return ok;
 }
+#undef OOP_MMA
+#undef OOP_MMA_EPILOGUE
+#undef OOP_MMA_TEST
+#undef OOP_MMA_PROLOGUE
 
 // Arrive (once) on `bar` when every tcgen05 op this thread issued completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {

@@ -1,6 +1,6 @@
 """GPU parity of the tensor-core OUT_PROD under both tile schedules.
 
-Data-parallel: one 128 (m) x 96 (n) dst tile per CTA.  Stream-K: one CTA per SM
+Data-parallel: one 128 (m) x 128 (n) dst tile per CTA.  Stream-K: one CTA per SM
 shares the (tile, k-block) iterations, tiles split between CTAs are summed by
 a fix-up kernel.  Both must meet |gpu - exact| <= 2e-6 * sum_k |a*b| against
 the oracle, stream-K must repeat bit for bit, and the call must enqueue the
@@ -103,11 +103,13 @@ def test_below_minimum_workspace_rejected(op):
 
 
 def test_auto_schedule_choice(op):
-    """The automatic schedule takes stream-K exactly when the data-parallel
-    waves (tiles / SMs, rounded up, times the k-blocks per tile) would cost
-    more than 10/9 of an even share of the iterations plus twelve k-blocks;
-    shown on the dense shapes and on small problems: a wave that is mostly
-    empty with long K (stream-K), short K (data-parallel), a single tile."""
+    """The automatic schedule takes stream-K exactly when an even share of
+    the iterations, plus the fix-up launch (~8 k-blocks) and the partials of
+    the split tail tiles (~6 per two of them a CTA), costs fewer k-block times
+    than the data-parallel waves (tiles / SMs, rounded up, times the k-blocks
+    per tile), and never when the tiles fill whole waves; shown on the dense
+    shapes and on small problems: a wave that is mostly empty with long K
+    (stream-K), short K (data-parallel), a single tile."""
     import torch
     sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 160)
     for m, k, n in ((5120, 5120, 1024), (5120, 17408, 1024), (1536, 1536, 1024),
@@ -118,12 +120,13 @@ def test_auto_schedule_choice(op):
         op.out_prod(ta, tb, a_type=Q8, ne_a=(m, k, 1, 1), path=op.PATH_TCGEN05)
         got = op.last_launch_count()
         torch.cuda.synchronize()
-        tiles = -(-m // 128) * -(-n // 96)
+        tiles = -(-m // 128) * -(-n // 128)
         nkb = -(-k // 32)
         g = min(sms, tiles * nkb)
         dp = -(-tiles // g) * nkb
-        sk = -(-(tiles * nkb) // g) + 12
-        want_sk = 10 * sk < 9 * dp
+        tail = tiles % g
+        sk = -(-(tiles * nkb) // g) + 8 + 6 * -(-(2 * tail) // g)
+        want_sk = tail != 0 and sk < dp
         assert got == (3 if want_sk else 2), (m, k, n, got)
 
 

@@ -33,22 +33,27 @@ def dense(t, m, k, n, slices=1):
 
 
 # (a_type, ne_a, ne_b), measured data-parallel / stream-K in microseconds
+# (128 x 128 tiles; stream-K runs the full waves as whole tiles first)
 DATA_PARALLEL_WINS = [
-    ((F32, (128, 512, 4, 1), (128, 512, 16, 1)), (31.7, 35.5)),    # grouped heads, 1 sequence
-    ((F32, (128, 512, 4, 2), (128, 512, 16, 2)), (33.9, 41.8)),    # grouped heads, 2 sequences
-    (dense(Q8, 1536, 1536, 1024), (57.1, 64.5)),
+    ((F32, (128, 512, 4, 1), (128, 512, 16, 1)), (36.9, 42.0)),    # grouped heads, 1 sequence
+    ((F32, (128, 512, 4, 2), (128, 512, 16, 2)), (38.9, 46.1)),    # grouped heads, 2 sequences
+    (dense(Q8, 1536, 1536, 1024), (65.5, 76.8)),
 ]
 STREAM_K_WINS = [
-    (dense(Q8, 512, 4096, 256), (110.9, 39.6)),
-    (dense(F32, 256, 2048, 96), (61.5, 37.7)),
-    (dense(F32, 512, 1024, 192), (42.0, 31.1)),
-    (dense(F32, 128, 8192, 128), (189.5, 42.0)),
-    (dense(Q8, 1024, 2048, 512), (66.6, 49.2)),
-    (dense(F32, 256, 512, 128), (29.3, 26.6)),
-    (dense(Q8, 1024, 1024, 256), (44.1, 35.8)),
-    (dense(F32, 128, 2048, 96), (62.3, 36.4)),
-    (dense(Q8, 2048, 2048, 384), (66.9, 54.3)),
-    (dense(F32, 640, 4096, 192), (105.2, 37.9)),
+    (dense(Q8, 512, 4096, 256), (135.1, 44.0)),
+    (dense(F32, 256, 2048, 96), (79.9, 46.0)),
+    (dense(F32, 512, 1024, 192), (49.2, 39.9)),
+    (dense(F32, 128, 8192, 128), (253.9, 62.4)),
+    (dense(Q8, 1024, 2048, 512), (77.8, 54.3)),
+    (dense(F32, 256, 512, 128), (38.8, 33.9)),
+    (dense(Q8, 1024, 1024, 256), (51.2, 42.0)),
+    (dense(F32, 128, 2048, 96), (79.9, 44.0)),
+    (dense(Q8, 2048, 2048, 384), (79.8, 62.5)),
+    (dense(F32, 640, 4096, 192), (135.2, 48.1)),
+    (dense(Q8, 1536, 1536, 256), (63.5, 48.1)),
+    (dense(Q8, 5120, 5120, 1024), (475.1, 369.7)),
+    (dense(Q8, 5120, 17408, 1024), (1520.6, 1152.0)),
+    (dense(Q8, 17408, 5120, 1024), (1231.9, 1160.2)),
 ]
 
 
@@ -68,11 +73,24 @@ def test_schedule_stream_k_where_it_measured_faster(shape, times):
 
 
 @pytest.mark.parametrize("m,k", [(5120, 5120), (5120, 17408), (17408, 5120)])
-def test_headline_shapes_stay_data_parallel(m, k):
-    """440 / 440 / 1496 tiles: 2.9, 2.9 and 9.8 waves, the last ones 89%, 89%
-    and 84% full, so stream-K's partials and fix-up buy nothing."""
+def test_headline_shapes_take_stream_k(m, k):
+    """320 / 320 / 1088 tiles: 2.1, 2.1 and 7.2 waves, the last ones 11%,
+    11% and 16% full; stream-K runs the full waves as whole tiles and splits
+    only the 16 / 16 / 24 tail tiles."""
     for t in (Q8, Q4):
-        assert plan(*dense(t, m, k, 1024))["kernel"] == op.KERNEL_TC_DATA_PARALLEL
+        p = plan(*dense(t, m, k, 1024))
+        assert p["kernel"] == op.KERNEL_TC_STREAM_K and p["ctas"] == SMS
+
+
+def test_whole_waves_stay_data_parallel():
+    # 304 tiles = two full waves: nothing to split, even when stream-K is forced
+    shape = dense(Q8, 128 * 38, 4096, 1024)
+    assert plan(*shape)["kernel"] == op.KERNEL_TC_DATA_PARALLEL
+    try:
+        op.oop_debug_set_tc_schedule(2)
+        assert plan(*shape)["kernel"] == op.KERNEL_TC_DATA_PARALLEL
+    finally:
+        op.oop_debug_set_tc_schedule(0)
 
 
 def test_minimum_workspace_and_forced_schedules():

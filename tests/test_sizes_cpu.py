@@ -6,7 +6,7 @@ import pytest
 import ggml_out_prod_gb300 as op
 
 F32, Q8, Q4, BF16 = 0, 8, 2, 30
-SLOT = 2 * 128 * 96 * 4            # two 128 x 96 fp32 partial tiles per stream-K CTA
+SLOT = 2 * 128 * 128 * 4           # two 128 x 128 fp32 partial tiles per stream-K CTA
 
 SHAPES = [
     (F32, (256, 512, 1, 1), (8, 512, 1, 1)),
