@@ -99,6 +99,10 @@ constexpr int MAX_REGS = 96;                // at launch: 5 warps x 32 lanes x 9
 // launched with, and each sub-partition's share fits its register file.
 constexpr int WARP_PROD0 = 4, WARP_FOLD0 = 12;
 constexpr int REGS_CTRL = 48, REGS_PROD = 72, REGS_FOLD = 144;
+// a producer that addresses row groups (its rows' offsets differ) gets 8 more
+constexpr int REGS_PROD_RG = 80, REGS_FOLD_RG = 136;
+static_assert(4 * REGS_CTRL + 8 * REGS_PROD_RG + 8 * REGS_FOLD_RG == THREADS / 32 * MAX_REGS,
+              "register split must equal the launch allocation");
 static_assert(4 * REGS_CTRL + 8 * REGS_PROD + 8 * REGS_FOLD == THREADS / 32 * MAX_REGS,
               "register split must equal the launch allocation");
 static_assert(REGS_CTRL + 2 * REGS_PROD + 2 * REGS_FOLD <= 512, "registers per sub-partition");
@@ -127,16 +131,34 @@ constexpr int MAX_RSTAGES = 4;
 // such offset needs.
 constexpr int gcd16(int x) { return (x % 16 == 0) ? 16 : (x % 8 == 0) ? 8 : (x % 4 == 0) ? 4 : (x % 2 == 0) ? 2 : 1; }
 
+// A staged row's bytes: at least `need`, a multiple of 16, and such that
+// `rows_per_box` of them fill a multiple of 128 bytes (where each box lands).
+constexpr int staged_row_bytes(int need, int rows_per_box) {
+    int b = (need + 15) / 16 * 16;
+    while ((b * rows_per_box) % 128 != 0) b += 16;
+    return b;
+}
+
 template <int TYPE>
 struct RawA {
     using F = QFormat<TYPE>;
     static constexpr bool PLAIN = F::QK == 1;
     static constexpr int BLOCK = F::BYTES;
-    // the bytes of a row one m-tile needs, and how far past a 16-byte boundary
-    // they may start
+    // Rows whose byte length is not a multiple of 16 cannot be a 2-D TMA
+    // map's rows; groups of 16 / gcd(row bytes, 16) of them are, at most RG
+    // (RG * BYTES is a multiple of 16), so the map's rows are groups of rows
+    // and one k-block takes one box per member of a group, box r holding
+    // member r of each group.  Used by the block types of the cooperative
+    // decode (the q8_0 / q4_0 path stages single rows).
+    static constexpr int RG = (PLAIN || TYPE == OOP_TYPE_Q8_0 || TYPE == OOP_TYPE_Q4_0)
+                                  ? 1 : 16 / gcd16(F::BYTES);
+    static_assert(BK % RG == 0, "a k-block holds whole row groups");
+    // the bytes of a row one m-tile needs, and how far past a 16-byte
+    // boundary they may start: a multiple of the tile's span in one row, or,
+    // for the row-group types, of one block (where a group's member rows start)
     static constexpr int SPAN = PLAIN ? BM * F::BYTES : (F::QK == 32 ? 4 * F::BYTES : F::BYTES);
-    static constexpr int MAXOFF = PLAIN ? 0 : 16 - gcd16(F::QK == 32 ? 4 * F::BYTES : F::BYTES);
-    static constexpr int ROW_BYTES = (SPAN + MAXOFF + 15) / 16 * 16;   // bytes per staged k row
+    static constexpr int MAXOFF = PLAIN ? 0 : 16 - gcd16(RG > 1 ? F::BYTES : SPAN);
+    static constexpr int ROW_BYTES = staged_row_bytes(SPAN + MAXOFF, BK / RG);  // per staged k row
     static constexpr int BOX_X = PLAIN ? BM : ROW_BYTES;              // in map elements
     static constexpr int SLOT = (ROW_BYTES * BK + 1023) / 1024 * 1024;
     static constexpr int RSTAGES = TYPE == OOP_TYPE_F32 ? 2 : 4;   // f32: room for 3 B stages
@@ -451,8 +473,17 @@ __device__ __forceinline__ void global_half(const uint8_t *row0, int64_t stride,
 // r of the m-tile.  Lane l of the warp owns row r = 32 * (warp % 4) + l, so a
 // warp covers one quantisation block: its 16 scales are read once (lane j
 // reads k row j) and passed around with shuffles.
-template <int TYPE>
-__device__ __forceinline__ void staged_half(const uint8_t *slot, int r, int off0, int lane,
+// Where k row j (0 .. BK-1) of a k-block sits in its staged slot: rows in
+// order, or (row groups of AG) member j % AG's box holds the block's rows
+// j % AG, j % AG + AG, ...
+template <int AG>
+__device__ __forceinline__ int slot_row(int j) {
+    if constexpr (AG <= 1) return j;
+    else return (j % AG) * (BK / AG) + j / AG;
+}
+
+template <int TYPE, int AG>
+__device__ __forceinline__ void staged_half(const uint8_t *slot, int r, uint32_t off0, int lane,
                                             int kh, float (&x)[KH], int mt) {
     using Raw = RawA<TYPE>;
     const uint8_t *rows = slot + kh * KH * Raw::ROW_BYTES;
@@ -472,12 +503,22 @@ __device__ __forceinline__ void staged_half(const uint8_t *slot, int r, int off0
         // once; each lane then takes its row's pair by shuffle and adds its
         // own code: one fused multiply-add, the same rounding as decode().
         const int quad = r >> 5;
-        const uint8_t *base = rows + off0 + (QFormat<TYPE>::QK == 32 ? quad * Raw::BLOCK : 0);
+        const int bofs = QFormat<TYPE>::QK == 32 ? quad * Raw::BLOCK : 0;
+        // this warp's bytes of its j-th k row of the block
+        auto row_at = [&](int j) -> const uint8_t * {
+            if constexpr (AG > 1) {
+                const int jb = kh * KH + j;                 // row in the k-block
+                return slot + slot_row<AG>(jb) * Raw::ROW_BYTES +
+                       ((off0 >> (4 * (jb % AG))) & 15u) + bofs;
+            } else {
+                return rows + j * Raw::ROW_BYTES + off0 + bofs;
+            }
+        };
         const int h = mt & 1;                               // K-quants: half of the super-block
         const int jr = lane & (KH - 1), hl = lane >> 4;
         float sc, of;
         uint32_t xw = 0;                                    // q5_0 / q5_1: the fifth bits
-        block_scale<TYPE>(base + jr * Raw::ROW_BYTES, quad, h, hl, sc, of, xw);
+        block_scale<TYPE>(row_at(jr), quad, h, hl, sc, of, xw);
         constexpr bool HALVES = TYPE == OOP_TYPE_Q6_K || TYPE == OOP_TYPE_Q2_K ||
                                 TYPE == OOP_TYPE_Q3_K;      // a scale per 16 elements
         const int src_add = HALVES ? 16 * (lane >> 4) : 0;
@@ -488,7 +529,7 @@ __device__ __forceinline__ void staged_half(const uint8_t *slot, int r, int off0
             uint32_t xj = 0;
             if constexpr (TYPE == OOP_TYPE_Q5_0 || TYPE == OOP_TYPE_Q5_1)
                 xj = __shfl_sync(0xffffffffu, xw, j);
-            const int q = block_code<TYPE>(base + j * Raw::ROW_BYTES, quad, h, lane, xj);
+            const int q = block_code<TYPE>(row_at(j), quad, h, lane, xj);
             x[j] = fmaf(sj, static_cast<float>(q), oj);
         }
     } else {
@@ -528,13 +569,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int TYPE, bool TMA_A, int MODE>
+// AG: how src0 is staged -- 0 loaded from global memory by the producer, 1
+// one TMA row per src0 row, >1 TMA rows of AG src0 rows (RawA::RG).
+template <int TYPE, int AG, int MODE>
 __global__ void __maxnreg__(MAX_REGS)
     tc_out_prod_kernel(const __grid_constant__ CUtensorMap map_bhi,
                        const __grid_constant__ CUtensorMap map_blo,
                        const __grid_constant__ CUtensorMap map_a, const TcParams p) {
     constexpr bool GROUPED = MODE == kModeGrouped;
+    constexpr bool TMA_A = AG > 0;
     using Raw = RawA<TYPE>;
+    static_assert(AG <= 1 || (Raw::RG % AG == 0 && (BK / AG) * Raw::ROW_BYTES % 128 == 0),
+                  "row groups: a divisor of RG, each box 128-byte aligned");
     constexpr bool HAS_ALO = !is_tf32_exact<TYPE>();   // bf16 / f16 values are TF32 values
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -662,12 +708,21 @@ __global__ void __maxnreg__(MAX_REGS)
                     ptx::mbar_arrive_expect_tx(
                         &bars->rfull[r],
                         static_cast<uint32_t>(2 * B_IMG + (TMA_A ? Raw::ROW_BYTES * BK : 0)));
-                    if constexpr (TMA_A) {
+                    if constexpr (AG == 1) {
                         const int box_x = elementwise_type<TYPE>()
                                               ? t.mt * BM
                                               : static_cast<int>(raw_tile_byte0<TYPE>(t.mt) & ~15);
                         ptx::tma_load_2d(ring + r * Raw::SLOT, &map_a, &bars->rfull[r], box_x,
                                          static_cast<int>(t.a_row0 + static_cast<int64_t>(w.kb) * BK));
+                    } else if constexpr (AG > 1) {
+                        // box g: member g of the block's BK / AG row groups
+                        const int64_t byte0 = raw_tile_byte0<TYPE>(t.mt);
+                        const int grp = static_cast<int>((t.a_row0 + static_cast<int64_t>(w.kb) * BK) / AG);
+#pragma unroll
+                        for (int gm = 0; gm < AG; ++gm)
+                            ptx::tma_load_2d(ring + r * Raw::SLOT + gm * (BK / AG) * Raw::ROW_BYTES,
+                                             &map_a, &bars->rfull[r],
+                                             static_cast<int>((gm * p.a_row_bytes + byte0) & ~15), grp);
                     }
                     if constexpr (GROUPED) {
                         ptx::tma_load_2d(st, &map_bhi, &bars->rfull[r], w.kb * BK,
@@ -798,7 +853,7 @@ __global__ void __maxnreg__(MAX_REGS)
         }                                                  // warps 2 and 3: idle
     } else if (warp < WARP_FOLD0) {
         // ---------------- src0 producer ----------------
-        ptx::setmaxnreg_dec<REGS_PROD>();
+        ptx::setmaxnreg_dec<(AG > 1 ? REGS_PROD_RG : REGS_PROD)>();
         const int quad = warp & 3;                       // TMEM lanes 32*quad ..
         const int kh = (warp - WARP_PROD0) >> 2;         // k rows KH*kh .. of each block
         const int r = 32 * quad + lane;                  // row of the m-tile
@@ -829,11 +884,19 @@ __global__ void __maxnreg__(MAX_REGS)
                 early_r = ptx::mbar_test_wait(&bars->rfull[rn.slot], rn.phase);
             }
             if constexpr (TMA_A) {
-                int off0 = 0;
-                if constexpr (!elementwise_type<TYPE>())
-                    off0 = static_cast<int>(raw_tile_byte0<TYPE>(t.mt) & 15);
+                // how far past its box's 16-byte start the tile's bytes begin:
+                // one offset, or (row groups) one per member, 4 bits each
+                uint32_t off0 = 0;
+                if constexpr (AG > 1) {
+                    const int64_t byte0 = raw_tile_byte0<TYPE>(t.mt);
+#pragma unroll
+                    for (int gm = 0; gm < AG; ++gm)
+                        off0 |= static_cast<uint32_t>((gm * p.a_row_bytes + byte0) & 15) << (4 * gm);
+                } else if constexpr (!elementwise_type<TYPE>()) {
+                    off0 = static_cast<uint32_t>(raw_tile_byte0<TYPE>(t.mt) & 15);
+                }
                 __syncwarp();
-                staged_half<TYPE>(ring + rs * Raw::SLOT, r, off0, lane, kh, x, t.mt);
+                staged_half<TYPE, AG>(ring + rs * Raw::SLOT, r, off0, lane, kh, x, t.mt);
                 // rows past M and k past K read whatever the box holds there
                 if (!(__all_sync(0xffffffffu, mok) && kfull)) {
 #pragma unroll
@@ -906,7 +969,7 @@ __global__ void __maxnreg__(MAX_REGS)
         }
     } else {
         // ---------------- fold + epilogue ----------------
-        ptx::setmaxnreg_inc<REGS_FOLD>();
+        ptx::setmaxnreg_inc<(AG > 1 ? REGS_FOLD_RG : REGS_FOLD)>();
         const int quad = warp & 3;                          // TMEM lanes 32*quad ..
         const int half = (warp - WARP_FOLD0) >> 2;          // columns FOLD_COLS*half ..
         const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
@@ -1446,13 +1509,15 @@ bool make_b_map_2d(CUtensorMap *map, void *base, int64_t Kp, int64_t rows) {
 
 // raw src0: rows of `a_row_bytes` (all slices stacked), boxes of 32 rows.
 template <int TYPE>
-bool make_a_map(CUtensorMap *map, const void *base, const OutProdShape &s) {
+bool make_a_map(CUtensorMap *map, const void *base, const OutProdShape &s, int rg) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const int64_t rows = s.K * s.ne02 * s.ne03;
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(RawA<TYPE>::BOX_X), BK};
+    // map rows: groups of rg src0 rows (rg = 1: the rows themselves)
+    const int64_t rows = s.K * s.ne02 * s.ne03 / rg;
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(RawA<TYPE>::BOX_X),
+                         static_cast<cuuint32_t>(BK / rg)};
     cuuint32_t estr[2] = {1, 1};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.a_row_bytes)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.a_row_bytes * rg)};
     if constexpr (elementwise_type<TYPE>()) {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.M), static_cast<cuuint64_t>(rows)};
         const CUtensorMapDataType dt = TYPE == OOP_TYPE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -1462,7 +1527,7 @@ bool make_a_map(CUtensorMap *map, const void *base, const OutProdShape &s) {
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     } else {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.a_row_bytes),
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.a_row_bytes * rg),
                               static_cast<cuuint64_t>(rows)};
         return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1512,12 +1577,24 @@ template <int TYPE, int MODE>
 cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap &mhi,
                          const CUtensorMap &mlo, const TcParams &p, dim3 grid,
                          cudaStream_t stream) {
-    // TMA needs a 16-byte aligned base and row stride, and rows that fit int32.
-    const bool tma_a = reinterpret_cast<uintptr_t>(a) % 16 == 0 && s.a_row_bytes % 16 == 0 &&
-                       s.K * s.ne02 * s.ne03 < (1LL << 31);
+    // TMA needs a 16-byte aligned base and row stride, and rows that fit
+    // int32.  Rows of another length are staged in groups of RawA::RG (whose
+    // length always is a multiple of 16) when every k-block starts a group:
+    // K a multiple of RG, a src0 slice per tile (not the segmented mode).
+    constexpr int RG = RawA<TYPE>::RG;
+    const bool tma_ok = reinterpret_cast<uintptr_t>(a) % 16 == 0 &&
+                        s.K * s.ne02 * s.ne03 < (1LL << 31);
+    // the smallest group whose bytes are a multiple of 16 (1: the rows are)
+    int group = 1;
+    while ((s.a_row_bytes * group) % 16 != 0) group *= 2;
+    int ag = 0;
+    if (tma_ok && group == 1)
+        ag = 1;
+    else if (tma_ok && MODE != kModeSegmented && RG % group == 0 && s.K % group == 0)
+        ag = group;
     CUtensorMap ma;
-    if (tma_a) {
-        if (!make_a_map<TYPE>(&ma, a, s)) return cudaErrorInvalidValue;
+    if (ag > 0) {
+        if (!make_a_map<TYPE>(&ma, a, s, ag)) return cudaErrorInvalidValue;
     } else {
         ma = mhi;   // unused by the kernel
     }
@@ -1554,8 +1631,16 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
         if (after && (e = cudaEventRecord(after, stream)) != cudaSuccess) return e;
         return cudaSuccess;
     };
-    return tma_a ? run(tc_out_prod_kernel<TYPE, true, MODE>)
-                 : run(tc_out_prod_kernel<TYPE, false, MODE>);
+    if (ag == 1) return run(tc_out_prod_kernel<TYPE, 1, MODE>);
+    if constexpr (MODE != kModeSegmented) {
+        if constexpr (RG >= 2)
+            if (ag == 2) return run(tc_out_prod_kernel<TYPE, 2, MODE>);
+        if constexpr (RG >= 4)
+            if (ag == 4) return run(tc_out_prod_kernel<TYPE, 4, MODE>);
+        if constexpr (RG >= 8)
+            if (ag == 8) return run(tc_out_prod_kernel<TYPE, 8, MODE>);
+    }
+    return run(tc_out_prod_kernel<TYPE, 0, MODE>);
 }
 
 size_t split_bytes(const OutProdShape &s) {

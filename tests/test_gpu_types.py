@@ -87,6 +87,48 @@ def test_every_type_unaligned_rows(op, orc, tid):
                           f"type {tid} M {M} path {p}")
 
 
+# the block types whose rows can miss TMA's 16-byte rule, and the largest
+# row group they can need (16 / gcd(block bytes, 16))
+ROW_GROUPS = {synth.TYPE_Q4_1: 4, synth.TYPE_Q5_0: 8, synth.TYPE_Q5_1: 2, synth.TYPE_Q2_K: 4,
+              synth.TYPE_Q3_K: 8, synth.TYPE_Q6_K: 8}
+
+
+def _group(row_bytes):
+    g = 1
+    while row_bytes * g % 16:
+        g *= 2
+    return g
+
+
+@pytest.mark.parametrize("tid", sorted(ROW_GROUPS))
+def test_row_groups_stage_unaligned_rows(op, orc, tid):
+    """Rows whose byte length is not a multiple of 16, with K a multiple of
+    the row group: the TMA stages groups of 2, 4 or 8 rows (one box per
+    member, the smallest group whose bytes are a multiple of 16) and the
+    producer finds each row at its member's offset.  Every group size the
+    type can need, ragged n and k tails, two slices of src1."""
+    qk = synth.BLOCK[tid][0]
+    seen = set()
+    for blocks in range(1, 17):
+        M = blocks * qk
+        if M % 128 and qk == 256:
+            continue
+        g = _group(synth.row_bytes(tid, M))
+        if g == 1 or g in seen:
+            continue
+        seen.add(g)
+        assert ROW_GROUPS[tid] % g == 0
+        K = 88
+        ne_a, ne_b = (M, K, 1, 1), (150, K, 2, 1)
+        a = _src0(tid, ne_a, 179 + tid + g)
+        b = synth.make_b(ne_b, 180, std=1e3, outliers=True)
+        ref = orc.out_prod(a, tid, b, ne_a, ne_b)
+        assert_parity(_run(op, a, tid, b, ne_a, op.PATH_TCGEN05), ref["f64"], ref["abs"],
+                      f"type {tid} M {M} K {K} groups of {g}")
+    want = {2, 4, 8} if ROW_GROUPS[tid] == 8 else {2, 4} if ROW_GROUPS[tid] == 4 else {2}
+    assert seen == want, seen
+
+
 @pytest.mark.parametrize("tid", ALL)
 def test_identity_gradient_reproduces_decoded_src0(op, orc, tid):
     """b = identity: the CUDA-core kernel returns the decoded src0 exactly as
