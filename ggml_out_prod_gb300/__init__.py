@@ -613,8 +613,8 @@ def last_launch_count() -> int:
 def out_prod_host(a_host, b_host, a_type=None, ne_a=None, out=None, device_buffer=None,
                   stream=None):
     """OUT_PROD from host tensors through the C ABI's host entry: the copies
-    in, the product and the copy of dst out are enqueued by one call (two
-    column chunks pipelined when the shape allows), then the stream is
+    in, the product and the copy of dst out are enqueued by one call (up to
+    four chunks of k pipelined when the shape allows), then the stream is
     synchronised.  a_host / b_host: CPU tensors (pinned memory makes the
     copies asynchronous); ``out``: a CPU float32 tensor of dst's shape
     (allocated pinned when None); ``device_buffer``: a CUDA uint8 tensor of at

@@ -1,16 +1,17 @@
 // host.cu -- OUT_PROD from host buffers: the copies in, the product, the copy
 // of dst out, enqueued as one call.
 //
-// For a single slice with N wide enough, the work is pipelined over up to four
-// chunks of dst columns n (boundaries on tile edges): src0 and the
-// first chunk's src1 columns go in, then each product runs while the next
-// chunk's src1 columns are copied in and the previous chunk of dst is copied
-// out.  The copies run on a library-owned copy stream (one per
-// device, created on first use) ordered against the caller's stream by
-// events; everything is enqueued before the call returns and the caller's
-// stream is made to wait for the last copy, so synchronising that stream is
-// enough.  Otherwise the copies and the product run in order on the caller's
-// stream.
+// For a single slice long enough in k (tensor-core shapes), the work is
+// pipelined over up to four chunks of k: chunk c's src0 rows and src1 rows --
+// contiguous host memory, so every copy runs at full speed -- go in while
+// chunk c-1's product runs; chunk 0's product writes dst, the others a
+// dst-sized partial each; then dst = the chunk results summed in k order with
+// a Kahan compensation, in four pieces, each copied out while the next is
+// summed.  The copies run on a library-owned copy stream (one per device,
+// created on first use) ordered against the caller's stream by events;
+// everything is enqueued before the call returns and the caller's stream is
+// made to wait for the last copy, so synchronising that stream is enough.
+// Otherwise the copies and the product run in order on the caller's stream.
 #include <algorithm>
 #include <mutex>
 
@@ -20,8 +21,10 @@ namespace oop {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxChunks = 4;
-constexpr int kEvents = 2 * kMaxChunks + 2;
+constexpr int kMaxChunks = 4;                 // chunks of k
+constexpr int kPieces = 4;                    // pieces of dst summed and copied out
+constexpr int64_t kMinChunkK = 256;           // k rows per chunk, at least
+constexpr int kEvents = kMaxChunks + kPieces + 2;
 
 struct HostPipe {
     cudaStream_t copy = nullptr;
@@ -35,7 +38,8 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct HostLayout {
     size_t a_bytes, b_bytes, dst_bytes;
-    size_t off_a, off_b, off_dst, off_ws, ws_bytes, total;
+    size_t off_a, off_b, off_dst, off_ws, ws_bytes, off_parts, part_bytes, total;
+    int chunks;                               // chunks of k (1: no pipelining)
 };
 
 int64_t src0_bytes(int a_type, const int64_t ne_a[4]) {
@@ -43,6 +47,15 @@ int64_t src0_bytes(int a_type, const int64_t ne_a[4]) {
     const int qk = type_block_elems(a_type);
     if (qk < 0) return -1;
     return ne_a[0] / qk * type_block_bytes(a_type) * rows;
+}
+
+// Chunks of k for the pipelined form: one slice, a tensor-core shape (the
+// skinny-N kernel, f32 with N <= 32, is one memory-bound pass), at least
+// kMinChunkK rows a chunk.
+int host_k_chunks(int a_type, const int64_t ne_a[4], const int64_t ne_b[4]) {
+    const bool single = ne_b[2] * ne_b[3] == 1 && ne_a[2] * ne_a[3] == 1;
+    if (!single || (a_type == OOP_TYPE_F32 && ne_b[0] <= 32)) return 1;
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxChunks, ne_a[1] / kMinChunkK)));
 }
 
 bool plan_host(int a_type, const int64_t ne_a[4], const int64_t ne_b[4], HostLayout *L) {
@@ -62,8 +75,31 @@ bool plan_host(int a_type, const int64_t ne_a[4], const int64_t ne_b[4], HostLay
     L->off_ws = o;
     L->ws_bytes = ws;
     o += align256(ws);
+    L->chunks = host_k_chunks(a_type, ne_a, ne_b);
+    L->off_parts = o;
+    L->part_bytes = align256(L->dst_bytes);
+    o += static_cast<size_t>(L->chunks - 1) * L->part_bytes;   // chunks 1.. write partials
     L->total = o;
     return true;
+}
+
+// dst[i] = dst[i] + parts[0][i] + ... + parts[nparts-1][i], added in that
+// (k) order with a Kahan compensation, for i in [i0, i1).
+__global__ void __launch_bounds__(256) chunk_sum_kernel(float *__restrict__ dst,
+                                                        const float *__restrict__ parts,
+                                                        int64_t part_stride, int nparts,
+                                                        int64_t i0, int64_t i1) {
+    for (int64_t i = i0 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < i1;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float s = dst[i], c = 0.f;
+        for (int q = 0; q < nparts; ++q) {
+            const float y = parts[q * part_stride + i] - c;
+            const float t = s + y;
+            c = (t - s) - y;
+            s = t;
+        }
+        dst[i] = s - c;
+    }
 }
 
 int pipe_for_device(HostPipe **out) {
@@ -123,10 +159,7 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     const int64_t M = ne_a[0], K = ne_a[1], N = ne_b[0];
-    const bool single = ne_b[2] * ne_b[3] == 1 && ne_a[2] * ne_a[3] == 1;
-    // chunks of at least two tiles, boundaries on tile edges
-    const int64_t tiles_n = (N + oop::kTcTileN - 1) / oop::kTcTileN;
-    const int chunks = single && K > 0 ? static_cast<int>(std::min<int64_t>(kMaxChunks, tiles_n / 2)) : 1;
+    const int chunks = K > 0 ? L.chunks : 1;
     if (chunks < 2) {
         rc = rc_of(cudaMemcpyAsync(a_dev, a_host, L.a_bytes, cudaMemcpyHostToDevice, st));
         if (rc == OOP_OK)
@@ -145,43 +178,64 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
     if (rc != OOP_OK) return rc;
     cudaStream_t cs = pp->copy;
     cudaEvent_t *ev = pp->ev;
-    int64_t nb[kMaxChunks + 1];                                // chunk c: columns [nb[c], nb[c+1])
-    for (int c = 0; c <= chunks; ++c)
-        nb[c] = std::min<int64_t>(N, (tiles_n * c + chunks - 1) / chunks * oop::kTcTileN);
+    // chunk c: src0 / src1 rows [kb[c], kb[c+1]), boundaries on 32-row k-blocks
+    const int64_t step = ((K + chunks - 1) / chunks + 31) / 32 * 32;
+    int64_t kb[kMaxChunks + 1];
+    for (int c = 0; c <= chunks; ++c) kb[c] = std::min<int64_t>(K, c * step);
+    const size_t a_row = L.a_bytes / static_cast<size_t>(K);          // src0 bytes per k row
+    const uint8_t *a_h = static_cast<const uint8_t *>(a_host);
+    uint8_t *a_d = static_cast<uint8_t *>(a_dev);
+    float *parts = reinterpret_cast<float *>(dbuf + L.off_parts);
+    const int64_t part_stride = static_cast<int64_t>(L.part_bytes / 4);
     cudaError_t e = cudaEventRecord(ev[0], st);                // after the caller's prior work
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[0], 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(a_dev, a_host, L.a_bytes, cudaMemcpyHostToDevice, cs);
-    // copy stream: src1 chunk c in, then (once product c is done) dst chunk c out
-    // compute (caller's) stream: product c once its src1 chunk is in
+    // copy stream: chunk c's src0 rows and src1 rows in
+    for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+        const int64_t k0 = kb[c], kc = kb[c + 1] - kb[c];
+        e = cudaMemcpyAsync(a_d + k0 * a_row, a_h + k0 * a_row, static_cast<size_t>(kc) * a_row,
+                            cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(b_dev + k0 * N, b_host + k0 * N, static_cast<size_t>(kc * N) * 4,
+                                cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[1 + c], cs);
+    }
+    // compute (caller's) stream: product c once its rows are in; chunk 0 into
+    // dst, chunk c > 0 into partial c - 1
     int launches = 0;
     for (int c = 0; c < chunks && e == cudaSuccess && rc == OOP_OK; ++c) {
-        const int64_t nc = nb[c + 1] - nb[c];
-        float *bc = b_dev + K * nb[c];                          // [K][nc] contiguous
-        e = cudaMemcpy2DAsync(bc, nc * 4, b_host + nb[c], N * 4, nc * 4, K,
-                              cudaMemcpyHostToDevice, cs);
-        if (e == cudaSuccess) e = cudaEventRecord(ev[1 + c], cs);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[1 + c], 0);
+        e = cudaStreamWaitEvent(st, ev[1 + c], 0);
         if (e != cudaSuccess) break;
-        const int64_t ne_bc[4] = {nc, K, 1, 1};
-        const int64_t ne_dc[4] = {M, nc, 1, 1};
-        rc = oop_out_prod(a_dev, a_type, bc, dst_dev + nb[c] * M, ne_a, ne_bc, ne_dc, ws,
+        const int64_t k0 = kb[c], kc = kb[c + 1] - kb[c];
+        const int64_t ne_ac[4] = {M, kc, 1, 1}, ne_bc[4] = {N, kc, 1, 1};
+        float *out = c == 0 ? dst_dev : parts + (c - 1) * part_stride;
+        rc = oop_out_prod(a_d + k0 * a_row, a_type, b_dev + k0 * N, out, ne_ac, ne_bc, ne_dst, ws,
                           L.ws_bytes, stream);
-        if (rc != OOP_OK) break;
         launches += g_kernel_launches;
-        e = cudaEventRecord(ev[1 + kMaxChunks + c], st);
     }
-    for (int c = 0; c < chunks && e == cudaSuccess && rc == OOP_OK; ++c) {
-        e = cudaStreamWaitEvent(cs, ev[1 + kMaxChunks + c], 0);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(dst_host + nb[c] * M, dst_dev + nb[c] * M,
-                                static_cast<size_t>((nb[c + 1] - nb[c]) * M) * 4,
+    // dst = the chunks summed in k order, a piece at a time, each piece copied
+    // out (copy stream) while the next one is summed
+    const int64_t elems = M * N;
+    for (int q = 0; q < kPieces && e == cudaSuccess && rc == OOP_OK; ++q) {
+        const int64_t i0 = elems * q / kPieces, i1 = elems * (q + 1) / kPieces;
+        if (i1 > i0) {
+            const int64_t blocks = std::min<int64_t>(4 * 152, (i1 - i0 + 255) / 256);
+            chunk_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+                dst_dev, parts, part_stride, chunks - 1, i0, i1);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) break;
+            ++launches;
+        }
+        e = cudaEventRecord(ev[1 + kMaxChunks + q], st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[1 + kMaxChunks + q], 0);
+        if (e == cudaSuccess && i1 > i0)
+            e = cudaMemcpyAsync(dst_host + i0, dst_dev + i0, static_cast<size_t>(i1 - i0) * 4,
                                 cudaMemcpyDeviceToHost, cs);
     }
     // Whatever failed, the caller's stream is made to wait for every copy
     // already enqueued on the copy stream, so that synchronising it still
     // means no copy touches the caller's buffers any more.
-    cudaError_t j = cudaEventRecord(ev[2 * kMaxChunks + 1], cs);
-    if (j == cudaSuccess) j = cudaStreamWaitEvent(st, ev[2 * kMaxChunks + 1], 0);
+    cudaError_t j = cudaEventRecord(ev[kMaxChunks + kPieces + 1], cs);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(st, ev[kMaxChunks + kPieces + 1], 0);
     g_kernel_launches = rc == OOP_OK && e == cudaSuccess ? launches : 0;
     if (rc != OOP_OK) return rc;
     if (e == cudaSuccess) e = j;

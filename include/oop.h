@@ -261,11 +261,14 @@ int oop_lora_backward(const float *x, const float *h, const float *dz, const flo
  *
  * device_buffer: device memory of at least
  * oop_out_prod_host_buffer_size(...) bytes (0 for an invalid shape),
- * 256-byte aligned, holding the device copies of a, b and dst and the
- * workspace.  For a single slice wide enough, the call pipelines up to four
- * column chunks of dst: a chunk's b columns are copied in while the previous
- * chunk is computed, and a chunk of dst is copied out while the next one is
- * computed; those copies run on a copy stream the library creates once per
+ * 256-byte aligned, holding the device copies of a, b and dst, the
+ * workspace and, for the pipelined form, one dst-sized partial per k chunk
+ * after the first.  For a single slice with K >= 512 (and not the skinny-N
+ * f32 case) the call pipelines up to four chunks of k: a chunk's a and b rows
+ * (contiguous host memory) are copied in while the previous chunk's product
+ * runs; the chunk results are then summed in k order with a Kahan
+ * compensation, in four pieces of dst, each copied out while the next one is
+ * summed.  Those copies run on a copy stream the library creates once per
  * device and are ordered against `stream` by events, so the call returns with
  * `stream` waiting for its last copy.  Calls on one device are enqueued one
  * at a time (a library lock).  Errors: as oop_out_prod; OOP_ERR_WORKSPACE for
