@@ -1347,17 +1347,17 @@ __global__ void __launch_bounds__(1024) mmid_route_kernel(const int32_t *__restr
     }
 }
 
-// Sorted slots j (kSplitSlots per CTA): g[rows[j]][0..R) -> ghi, glo [j][Kp],
-// TF32 split, zero padding for r in [R, Kp).  Rows past the routed total are
-// left alone: the tile kernel never stores the columns they feed.
+// Sorted slots j, one warp each (kSplitSlots per CTA): g[rows[j]][0..R) ->
+// ghi, glo [j][Kp], TF32 split, zero padding for r in [R, Kp).  With `vec`
+// (R a multiple of 4, 16-byte aligned rows) each lane moves four words at a
+// time.  Rows past the routed total are left alone: the tile kernel never
+// stores the columns they feed.
 constexpr int kSplitSlots = 8;
 
-__global__ void __launch_bounds__(256) mmid_gsplit_kernel(const float *__restrict__ g,
-                                                          const int *__restrict__ rows,
-                                                          const int *__restrict__ count, int E,
-                                                          uint32_t *__restrict__ ghi,
-                                                          uint32_t *__restrict__ glo, int64_t R,
-                                                          int64_t Kp) {
+__global__ void __launch_bounds__(32 * kSplitSlots) mmid_gsplit_kernel(
+    const float *__restrict__ g, const int *__restrict__ rows, const int *__restrict__ count,
+    int E, uint32_t *__restrict__ ghi, uint32_t *__restrict__ glo, int64_t R, int64_t Kp,
+    bool vec) {
     __shared__ int total;
     if (threadIdx.x == 0) {
         int t = 0;
@@ -1365,15 +1365,31 @@ __global__ void __launch_bounds__(256) mmid_gsplit_kernel(const float *__restric
         total = t;
     }
     __syncthreads();
-    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kSplitSlots;
-    const int64_t j1 = min(static_cast<int64_t>(total), j0 + kSplitSlots);
-    for (int64_t j = j0; j < j1; ++j) {
+    const int lane = threadIdx.x & 31;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kSplitSlots + (threadIdx.x >> 5);
+    if (j < total) {
         const float *src = g + static_cast<int64_t>(rows[j]) * R;
-        for (int64_t r = threadIdx.x; r < Kp; r += blockDim.x) {
-            uint32_t h = 0, l = 0;
-            if (r < R) ptx::split_tf32(__ldg(src + r), h, l);
-            ghi[j * Kp + r] = h;
-            glo[j * Kp + r] = l;
+        uint32_t *dh = ghi + j * Kp, *dl = glo + j * Kp;
+        if (vec) {
+            for (int64_t r = 4 * lane; r < Kp; r += 128) {
+                uint4 h = make_uint4(0, 0, 0, 0), l = make_uint4(0, 0, 0, 0);
+                if (r < R) {
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(src + r));
+                    ptx::split_tf32(v.x, h.x, l.x);
+                    ptx::split_tf32(v.y, h.y, l.y);
+                    ptx::split_tf32(v.z, h.z, l.z);
+                    ptx::split_tf32(v.w, h.w, l.w);
+                }
+                *reinterpret_cast<uint4 *>(dh + r) = h;
+                *reinterpret_cast<uint4 *>(dl + r) = l;
+            }
+        } else {
+            for (int64_t r = lane; r < Kp; r += 32) {
+                uint32_t h = 0, l = 0;
+                if (r < R) ptx::split_tf32(__ldg(src + r), h, l);
+                dh[r] = h;
+                dl[r] = l;
+            }
         }
     }
     ptx::griddep_launch_dependents();   // as in bsplit_kernel
@@ -1835,9 +1851,12 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++g_kernel_launches;
-    mmid_gsplit_kernel<<<static_cast<unsigned>((t.nslot + kSplitSlots - 1) / kSplitSlots), 256, 0,
-                         stream>>>(
-        g, rw.rows, rw.count, static_cast<int>(s.E), ghi, glo, s.N, t.Kp);
+    const bool vec = s.N % 4 == 0 && reinterpret_cast<uintptr_t>(g) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(ghi) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(glo) % 16 == 0 && t.Kp % 4 == 0;
+    mmid_gsplit_kernel<<<static_cast<unsigned>((t.nslot + kSplitSlots - 1) / kSplitSlots),
+                         32 * kSplitSlots, 0, stream>>>(
+        g, rw.rows, rw.count, static_cast<int>(s.E), ghi, glo, s.N, t.Kp, vec);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++g_kernel_launches;
