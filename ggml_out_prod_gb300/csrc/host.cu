@@ -178,10 +178,15 @@ int oop_out_prod_host(const void *a_host, int a_type, const float *b_host, float
     if (rc != OOP_OK) return rc;
     cudaStream_t cs = pp->copy;
     cudaEvent_t *ev = pp->ev;
-    // chunk c: src0 / src1 rows [kb[c], kb[c+1]), boundaries on 32-row k-blocks
-    const int64_t step = ((K + chunks - 1) / chunks + 31) / 32 * 32;
+    // chunk c: src0 / src1 rows [kb[c], kb[c+1]), boundaries on 32-row k-blocks;
+    // the first chunk's copy is the one nothing overlaps, so it is half the
+    // others (the copies then stay ahead of the products: ~200 GB/s of pinned
+    // copies bring rows faster than the product consumes them)
     int64_t kb[kMaxChunks + 1];
-    for (int c = 0; c <= chunks; ++c) kb[c] = std::min<int64_t>(K, c * step);
+    kb[0] = 0;
+    kb[1] = std::min<int64_t>(K, (K / (2 * chunks - 1) + 31) / 32 * 32);
+    const int64_t step = ((K - kb[1] + chunks - 2) / (chunks - 1) + 31) / 32 * 32;
+    for (int c = 2; c <= chunks; ++c) kb[c] = std::min<int64_t>(K, kb[1] + (c - 1) * step);
     const size_t a_row = L.a_bytes / static_cast<size_t>(K);          // src0 bytes per k row
     const uint8_t *a_h = static_cast<const uint8_t *>(a_host);
     uint8_t *a_d = static_cast<uint8_t *>(a_dev);

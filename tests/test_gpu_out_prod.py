@@ -256,11 +256,11 @@ def test_host_checks_reject(op):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("a_type,ne_a,ne_b", [
-    (Q8, (640, 1000, 1, 1), (300, 1000, 1, 1)),     # pipelined: three k chunks (352, 352, 296)
+    (Q8, (640, 1000, 1, 1), (300, 1000, 1, 1)),     # pipelined: three k chunks (224, 416, 360)
     (Q8, (256, 4096, 1, 1), (100, 4096, 1, 1)),     # long K, narrow: four k chunks
     (F32, (200, 300, 2, 1), (70, 300, 4, 3)),       # several slices: one pass
     (F32, (256, 512, 1, 1), (8, 512, 1, 1)),        # skinny-N: one pass
-    (Q4, (384, 700, 1, 1), (200, 700, 1, 1)),       # two k chunks (352, 348)
+    (Q4, (384, 700, 1, 1), (200, 700, 1, 1)),       # two k chunks (256, 444)
     (F32, (300, 300, 1, 1), (50, 300, 1, 1)),       # K < 512: one pass
 ])
 def test_host_entry_matches_oracle(op, orc, a_type, ne_a, ne_b):
