@@ -1048,6 +1048,15 @@ __global__ void __maxnreg__(MAX_REGS)
             // plain: column jc of the tile is dst row nt * BN + jc
             float *dcol = (GROUPED ? p.dst : p.dst + t.slice * p.N * p.M) + m;
             if constexpr (!GROUPED) dcol += static_cast<int64_t>(t.nt) * BN * p.M;
+            // grouped: the dst rows of the thread's 64 columns, read once per
+            // tile, lane l holding those of columns col0 + l and col0 + 32 + l,
+            // handed out by shuffles as the columns are stored
+            int rows_lo = 0, rows_hi = 0;
+            if constexpr (GROUPED) {
+                const int c = static_cast<int>(col0) + lane;
+                if (c < tile_cols) rows_lo = p.grp_rows[t.brow0 + c];
+                if (c + 32 < tile_cols) rows_hi = p.grp_rows[t.brow0 + c + 32];
+            }
             // S - C first: the compensations' registers are free for the loads
 #pragma unroll
             for (int j = 0; j < FOLD_COLS; j += 2) {
@@ -1062,6 +1071,23 @@ __global__ void __maxnreg__(MAX_REGS)
                 uint32_t dv[16];
                 __syncwarp();                               // converged for tcgen05.ld
                 ptx::tmem_ld16_wait(tmem + lane_off + COL_D2 + col, dv);
+                if constexpr (GROUPED) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int rel = pc * 16 + j;        // the thread's column
+                        const int drow =
+                            __shfl_sync(0xffffffffu, rel < 32 ? rows_lo : rows_hi, rel & 31);
+                        const float v = sreg[rel] + (has_d2 ? __uint_as_float(dv[j]) : 0.f);
+                        const int jc = col + j;
+                        if (m < p.M) {
+                            if (part)
+                                part[jc * BM] = v;
+                            else if (jc < tile_cols)
+                                dcol[static_cast<int64_t>(drow) * p.M] = v;
+                        }
+                    }
+                    continue;
+                }
                 if (m >= p.M) continue;
 #pragma unroll
                 for (int j = 0; j < 16; j += 2) {
@@ -1072,14 +1098,10 @@ __global__ void __maxnreg__(MAX_REGS)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int jc = col + j + e;         // column in the tile
-                        if (part) {
+                        if (part)
                             part[jc * BM] = v[e];
-                        } else if (jc < tile_cols) {
-                            if constexpr (GROUPED)
-                                dcol[static_cast<int64_t>(p.grp_rows[t.brow0 + jc]) * p.M] = v[e];
-                            else
-                                dcol[static_cast<int64_t>(jc) * p.M] = v[e];
-                        }
+                        else if (jc < tile_cols)
+                            dcol[static_cast<int64_t>(jc) * p.M] = v[e];
                     }
                 }
             }
