@@ -192,20 +192,38 @@ struct Bars {
 template <int TYPE>
 constexpr bool elementwise_type() { return is_plain_type<TYPE>(); }
 
-// Shared memory: [B stages][raw src0 ring][barriers], from a 1024-byte
-// boundary (the 128-byte swizzle's); as many B stages as fit, up to six.
-template <int TYPE>
+// The tile kernel's modes: plain OUT_PROD (every head x batch slice in one
+// grid), grouped (MUL_MAT_ID_BACK: slices are experts, src1 rows are the
+// routed slots sorted by expert, dst rows scattered back to slots) and
+// segmented (MUL_MAT_ID's expert-weight gradient: slice e reduces over its
+// own k range).  A compile-time parameter, so that the plain and grouped
+// kernels carry none of the segmented mode's state.
+constexpr int kModePlain = 0, kModeGrouped = 1, kModeSegmented = 2;
+
+// The grouped and segmented modes' tiles are short in k, so their epilogue
+// is a large share of a tile: there the result columns go through shared
+// memory (EPI_COLS columns of each half of the tile at a time) to bulk
+// copies, and the fold moves on while the copies drain.
+constexpr int EPI_COLS = 32;
+constexpr int EPI_BYTES = 2 * EPI_COLS * BM * 4;
+template <int MODE>
+constexpr bool staged_epilogue() { return MODE != kModePlain; }
+
+// Shared memory: [B stages][raw src0 ring][epilogue staging][barriers], from a
+// 1024-byte boundary (the 128-byte swizzle's); as many B stages as fit, up to six.
+template <int TYPE, int MODE>
 constexpr size_t smem_fixed_bytes() {
-    return RawA<TYPE>::RSTAGES * RawA<TYPE>::SLOT + sizeof(Bars) + 1024;
+    return RawA<TYPE>::RSTAGES * RawA<TYPE>::SLOT + (staged_epilogue<MODE>() ? EPI_BYTES : 0) +
+           sizeof(Bars) + 1024;
 }
-template <int TYPE>
+template <int TYPE, int MODE>
 constexpr int b_stages() {
-    return static_cast<int>(std::min<size_t>(MAX_BSTAGES,
-                                             (SMEM_LIMIT - smem_fixed_bytes<TYPE>()) / STAGE_BYTES));
+    return static_cast<int>(std::min<size_t>(
+        MAX_BSTAGES, (SMEM_LIMIT - smem_fixed_bytes<TYPE, MODE>()) / STAGE_BYTES));
 }
-template <int TYPE>
+template <int TYPE, int MODE>
 constexpr size_t smem_bytes() {
-    return b_stages<TYPE>() * STAGE_BYTES + smem_fixed_bytes<TYPE>();
+    return b_stages<TYPE, MODE>() * STAGE_BYTES + smem_fixed_bytes<TYPE, MODE>();
 }
 
 struct TcParams {
@@ -236,6 +254,9 @@ struct TcParams {
     // column seg_off[e] of the split src1 (one slice, every segment)
     const int *seg_off;
     const int *seg_nkb;
+    // grouped / segmented: results leave through bulk copies (M % 4 == 0 and
+    // dst 16-byte aligned, so every column's rows start on 16 bytes)
+    int bulk_epi;
 };
 
 // First iteration of stream-K CTA c, and the CTA that owns iteration x.
@@ -248,14 +269,6 @@ __host__ __device__ __forceinline__ int64_t sk_owner(int64_t iters, int ctas, in
 
 // Where tile t sits: m-tile, n-tile, dst slice, its valid src1 rows, and the
 // first src0 row (k = 0) of the src0 slice it reads.
-// The tile kernel's modes: plain OUT_PROD (every head x batch slice in one
-// grid), grouped (MUL_MAT_ID_BACK: slices are experts, src1 rows are the
-// routed slots sorted by expert, dst rows scattered back to slots) and
-// segmented (MUL_MAT_ID's expert-weight gradient: slice e reduces over its
-// own k range).  A compile-time parameter, so that the plain and grouped
-// kernels carry none of the segmented mode's state.
-constexpr int kModePlain = 0, kModeGrouped = 1, kModeSegmented = 2;
-
 struct Tile {
     int mt, nt;
     int64_t slice, ncols, brow0, a_row0;
@@ -585,9 +598,10 @@ __global__ void __maxnreg__(MAX_REGS)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    constexpr int BST = b_stages<TYPE>();
+    constexpr int BST = b_stages<TYPE, MODE>();
     uint8_t *ring = smem + BST * STAGE_BYTES;
-    Bars *bars = reinterpret_cast<Bars *>(ring + Raw::RSTAGES * Raw::SLOT);
+    uint8_t *epi = ring + Raw::RSTAGES * Raw::SLOT;
+    Bars *bars = reinterpret_cast<Bars *>(epi + (staged_epilogue<MODE>() ? EPI_BYTES : 0));
     volatile int *abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5;
@@ -1065,6 +1079,55 @@ __global__ void __maxnreg__(MAX_REGS)
                 sreg[j] -= c0;
                 sreg[j + 1] -= c1;
             }
+            if constexpr (staged_epilogue<MODE>()) {
+                if (p.bulk_epi && !part) {
+                    // Each half's four warps write EPI_COLS columns x 128 rows
+                    // to its staging area (a column's rows contiguous, as in
+                    // dst); lane l of the half's first warp then copies column
+                    // l of them to its dst row.  Rows past M are staged but not
+                    // copied.
+                    float *stg = reinterpret_cast<float *>(epi) + half * EPI_COLS * BM;
+                    const bool issuer = quad == 0;
+                    const int64_t mrow0 = static_cast<int64_t>(t.mt) * BM;
+                    const uint32_t bytes =
+                        static_cast<uint32_t>(std::min<int64_t>(BM, p.M - mrow0)) * 4;
+                    float *dbase = p.dst + mrow0;
+                    if constexpr (!GROUPED)
+                        dbase += t.slice * p.N * p.M + static_cast<int64_t>(t.nt) * BN * p.M;
+#pragma unroll
+                    for (int rd = 0; rd < FOLD_COLS / EPI_COLS; ++rd) {
+                        if (issuer) ptx::bulk_wait_read();   // the last copies left the staging
+                        ptx::named_bar_sync(1 + half, 128);
+#pragma unroll
+                        for (int pp = 0; pp < EPI_COLS / 16; ++pp) {
+                            const int pc = rd * (EPI_COLS / 16) + pp;
+                            uint32_t dv[16];
+                            __syncwarp();                   // converged for tcgen05.ld
+                            ptx::tmem_ld16_wait(tmem + lane_off + COL_D2 + col0 + pc * 16, dv);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                stg[(pp * 16 + j) * BM + row] =
+                                    sreg[pc * 16 + j] + (has_d2 ? __uint_as_float(dv[j]) : 0.f);
+                        }
+                        if (rd == FOLD_COLS / EPI_COLS - 1) {
+                            // D2 is read: the next segment's cross terms may start
+                            ptx::tc_fence_before();
+                            ptx::mbar_arrive(&bars->d2free);
+                        }
+                        ptx::fence_async_shared();
+                        ptx::named_bar_sync(1 + half, 128);
+                        if (issuer) {
+                            const int jc = static_cast<int>(col0) + rd * EPI_COLS + lane;
+                            if (jc < tile_cols) {
+                                const int64_t drow = GROUPED ? (rd == 0 ? rows_lo : rows_hi) : jc;
+                                ptx::bulk_store(dbase + drow * p.M, stg + lane * BM, bytes);
+                            }
+                            ptx::bulk_commit();
+                        }
+                    }
+                    continue;
+                }
+            }
 #pragma unroll
             for (int pc = 0; pc < FOLD_COLS / 16; ++pc) {
                 const int col = static_cast<int>(col0) + pc * 16;
@@ -1110,6 +1173,10 @@ __global__ void __maxnreg__(MAX_REGS)
         }
     }
 
+    // the bulk copies of the last epilogue complete before the CTA exits
+    if constexpr (staged_epilogue<MODE>()) {
+        if (warp >= WARP_FOLD0 && (warp & 3) == 0) ptx::bulk_wait();
+    }
     if (timed_out) record_status(p.status, OOP_ERR_DEVICE_TIMEOUT);
     ptx::tc_fence_before();
     __syncthreads();
@@ -1636,7 +1703,7 @@ cudaError_t launch_typed(const void *a, const OutProdShape &s, const CUtensorMap
     } else {
         ma = mhi;   // unused by the kernel
     }
-    constexpr size_t smem = smem_bytes<TYPE>();
+    constexpr size_t smem = smem_bytes<TYPE, MODE>();
     static_assert(smem <= 232448, "shared memory budget");
     auto run = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1922,6 +1989,7 @@ cudaError_t launch_mmid_tc(const void *W, const int32_t *ids, const float *g, fl
     p.grp_rows = rw.rows;
     p.grp_tiles = rw.tiles;
     p.grp_ntiles = rw.ntiles;
+    p.bulk_epi = p.M % 4 == 0 && reinterpret_cast<uintptr_t>(dx) % 16 == 0;
     // The work list is only known on the device, so the schedule is chosen
     // here: stream-K (one CTA per SM walking the (tile, k-block) iterations
     // the device computes from the list's length) unless data-parallel is
@@ -2065,6 +2133,7 @@ cudaError_t launch_mmid_wgrad(const float *x, const int32_t *ids, const float *d
     p.ntiles = static_cast<int>(ntiles);
     p.seg_off = seg_off;
     p.seg_nkb = seg_nkb;
+    p.bulk_epi = p.M % 4 == 0 && reinterpret_cast<uintptr_t>(dW) % 16 == 0;
     // persistent by default: one CTA per SM takes whole tiles round-robin, so
     // the short tiles (a few k-blocks each) flow into one another; the test
     // hook's data-parallel schedule gives each tile its own CTA

@@ -53,6 +53,25 @@ def test_small_whole(op, orc, wt, path):
     assert_parity(got, ref["f64"], ref["abs"], f"mmid small {wt} {path}")
 
 
+@pytest.mark.parametrize("sched", ["auto", "stream_k"])
+def test_rows_off_16_bytes(op, orc, sched):
+    """dx rows of 302 floats: a row start is not always 16-byte aligned, so
+    the tile kernel stores the results itself instead of copying them out in
+    bulk; the stream-K schedule's shared tiles go through partial sums."""
+    K, N, E, n_used, T = 302, 72, 5, 2, 90
+    W = synth.normal(63, K * N * E, std=0.02).reshape(E, N, K)
+    ids = synth.routing_ids(64, E, n_used, T)
+    g = synth.normal(65, N * n_used * T).reshape(T, n_used, N)
+    ref = orc.mul_mat_id_back(W, synth.TYPE_F32, ids, g, (K, N, E))
+    op.set_tc_schedule(op.SCHEDULE_AUTO if sched == "auto" else op.SCHEDULE_STREAM_K)
+    try:
+        got = _run(op, W, synth.TYPE_F32, ids, g, op.PATH_TCGEN05).cpu().numpy()
+    finally:
+        op.set_tc_schedule(op.SCHEDULE_AUTO)
+    assert op.device_status() == 0
+    assert_parity(got, ref["f64"], ref["abs"], f"mmid rows off 16 bytes {sched}")
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("wt", [synth.TYPE_F32, synth.TYPE_BF16])
 def test_moe_full_sampled(op, orc, wt, path):
@@ -178,6 +197,7 @@ def _wgrad(op, x, ids, dy, E):
     (256, 96, 6, 3, 3, 70),      # one x row per slot, ragged segments
     (300, 136, 5, 4, 1, 33),     # one x row per token, ragged m and n tiles
     (128, 50, 40, 2, 2, 9),      # most experts with no slot: their gradient is zero
+    (302, 72, 3, 2, 2, 20),      # dW rows of 302 floats: stored directly, not in bulk
 ])
 def test_expert_weight_grad_whole(op, orc, K, N, E, n_used, n_x, T):
     """Both schedules: persistent (the default) and one CTA per tile."""
