@@ -202,10 +202,10 @@ constexpr int kModePlain = 0, kModeGrouped = 1, kModeSegmented = 2;
 
 // The grouped and segmented modes' tiles are short in k, so their epilogue
 // is a large share of a tile: there the result columns go through shared
-// memory (EPI_COLS columns of each half of the tile at a time) to bulk
-// copies, and the fold moves on while the copies drain.
+// memory (each fold warp stages EPI_COLS columns of its 32 rows at a time)
+// to bulk copies, and the fold moves on while the copies drain.
 constexpr int EPI_COLS = 32;
-constexpr int EPI_BYTES = 2 * EPI_COLS * BM * 4;
+constexpr int EPI_BYTES = FOLD_THREADS / 32 * EPI_COLS * 32 * 4;
 template <int MODE>
 constexpr bool staged_epilogue() { return MODE != kModePlain; }
 
@@ -1081,32 +1081,30 @@ __global__ void __maxnreg__(MAX_REGS)
             }
             if constexpr (staged_epilogue<MODE>()) {
                 if (p.bulk_epi && !part) {
-                    // Each half's four warps write EPI_COLS columns x 128 rows
-                    // to its staging area (a column's rows contiguous, as in
-                    // dst); lane l of the half's first warp then copies column
-                    // l of them to its dst row.  Rows past M are staged but not
-                    // copied.
-                    float *stg = reinterpret_cast<float *>(epi) + half * EPI_COLS * BM;
-                    const bool issuer = quad == 0;
-                    const int64_t mrow0 = static_cast<int64_t>(t.mt) * BM;
-                    const uint32_t bytes =
-                        static_cast<uint32_t>(std::min<int64_t>(BM, p.M - mrow0)) * 4;
+                    // Each warp stages its 32 rows of EPI_COLS columns at a
+                    // time (a column's rows contiguous, as in dst) and lane l
+                    // copies column l's 32 rows to its dst row with a bulk
+                    // copy: the warp needs no other warp, so no barrier.
+                    // Rows past M are staged but not copied.
+                    float *stg =
+                        reinterpret_cast<float *>(epi) + (warp - WARP_FOLD0) * EPI_COLS * 32;
+                    const int64_t mrow0 = static_cast<int64_t>(t.mt) * BM + 32 * quad;
+                    const int64_t nrows = std::min<int64_t>(32, p.M - mrow0);
                     float *dbase = p.dst + mrow0;
                     if constexpr (!GROUPED)
                         dbase += t.slice * p.N * p.M + static_cast<int64_t>(t.nt) * BN * p.M;
 #pragma unroll
                     for (int rd = 0; rd < FOLD_COLS / EPI_COLS; ++rd) {
-                        if (issuer) ptx::bulk_wait_read();   // the last copies left the staging
-                        ptx::named_bar_sync(1 + half, 128);
+                        ptx::bulk_wait_read();              // this lane's last copy left the staging
+                        __syncwarp();
 #pragma unroll
                         for (int pp = 0; pp < EPI_COLS / 16; ++pp) {
                             const int pc = rd * (EPI_COLS / 16) + pp;
                             uint32_t dv[16];
-                            __syncwarp();                   // converged for tcgen05.ld
                             ptx::tmem_ld16_wait(tmem + lane_off + COL_D2 + col0 + pc * 16, dv);
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
-                                stg[(pp * 16 + j) * BM + row] =
+                                stg[(pp * 16 + j) * 32 + lane] =
                                     sreg[pc * 16 + j] + (has_d2 ? __uint_as_float(dv[j]) : 0.f);
                         }
                         if (rd == FOLD_COLS / EPI_COLS - 1) {
@@ -1115,15 +1113,14 @@ __global__ void __maxnreg__(MAX_REGS)
                             ptx::mbar_arrive(&bars->d2free);
                         }
                         ptx::fence_async_shared();
-                        ptx::named_bar_sync(1 + half, 128);
-                        if (issuer) {
-                            const int jc = static_cast<int>(col0) + rd * EPI_COLS + lane;
-                            if (jc < tile_cols) {
-                                const int64_t drow = GROUPED ? (rd == 0 ? rows_lo : rows_hi) : jc;
-                                ptx::bulk_store(dbase + drow * p.M, stg + lane * BM, bytes);
-                            }
-                            ptx::bulk_commit();
+                        __syncwarp();
+                        const int jc = static_cast<int>(col0) + rd * EPI_COLS + lane;
+                        if (jc < tile_cols && nrows > 0) {
+                            const int64_t drow = GROUPED ? (rd == 0 ? rows_lo : rows_hi) : jc;
+                            ptx::bulk_store(dbase + drow * p.M, stg + lane * 32,
+                                            static_cast<uint32_t>(nrows) * 4);
                         }
+                        ptx::bulk_commit();
                     }
                     continue;
                 }
@@ -1175,7 +1172,7 @@ __global__ void __maxnreg__(MAX_REGS)
 
     // the bulk copies of the last epilogue complete before the CTA exits
     if constexpr (staged_epilogue<MODE>()) {
-        if (warp >= WARP_FOLD0 && (warp & 3) == 0) ptx::bulk_wait();
+        if (warp >= WARP_FOLD0) ptx::bulk_wait();
     }
     if (timed_out) record_status(p.status, OOP_ERR_DEVICE_TIMEOUT);
     ptx::tc_fence_before();

@@ -308,10 +308,6 @@ __device__ __forceinline__ void bulk_wait() {
 __device__ __forceinline__ void fence_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// barrier `id` (not 0, which __syncthreads uses) over `n` threads
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 // 32 lanes x 16 consecutive 32-bit columns: thread i writes lane (base + i).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
