@@ -143,7 +143,6 @@ template <int TYPE>
 struct RawA {
     using F = QFormat<TYPE>;
     static constexpr bool PLAIN = F::QK == 1;
-    static constexpr int BLOCK = F::BYTES;
     // Rows whose byte length is not a multiple of 16 cannot be a 2-D TMA
     // map's rows; groups of 16 / gcd(row bytes, 16) of them are, at most RG
     // (RG * BYTES is a multiple of 16), so the map's rows are groups of rows
@@ -516,7 +515,7 @@ __device__ __forceinline__ void staged_half(const uint8_t *slot, int r, uint32_t
         // once; each lane then takes its row's pair by shuffle and adds its
         // own code: one fused multiply-add, the same rounding as decode().
         const int quad = r >> 5;
-        const int bofs = QFormat<TYPE>::QK == 32 ? quad * Raw::BLOCK : 0;
+        const int bofs = QFormat<TYPE>::QK == 32 ? quad * QFormat<TYPE>::BYTES : 0;
         // this warp's bytes of its j-th k row of the block
         auto row_at = [&](int j) -> const uint8_t * {
             if constexpr (AG > 1) {
@@ -546,7 +545,7 @@ __device__ __forceinline__ void staged_half(const uint8_t *slot, int r, uint32_t
             x[j] = fmaf(sj, static_cast<float>(q), oj);
         }
     } else {
-        const uint8_t *blk = rows + off0 + (r >> 5) * Raw::BLOCK;
+        const uint8_t *blk = rows + off0 + (r >> 5) * QFormat<TYPE>::BYTES;
         const float dl = half_bits_to_float(
             *reinterpret_cast<const uint16_t *>(blk + (lane & (KH - 1)) * Raw::ROW_BYTES));
         // d*v two k rows at a time in packed f32x2 arithmetic, exactly: with
@@ -592,7 +591,8 @@ __global__ void __maxnreg__(MAX_REGS)
     constexpr bool GROUPED = MODE == kModeGrouped;
     constexpr bool TMA_A = AG > 0;
     using Raw = RawA<TYPE>;
-    static_assert(AG <= 1 || (Raw::RG % AG == 0 && (BK / AG) * Raw::ROW_BYTES % 128 == 0),
+    constexpr int AGD = AG > 1 ? AG : 1;                 // the group size (1: single rows)
+    static_assert(Raw::RG % AGD == 0 && (BK / AGD) * Raw::ROW_BYTES % 128 == 0,
                   "row groups: a divisor of RG, each box 128-byte aligned");
     constexpr bool HAS_ALO = !is_tf32_exact<TYPE>();   // bf16 / f16 values are TF32 values
     extern __shared__ uint8_t smem_raw[];
@@ -922,9 +922,10 @@ __global__ void __maxnreg__(MAX_REGS)
                 if constexpr (!Raw::PLAIN && TYPE != OOP_TYPE_Q8_0 && TYPE != OOP_TYPE_Q4_0) {
                     // blocks hold whole 32-element groups, so mok is the same
                     // in every lane: a group past M is neither read nor used
+                    using F = QFormat<TYPE>;
                     const uint8_t *row0 = a_slice + k0 * p.a_row_bytes +
                                           raw_tile_byte0<TYPE>(t.mt) +
-                                          (QFormat<TYPE>::QK == 32 ? (r >> 5) * Raw::BLOCK : 0);
+                                          (F::QK == 32 ? (r >> 5) * F::BYTES : 0);
                     const int nk = static_cast<int>(
                         mok ? std::min<int64_t>(KH, std::max<int64_t>(0, p.K - k0)) : 0);
                     global_half<TYPE>(row0, p.a_row_bytes, nk, r >> 5, t.mt & 1, lane, x);
