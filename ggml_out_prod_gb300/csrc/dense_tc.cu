@@ -1390,6 +1390,86 @@ __global__ void __launch_bounds__(256) bsplit_kernel(const float *__restrict__ b
     ptx::griddep_launch_dependents();
 }
 
+// ---- MoE routing (MUL_MAT_ID_BACK and the expert-weight gradient) ----------
+// Both lay the routed slots out sorted by expert in one CTA.  The weight
+// gradient sums over each expert's slots, so there the sort is a stable
+// counting sort: each expert's slots land in ascending slot order, and the
+// order of every such sum is the same in every run.  MUL_MAT_ID_BACK computes
+// every slot's dx row alone, so any order gives the same bits and its slots
+// are placed by atomic cursors (faster).  Shared memory: [E] counts, [E]
+// cursors, then (stable sort) [warps][E] counts of one batch of blockDim slots.
+constexpr int kRouteSmemInts = 232448 / 4;
+
+// Threads of a routing CTA for E experts (its shared memory must hold
+// (2 + warps) * E ints), 0 when E is too large.
+int route_threads(int64_t E) {
+    const int64_t warps = std::min<int64_t>(32, kRouteSmemInts / std::max<int64_t>(E, 1) - 2);
+    return warps >= 1 ? static_cast<int>(warps) * 32 : 0;
+}
+size_t route_smem_bytes(int64_t E, int threads) {
+    return static_cast<size_t>(2 + threads / 32) * static_cast<size_t>(E) * sizeof(int);
+}
+
+// Adds every valid slot's expert to cnt[]; ids are read four batches at a
+// time so that their loads are in flight together.  Returns nothing; a slot
+// whose id is outside [0, E) is passed to bad(s).
+template <typename Bad>
+__device__ __forceinline__ void route_count(const int32_t *__restrict__ ids, int64_t nslot, int E,
+                                            int *cnt, Bad bad) {
+    for (int64_t s0 = threadIdx.x; s0 < nslot; s0 += 4 * static_cast<int64_t>(blockDim.x)) {
+        int e4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t s = s0 + u * static_cast<int64_t>(blockDim.x);
+            e4[u] = s < nslot ? ids[s] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t s = s0 + u * static_cast<int64_t>(blockDim.x);
+            if (s >= nslot) break;
+            if (e4[u] >= 0 && e4[u] < E) atomicAdd(&cnt[e4[u]], 1);
+            else bad(s);
+        }
+    }
+}
+
+// rows[cur[e] + (rank of slot s among expert e's slots)] = s, for every valid
+// slot, in slot order: batches of blockDim slots, ranked inside a warp by
+// __match_any_sync and across warps by the batch's per-warp counts.  cur[]
+// ends past each expert's slots.  Called by the whole CTA.
+__device__ __forceinline__ void route_place(const int32_t *__restrict__ ids, int64_t nslot, int E,
+                                            int *cur, int *wc, int *rows) {
+    const int nw = static_cast<int>(blockDim.x >> 5);
+    const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+    int e_next = threadIdx.x < nslot ? ids[threadIdx.x] : -1;
+    for (int64_t base = 0; base < nslot; base += blockDim.x) {
+        const int64_t s = base + threadIdx.x;
+        const int e = e_next;
+        const int64_t sn = s + blockDim.x;
+        e_next = sn < nslot ? ids[sn] : -1;         // the next batch's id, in flight meanwhile
+        const bool ok = s < nslot && e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        for (int i = static_cast<int>(threadIdx.x); i < nw * E; i += static_cast<int>(blockDim.x))
+            wc[i] = 0;
+        __syncthreads();
+        if (ok && rank == 0) wc[warp * E + e] = __popc(peers);
+        __syncthreads();
+        if (ok) {
+            int pos = cur[e] + rank;
+            for (int w = 0; w < warp; ++w) pos += wc[w * E + e];
+            rows[pos] = static_cast<int>(s);
+        }
+        __syncthreads();
+        for (int x = static_cast<int>(threadIdx.x); x < E; x += static_cast<int>(blockDim.x)) {
+            int t = 0;
+            for (int w = 0; w < nw; ++w) t += wc[w * E + x];
+            cur[x] += t;
+        }
+        __syncthreads();
+    }
+}
+
 // ---- MUL_MAT_ID_BACK as a grouped product ----------------------------------
 // Routing, one CTA: count the slots of each expert, lay them out sorted by
 // expert, build the (expert, n-tile) work list.  A slot with an id outside
@@ -1406,15 +1486,10 @@ __global__ void __launch_bounds__(1024) mmid_route_kernel(const int32_t *__restr
     int *cnt = sh, *cur = sh + E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
-    for (int64_t s = threadIdx.x; s < nslot; s += blockDim.x) {
-        const int e = ids[s];
-        if (e >= 0 && e < E) {
-            atomicAdd(&cnt[e], 1);
-        } else {
-            record_status(status, OOP_ERR_BAD_ID);
-            for (int64_t k = 0; k < Kw; ++k) dx[s * Kw + k] = 0.f;
-        }
-    }
+    route_count(ids, nslot, E, cnt, [&](int64_t s) {
+        record_status(status, OOP_ERR_BAD_ID);
+        for (int64_t k = 0; k < Kw; ++k) dx[s * Kw + k] = 0.f;
+    });
     __syncthreads();
     if (threadIdx.x == 0) {
         int acc = 0, nt = 0;
@@ -1499,16 +1574,12 @@ __global__ void __launch_bounds__(1024) wgrad_route_kernel(const int32_t *__rest
                                                            int64_t rows_max, int *seg_off,
                                                            int *seg_nkb, int *total, int *rows,
                                                            int *status) {
-    extern __shared__ int sh[];                   // [E] counts, then [E] cursors
+    extern __shared__ int sh[];                   // [E] counts, [E] cursors, [warps][E]
     int *cnt = sh, *cur = sh + E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     for (int64_t j = threadIdx.x; j < rows_max; j += blockDim.x) rows[j] = -1;
     __syncthreads();
-    for (int64_t s = threadIdx.x; s < nslot; s += blockDim.x) {
-        const int e = ids[s];
-        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-        else record_status(status, OOP_ERR_BAD_ID);
-    }
+    route_count(ids, nslot, E, cnt, [&](int64_t) { record_status(status, OOP_ERR_BAD_ID); });
     __syncthreads();
     if (threadIdx.x == 0) {
         int acc = 0;
@@ -1522,10 +1593,7 @@ __global__ void __launch_bounds__(1024) wgrad_route_kernel(const int32_t *__rest
         *total = acc;
     }
     __syncthreads();
-    for (int64_t s = threadIdx.x; s < nslot; s += blockDim.x) {
-        const int e = ids[s];
-        if (e >= 0 && e < E) rows[atomicAdd(&cur[e], 1)] = static_cast<int>(s);
-    }
+    route_place(ids, nslot, E, cur, sh + 2 * E, rows);
 }
 
 // Sorted slot j (one per CTA) -> xg[j][0..K) = x[., i % n_x, t] of slot
@@ -2079,11 +2147,16 @@ cudaError_t launch_mmid_wgrad(const float *x, const int32_t *ids, const float *d
     uint32_t *bhi = reinterpret_cast<uint32_t *>(ws + t.off_bhi);
     uint32_t *blo = reinterpret_cast<uint32_t *>(ws + t.off_blo);
 
-    const size_t route_smem = 2 * sizeof(int) * static_cast<size_t>(s.E);
-    if (route_smem > 48 * 1024) return cudaErrorInvalidConfiguration;
-    wgrad_route_kernel<<<1, 1024, route_smem, stream>>>(ids, t.nslot, static_cast<int>(s.E),
-                                                         t.rows_max, seg_off, seg_nkb, total,
-                                                         rows, status);
+    const int route_thr = route_threads(s.E);
+    const size_t route_smem = route_smem_bytes(s.E, route_thr);
+    if (route_thr == 0) return cudaErrorInvalidConfiguration;
+    if (route_smem > 48 * 1024 &&
+        cudaFuncSetAttribute(wgrad_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(route_smem)) != cudaSuccess)
+        return cudaErrorInvalidConfiguration;
+    wgrad_route_kernel<<<1, route_thr, route_smem, stream>>>(ids, t.nslot, static_cast<int>(s.E),
+                                                              t.rows_max, seg_off, seg_nkb, total,
+                                                              rows, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++g_kernel_launches;

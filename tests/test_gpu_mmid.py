@@ -213,6 +213,21 @@ def test_expert_weight_grad_whole(op, orc, K, N, E, n_used, n_x, T):
         assert_parity(got, ref["f64"], ref["abs"], f"expert weight grad {K}x{N}x{E} {sched}")
 
 
+def test_expert_weight_grad_repeatable(op, orc):
+    """The routing lays each expert's slots out in slot order, so every sum
+    over an expert's slots runs in one order: repeated calls give the same
+    bits.  2400 slots (three routing batches), ~300 slots an expert."""
+    K, N, E, n_used, n_x, T = 256, 96, 8, 4, 2, 600
+    x, ids, dy = _wgrad_inputs(198, K, N, E, n_used, n_x, T)
+    first = _wgrad(op, x, ids, dy, E).cpu().numpy()
+    assert op.device_status() == 0
+    for _ in range(3):
+        again = _wgrad(op, x, ids, dy, E).cpu().numpy()
+        assert np.array_equal(first.view(np.uint32), again.view(np.uint32))
+    ref = orc.mul_mat_id_weight_grad(x, ids, dy, E)
+    assert_parity(first, ref["f64"], ref["abs"], "expert weight grad repeatable")
+
+
 def test_expert_weight_grad_skewed(op, orc):
     """Most slots routed to one expert (a segment of many k-blocks next to
     segments of one)."""
